@@ -1,0 +1,193 @@
+"""Block tables, free list, reference counts and copy-on-write, on the host.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The rules, as the pages state them:
+
+* [note] 关键设计 2 ("Block table 与按需分配"), [guide] 03: each sequence has a
+  list of logical blocks; each records its physical block id and how many of
+  its token slots are filled.  Prefill takes just enough blocks for the
+  prompt; each decode token goes to the last block, and a new physical block
+  is taken only once the last one is full, so at most one block per sequence
+  is partly filled (0 <= tail waste < B tokens).
+* [lecture] PagedAttention 原理: the worked example -- a 7-token prompt with B=4
+  fills logical block 0 (4 tokens) and logical block 1 (3 tokens + 1 free
+  slot); "fathers" fills block 1; "brought" goes to a newly taken block 2.
+* [note] 关键设计 3 ("共享、引用计数与写时复制"), [guide] 04 step 4, [lecture]
+  Parallel Sampling 场景: a physical block shared by several logical blocks
+  carries a reference count.  A sequence about to write into a shared block
+  (count > 1) takes a new block, has the old content copied into it, lowers
+  the old block's count by one and points its logical block at the copy; a
+  block whose count is 1 is written in place.
+* [guide] 04 (shared prefix): the provider stores a prefix's blocks ahead of
+  time; a request maps its first logical blocks onto them, the last one
+  marked copy-on-write.
+* [lecture] Beam Search 场景 / [note] 失败案例 4: sharing is driven by three
+  actions, fork, append and free; freeing returns blocks whose count drops
+  to zero.
+
+Readings where the pages are silent or garbled (each test pins one):
+
+* The order in which a full last block and a shared last block are checked:
+  a full block is never written again, so fullness is checked first and a
+  full shared block needs no copy.  After taking a new block for a full last
+  block, the token is written to the new block (the page's listing keeps
+  using the old block's fill counter; the prose says the new token goes to
+  the new block).
+* Newly taken blocks start with reference count 1.
+* The free list is a FIFO over a caller-given order of physical ids: taking
+  pops the front, a freed block is pushed at the back (in logical order when
+  a whole sequence is freed).
+* A registered prefix holds one reference on each of its blocks, so a request
+  that writes into a partly filled last prefix block always copies it.
+* Running out of blocks raises ``MemoryError`` and changes nothing.
+* slot = physical id * B + row.
+"""
+from __future__ import annotations
+
+from collections import deque
+from typing import Dict, List, Optional, Sequence, Tuple
+
+
+class LogicalBlock:
+    __slots__ = ("physical", "filled")
+
+    def __init__(self, physical: int, filled: int):
+        self.physical = physical
+        self.filled = filled
+
+
+class BlockManager:
+    def __init__(self, num_blocks: int, block_size: int, free_order: Optional[Sequence[int]] = None):
+        if num_blocks <= 0 or block_size <= 0:
+            raise ValueError("num_blocks and block_size must be positive")
+        order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise ValueError("free_order must be a permutation of 0..num_blocks-1")
+        self.B = block_size
+        self.num_blocks = num_blocks
+        self.free_list = deque(order)
+        self.ref = [0] * num_blocks
+        self.seqs: Dict[int, List[LogicalBlock]] = {}
+        self.prefixes: Dict[int, List[LogicalBlock]] = {}
+        self.cow_copies = 0
+
+    # -- physical blocks -------------------------------------------------
+    def _take(self) -> int:
+        block = self.free_list.popleft()
+        self.ref[block] = 1
+        return block
+
+    def _release(self, block: int) -> None:
+        self.ref[block] -= 1
+        if self.ref[block] < 0:
+            raise RuntimeError(f"reference count of block {block} went negative")
+        if self.ref[block] == 0:
+            self.free_list.append(block)
+
+    def _need(self, n: int) -> None:
+        if n > len(self.free_list):
+            raise MemoryError(f"need {n} free blocks, have {len(self.free_list)}")
+
+    def _fresh_blocks(self, num_tokens: int) -> List[LogicalBlock]:
+        n = -(-num_tokens // self.B)
+        self._need(n)
+        blocks = []
+        for j in range(n):
+            blocks.append(LogicalBlock(self._take(), min(self.B, num_tokens - j * self.B)))
+        return blocks
+
+    def _slots(self, blocks: List[LogicalBlock]) -> List[int]:
+        return [b.physical * self.B + r for b in blocks for r in range(b.filled)]
+
+    # -- sequences -------------------------------------------------------
+    def add_seq(self, seq_id: int, prompt_len: int) -> List[int]:
+        """Prefill: take ceil(prompt_len / B) blocks; return the prompt tokens' slots."""
+        if seq_id in self.seqs:
+            raise ValueError(f"sequence {seq_id} exists")
+        if prompt_len <= 0:
+            raise ValueError("prompt_len must be positive")
+        blocks = self._fresh_blocks(prompt_len)
+        self.seqs[seq_id] = blocks
+        return self._slots(blocks)
+
+    def fork(self, parent: int, child: int) -> None:
+        """The child maps every logical block onto the parent's physical block."""
+        if child in self.seqs:
+            raise ValueError(f"sequence {child} exists")
+        src = self.seqs[parent]
+        for b in src:
+            self.ref[b.physical] += 1
+        self.seqs[child] = [LogicalBlock(b.physical, b.filled) for b in src]
+
+    def append_slot(self, seq_id: int) -> Tuple[int, int, int]:
+        """Find the slot of the sequence's next token.
+
+        Returns (slot, copy_src, copy_dst); copy_src = copy_dst = -1 unless the
+        write needed a copy of a shared block first.
+        """
+        blocks = self.seqs[seq_id]
+        last = blocks[-1]
+        src = dst = -1
+        if last.filled == self.B:
+            # full: the token starts a new logical block on a newly taken physical block
+            self._need(1)
+            last = LogicalBlock(self._take(), 0)
+            blocks.append(last)
+        elif self.ref[last.physical] > 1:
+            # shared and partly filled: copy it, move this sequence onto the copy
+            self._need(1)
+            new = self._take()
+            src, dst = last.physical, new
+            self.ref[last.physical] -= 1
+            last.physical = new
+            self.cow_copies += 1
+        slot = last.physical * self.B + last.filled
+        last.filled += 1
+        return slot, src, dst
+
+    def free(self, seq_id: int) -> None:
+        for b in self.seqs.pop(seq_id):
+            self._release(b.physical)
+
+    # -- provider-stored prefixes -----------------------------------------
+    def register_prefix(self, prefix_id: int, length: int) -> List[int]:
+        """Take and hold blocks for a prefix; return its tokens' slots (to be filled once)."""
+        if prefix_id in self.prefixes:
+            raise ValueError(f"prefix {prefix_id} exists")
+        if length <= 0:
+            raise ValueError("length must be positive")
+        blocks = self._fresh_blocks(length)
+        self.prefixes[prefix_id] = blocks
+        return self._slots(blocks)
+
+    def add_seq_with_prefix(self, seq_id: int, prefix_id: int) -> None:
+        """A request whose first logical blocks are the prefix's physical blocks."""
+        if seq_id in self.seqs:
+            raise ValueError(f"sequence {seq_id} exists")
+        src = self.prefixes[prefix_id]
+        for b in src:
+            self.ref[b.physical] += 1
+        self.seqs[seq_id] = [LogicalBlock(b.physical, b.filled) for b in src]
+
+    def drop_prefix(self, prefix_id: int) -> None:
+        for b in self.prefixes.pop(prefix_id):
+            self._release(b.physical)
+
+    # -- views -------------------------------------------------------------
+    def block_table(self, seq_id: int) -> Tuple[List[int], int]:
+        blocks = self.seqs[seq_id]
+        return [b.physical for b in blocks], sum(b.filled for b in blocks)
+
+    def filled(self, seq_id: int) -> List[int]:
+        return [b.filled for b in self.seqs[seq_id]]
+
+    def ref_count(self, block: int) -> int:
+        return self.ref[block]
+
+    def num_free(self) -> int:
+        return len(self.free_list)
+
+    def tail_waste_tokens(self) -> int:
+        """Sum over sequences of the unfilled slots of their blocks."""
+        return sum(self.B * len(bl) - sum(b.filled for b in bl) for bl in self.seqs.values())

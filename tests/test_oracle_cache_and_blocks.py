@@ -1,0 +1,288 @@
+"""Pins for the cache-op, size and block-manager oracles.
+
+The block-manager pins are the pages' own worked examples (stored under
+tests/golden/ with their citations) plus the invariants the pages state:
+at most one partly filled block per sequence, reference counts, n-1 copies
+when n sequences share a partly filled block, and the physical-block count
+under sharing.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import block_manager as obm
+from oracle import cache_ops as oc
+from oracle import sizes
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "block_manager_examples.json")
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _free_order(n, head):
+    rest = [b for b in range(n) if b not in head]
+    return list(head) + rest
+
+
+# ---- sizes --------------------------------------------------------------------------------
+
+def test_kv_bytes_per_token_matches_page():
+    g = _golden()["kv_size"]
+    heads, head_dim = 40, 128
+    assert heads * head_dim == g["hidden"]
+    per_token = sizes.kv_bytes_per_token(g["num_layers"], heads, head_dim, g["dtype_bytes"])
+    assert per_token == 2 * 5120 * 40 * 2 == 819200
+    assert 780_000 <= per_token <= 820_000                          # "about 800 KB"
+    req = per_token * g["max_tokens"]
+    assert 1.55e9 <= req <= 1.75e9                                   # "about 1.6 GB"
+
+
+def test_block_bytes():
+    assert sizes.kv_bytes_per_block(40, 128, 16) * 2 == 16 * sizes.kv_bytes_per_token(1, 40, 128)
+
+
+# ---- cache ops ----------------------------------------------------------------------------
+
+def test_reshape_and_cache_places_rows_and_skips_padding():
+    rng = np.random.default_rng(1)
+    N, H, B, D, T = 6, 3, 4, 8, 7
+    k = rng.standard_normal((N, H, B, D)).astype(np.float16)
+    v = rng.standard_normal((N, H, B, D)).astype(np.float16)
+    k0, v0 = k.copy(), v.copy()
+    key = rng.standard_normal((T, H, D)).astype(np.float16)
+    val = rng.standard_normal((T, H, D)).astype(np.float16)
+    slots = [5, -1, 0, 23, 13, -7, 8]
+    oc.reshape_and_cache(key, val, k, v, slots)
+    # read back through the flat-slot view: pool[n, h, r, :] is slot n*B + r of head h
+    flat_k = k.transpose(1, 0, 2, 3).reshape(H, N * B, D)
+    flat_v = v.transpose(1, 0, 2, 3).reshape(H, N * B, D)
+    written = set()
+    for t, s in enumerate(slots):
+        if s >= 0:
+            np.testing.assert_array_equal(flat_k[:, s], key[t])
+            np.testing.assert_array_equal(flat_v[:, s], val[t])
+            written.add(s)
+    untouched = [s for s in range(N * B) if s not in written]
+    f0k = k0.transpose(1, 0, 2, 3).reshape(H, N * B, D)
+    np.testing.assert_array_equal(flat_k[:, untouched], f0k[:, untouched])
+
+
+def test_copy_blocks_copies_every_layer_and_nothing_else():
+    rng = np.random.default_rng(2)
+    L, N, H, B, D = 3, 8, 2, 4, 8
+    ks = [rng.standard_normal((N, H, B, D)).astype(np.float16) for _ in range(L)]
+    vs = [rng.standard_normal((N, H, B, D)).astype(np.float16) for _ in range(L)]
+    before_k = [x.copy() for x in ks]
+    before_v = [x.copy() for x in vs]
+    pairs = [(1, 5), (2, 7), (0, 3)]
+    oc.copy_blocks(ks, vs, pairs)
+    for layer in range(L):
+        for src, dst in pairs:
+            np.testing.assert_array_equal(ks[layer][dst], before_k[layer][src])
+            np.testing.assert_array_equal(vs[layer][dst], before_v[layer][src])
+        for b in (0, 1, 2, 4, 6):
+            np.testing.assert_array_equal(ks[layer][b], before_k[layer][b])
+            np.testing.assert_array_equal(vs[layer][b], before_v[layer][b])
+
+
+# ---- block manager: the pages' worked examples --------------------------------------------
+
+def test_single_request_walkthrough():
+    g = _golden()["single_request"]
+    B = g["block_size"]
+    bm = obm.BlockManager(16, B, _free_order(16, g["free_order_head"]))
+    slots = bm.add_seq(0, len(g["prompt"]))
+    table, ctx = bm.block_table(0)
+    assert len(table) == g["after_prefill"]["num_logical_blocks"]
+    assert bm.filled(0) == g["after_prefill"]["filled"]
+    assert table == g["after_prefill"]["table"]
+    assert table[0] == 7                                              # logical 0 -> physical 7
+    assert slots == [7 * B + r for r in range(4)] + [1 * B + r for r in range(3)]
+    for step in g["decode"]:
+        slot, src, dst = bm.append_slot(0)
+        assert (src, dst) == (-1, -1)
+        assert bm.filled(0) == step["filled"]
+        assert len(bm.block_table(0)[0]) == step["num_logical_blocks"]
+    # "fathers" went to the reserved slot of block 1, "brought" to row 0 of the new block
+    table, ctx = bm.block_table(0)
+    assert ctx == 9 and table[2] == 3 and slot == 3 * B
+
+
+def test_parallel_sampling_copy_on_write():
+    g = _golden()["parallel_sampling"]
+    B = g["block_size"]
+    bm = obm.BlockManager(16, B, _free_order(16, g["free_order_head"]))
+    bm.add_seq(1, g["prompt_len"])                                    # A1
+    bm.fork(1, 2)                                                     # A2 shares A1's blocks
+    assert bm.block_table(1)[0] == g["after_prefill"]["A1"]
+    assert bm.block_table(2)[0] == g["after_prefill"]["A2"]
+    for b, r in g["after_prefill"]["ref"].items():
+        assert bm.ref_count(int(b)) == r
+    slot, src, dst = bm.append_slot(1)                                # A1 writes "fathers"
+    step = g["A1_writes_first"]
+    assert [src, dst] == step["copy"]
+    assert bm.block_table(1)[0] == step["A1"] and bm.block_table(2)[0] == step["A2"]
+    for b, r in step["ref"].items():
+        assert bm.ref_count(int(b)) == r
+    assert slot == 3 * B + 3
+    slot, src, dst = bm.append_slot(2)                                # A2 writes "mothers" in place
+    assert (src, dst) == (-1, -1) and g["A2_writes_next"]["copy"] is None
+    assert bm.block_table(2)[0] == g["A2_writes_next"]["A2"] and slot == 1 * B + 3
+
+
+# ---- block manager: invariants the pages state ---------------------------------------------
+
+def _random_ops(bm, rng, steps, max_prompt=40):
+    live = []
+    next_id = 0
+    copies = []
+    for _ in range(steps):
+        op = rng.integers(0, 10)
+        try:
+            if op < 2 or not live:
+                bm.add_seq(next_id, int(rng.integers(1, max_prompt)))
+                live.append(next_id)
+                next_id += 1
+            elif op < 3:
+                bm.fork(int(rng.choice(live)), next_id)
+                live.append(next_id)
+                next_id += 1
+            elif op < 4 and len(live) > 1:
+                s = int(rng.choice(live))
+                bm.free(s)
+                live.remove(s)
+            else:
+                s = int(rng.choice(live))
+                slot, src, dst = bm.append_slot(s)
+                if src >= 0:
+                    copies.append((src, dst))
+        except MemoryError:
+            pass
+    return live, copies
+
+
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_at_most_one_partial_block_and_counts_consistent(B):
+    rng = np.random.default_rng(B)
+    bm = obm.BlockManager(200, B, rng.permutation(200))
+    live, _ = _random_ops(bm, rng, 600)
+    refs = np.zeros(200, dtype=int)
+    for s in live:
+        table, ctx = bm.block_table(s)
+        filled = bm.filled(s)
+        assert all(f == B for f in filled[:-1]) and 1 <= filled[-1] <= B   # one partial block at most
+        assert 0 <= B * len(table) - ctx < B                                 # 0 <= tail waste < B
+        for b in table:
+            refs[b] += 1
+    for b in range(200):
+        assert bm.ref_count(b) == refs[b]
+    assert bm.num_free() == int((refs == 0).sum())
+
+
+def test_n_sharers_of_a_partial_block_make_n_minus_1_copies():
+    B, n = 16, 4
+    bm = obm.BlockManager(64, B)
+    bm.add_seq(0, 511)                                 # 31 full blocks + one 15-token block
+    for i in range(1, n):
+        bm.fork(0, i)
+    last = bm.block_table(0)[0][-1]
+    copies = [bm.append_slot(i)[1:] for i in range(n)]
+    made = [c for c in copies if c[0] >= 0]
+    assert len(made) == n - 1 and all(c[0] == last for c in made)
+    assert bm.ref_count(last) == 1 and copies[-1] == (-1, -1)
+
+
+def test_full_shared_last_block_needs_no_copy():
+    bm = obm.BlockManager(64, 16)
+    bm.add_seq(0, 512)
+    for i in range(1, 4):
+        bm.fork(0, i)
+    assert all(bm.append_slot(i)[1] == -1 for i in range(4))
+    assert bm.cow_copies == 0
+
+
+def test_physical_block_count_under_sharing():
+    # N_physical = sum_r ceil(L_r / B) - (references saved by sharing)
+    B, prompts, n = 16, 5, 4
+    rng = np.random.default_rng(4)
+    bm = obm.BlockManager(4096, B, rng.permutation(4096))
+    lens = {}
+    sid = 0
+    for p in range(prompts):
+        base = sid
+        bm.add_seq(base, 512)
+        for i in range(1, n):
+            bm.fork(base, base + i)
+        for i in range(n):
+            for _ in range(int(rng.integers(1, 257))):
+                bm.append_slot(base + i)
+        sid += n
+    total_logical = 0
+    saved = 0
+    for s in range(sid):
+        table, ctx = bm.block_table(s)
+        assert len(table) == -(-ctx // B)
+        total_logical += len(table)
+    for b in range(4096):
+        if bm.ref_count(b) > 1:
+            saved += bm.ref_count(b) - 1
+    assert 4096 - bm.num_free() == total_logical - saved
+    assert saved == prompts * (n - 1) * 32
+
+
+def test_shared_prefix_last_block_is_copy_on_write():
+    B = 16
+    bm = obm.BlockManager(256, B)
+    pre_slots = bm.register_prefix(9, 40)                  # 2 full blocks + 8 tokens
+    assert len(pre_slots) == 40
+    table_p = [s // B for s in pre_slots[::B]]
+    bm.add_seq_with_prefix(1, 9)
+    bm.add_seq_with_prefix(2, 9)
+    assert bm.ref_count(table_p[2]) == 3
+    slot, src, dst = bm.append_slot(1)
+    assert src == table_p[2] and dst >= 0 and slot == dst * B + 8
+    slot, src, dst = bm.append_slot(2)
+    assert src == table_p[2]                                # the provider still holds the original
+    assert bm.ref_count(table_p[2]) == 1
+    bm.free(1)
+    bm.free(2)
+    bm.drop_prefix(9)
+    assert bm.num_free() == 256
+
+
+def test_full_prefix_blocks_shared_without_copy():
+    bm = obm.BlockManager(256, 16)
+    bm.register_prefix(0, 1024)
+    for s in range(8):
+        bm.add_seq_with_prefix(s, 0)
+        bm.append_slot(s)
+    assert bm.cow_copies == 0 and bm.num_free() == 256 - 64 - 8
+
+
+def test_out_of_blocks_changes_nothing():
+    bm = obm.BlockManager(4, 4)
+    bm.add_seq(0, 13)                                       # 4 blocks
+    with pytest.raises(MemoryError):
+        bm.add_seq(1, 1)
+    assert 1 not in bm.seqs
+    bm.fork(0, 1)
+    with pytest.raises(MemoryError):
+        bm.append_slot(1)                                   # needs a copy of the shared 1-token block
+    assert bm.block_table(1)[0] == bm.block_table(0)[0] and bm.filled(1)[-1] == 1
+
+
+def test_free_returns_blocks_only_when_unreferenced():
+    bm = obm.BlockManager(32, 4, list(range(32)))
+    bm.add_seq(0, 8)                                        # blocks 0, 1
+    bm.fork(0, 1)
+    bm.append_slot(1)                                       # full -> new block 2 for seq 1
+    bm.free(0)
+    assert bm.num_free() == 29 and bm.ref_count(0) == 1
+    bm.free(1)
+    assert bm.num_free() == 32
+    assert list(bm.free_list)[-3:] == [0, 1, 2]              # FIFO: freed blocks go to the back
