@@ -1,0 +1,226 @@
+/*
+ * pkv.h -- C ABI of the paged K/V-cache decode path (libpkv.so), sm_103a.
+ *
+ * Sources, cited by page title and section:
+ *   [note]    "vLLM / PagedAttention -- 把 LLM 服务的瓶颈从显存碎片里救出来"
+ *             (awesome.papernotes.org, 2023_vllm)
+ *   [lecture] "vLLM" lecture notes (formulaic.cloudchewie.com, 5-vllm)
+ *   [guide]   "vLLM / PagedAttention (SOSP 2023)" (upskillscore.com system-design guide)
+ *
+ * Conventions for every entry point:
+ *   - fp16 tensors are passed as uint16_t bit patterns (IEEE binary16).
+ *   - "device" pointers point into memory of the current CUDA device; "host"
+ *     pointers into ordinary host memory.  The caller owns every buffer and the
+ *     stream; the library never allocates device memory, never frees caller
+ *     memory and keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work is
+ *     asynchronous on it; arguments are validated on the host first.
+ *   - Return value: PKV_OK or a negative pkv_status; pkv_last_error() gives a
+ *     message (thread-local) for the last failing call.  No exception crosses
+ *     the ABI.
+ *   - Kernels check every block id, slot and context length they read against
+ *     the sizes passed in; a bad value is skipped (never dereferenced) and its
+ *     code is recorded in a per-device error word that pkv_device_error reads.
+ *
+ * K/V pool layout (the pages leave it open; [note] 关键设计 5 asks only for "a
+ * layout suited to block reads"): each layer has a K pool and a V pool, each
+ * [num_blocks, num_heads, block_size, head_dim] fp16, row-major.  Token slot
+ * `slot` is row slot % block_size of physical block slot / block_size, so one
+ * (block, head) tile of a pool is block_size*head_dim*2 contiguous bytes.
+ *
+ * Supported shapes: head_dim in {64, 128}, block_size in {8, 16, 32}, one K/V
+ * head per query head.  Other values return PKV_ERR_UNSUPPORTED.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1,   /* bad pointer, size, alignment or id */
+  PKV_ERR_UNSUPPORTED = -2,   /* a shape outside the supported set */
+  PKV_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+  PKV_ERR_WORKSPACE = -4,     /* workspace missing or too small */
+  PKV_ERR_OOM = -5,           /* block manager: not enough free blocks (state unchanged) */
+  PKV_ERR_DEVICE_CHECK = -6,  /* a kernel met an out-of-range id, slot or length */
+  PKV_ERR_NOT_FOUND = -7      /* block manager: unknown sequence or prefix id */
+} pkv_status;
+
+/* Device-side check codes recorded by the kernels (first one wins). */
+enum {
+  PKV_DEV_OK = 0,
+  PKV_DEV_BAD_BLOCK_ID = 1,     /* a block table entry outside [0, num_blocks) */
+  PKV_DEV_BAD_CONTEXT_LEN = 2,  /* a context length < 0 or > max_blocks_per_seq*block_size */
+  PKV_DEV_BAD_SLOT = 3,         /* a slot >= num_blocks*block_size */
+  PKV_DEV_BAD_COPY_PAIR = 4,    /* a copy pair with an id outside [0, num_blocks) */
+  PKV_DEV_WAIT_TIMEOUT = 5      /* a shared-memory copy did not complete in time */
+};
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* ABI version (major*100 + minor). */
+int pkv_version(void);
+
+/*
+ * Synchronises `stream`, then returns PKV_OK if no kernel of this library on the
+ * current device recorded a check failure, else PKV_ERR_DEVICE_CHECK with the
+ * first recorded PKV_DEV_* code in *code (may be NULL).  reset != 0 clears the
+ * recorded code.
+ */
+int pkv_device_error(void* stream, int reset, int* code);
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention ([note] 关键设计 1, both equations; 关键设计 5, "fusing
+ * block read and attention").
+ *
+ * For every sequence s < num_seqs and head h < num_heads:
+ *   out[s,h,:] = sum_{t < ctx_s} softmax_t(scale * q[s,h,:] . k_t) v_t
+ * with k_t = k_cache[block_tables[s, t / B], h, t % B, :] (v_t likewise) and
+ * ctx_s = context_lens[s].  The softmax normalises over all ctx_s tokens.
+ * ctx_s = 0 gives a zero row.  Table entries at column >= ceil(ctx_s / B) are
+ * never read.  Accumulation is fp32; out is rounded to nearest even.
+ *
+ *   q            device [num_seqs, num_heads, head_dim] fp16, 16-byte aligned
+ *   k_cache,
+ *   v_cache      device [num_blocks, num_heads, block_size, head_dim] fp16,
+ *                16-byte aligned
+ *   block_tables device [num_seqs, max_blocks_per_seq] int32 physical ids
+ *   context_lens device [num_seqs] int32
+ *   out          device [num_seqs, num_heads, head_dim] fp16, 16-byte aligned;
+ *                must not overlap the inputs
+ *   workspace    device scratch for the split over the context (partial
+ *                max / sum / output per partition); at least
+ *                pkv_paged_attention_workspace_size(...) bytes, 16-byte aligned.
+ *                May be NULL when that size is 0.  Contents need no
+ *                initialisation and are garbage afterwards.  Calls that share a
+ *                workspace must be ordered on one stream.
+ *
+ * Returns PKV_ERR_WORKSPACE if the workspace is needed and missing or small.
+ * ------------------------------------------------------------------------- */
+size_t pkv_paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                          int max_blocks_per_seq, int block_size);
+
+int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int num_seqs, int num_heads, int head_dim, int num_blocks,
+                               int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Reshape and cache ([note] 关键设计 5, "fused reshape and block write").
+ *
+ * For every token t < num_tokens with slot = slot_mapping[t] >= 0:
+ *   k_cache[slot / B, h, slot % B, :] = key[t, h, :]   for all h  (value likewise)
+ * A negative slot marks a padding token and is skipped.  Bit-exact copy.
+ *
+ *   key, value   device [num_tokens, num_heads, head_dim] fp16, contiguous,
+ *                16-byte aligned
+ *   k_cache,
+ *   v_cache      device pools as above
+ *   slot_mapping device [num_tokens] int64
+ * Two tokens with the same slot race (one of them wins).
+ * ------------------------------------------------------------------------- */
+int pkv_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* k_cache,
+                          uint16_t* v_cache, const int64_t* slot_mapping, int num_tokens,
+                          int num_heads, int head_dim, int block_size, int num_blocks, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Batched block copy ([note] 关键设计 3 copy-on-write; 关键设计 5, "fused block
+ * copy": many small block copies in one kernel instead of one memcpy each).
+ *
+ * For every pair p < num_pairs and every layer l < num_layers:
+ *   k_caches[l][dst_p] = k_caches[l][src_p]; v_caches[l][dst_p] = v_caches[l][src_p]
+ * with (src_p, dst_p) = (block_mapping[2p], block_mapping[2p+1]); whole blocks,
+ * all heads and rows.  Bit-exact.  A destination must not be the source or
+ * destination of another pair in the same call.
+ *
+ *   k_caches,
+ *   v_caches      HOST arrays of num_layers device pool pointers (16-byte aligned)
+ *   block_mapping device [num_pairs, 2] int64
+ * ------------------------------------------------------------------------- */
+int pkv_copy_blocks(uint16_t* const* k_caches, uint16_t* const* v_caches, int num_layers,
+                    const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
+                    int block_size, int num_blocks, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager ([note] 关键设计 2 and 3; [lecture] PagedAttention 原理 and
+ * Parallel Sampling 场景; [guide] 03 and 04).  No device memory, no CUDA.
+ *
+ * Each sequence owns a list of logical blocks; each logical block records a
+ * physical block id and how many of its B slots are filled.  Physical blocks
+ * carry reference counts.  Rules:
+ *   - prefill takes ceil(len / B) blocks; tokens fill blocks left to right;
+ *   - append: if the last block is full, take a new block and write there;
+ *     else if the last block's count is > 1, take a new block, report the
+ *     copy (old -> new) the caller must run with pkv_copy_blocks before the
+ *     write, decrement the old count and move the sequence onto the copy;
+ *     else write in place;
+ *   - fork: the child maps every logical block onto the parent's physical
+ *     blocks (counts +1); free: counts -1, blocks reaching 0 return to the
+ *     free list;
+ *   - a registered prefix holds one reference on each of its blocks; a
+ *     sequence added on a prefix maps its first logical blocks onto them.
+ * The free list is FIFO over `free_order`: taking pops the front, a freed
+ * block is pushed at the back.  slot = physical id * B + row.
+ * Every call is all-or-nothing: PKV_ERR_OOM (and every other error) leaves
+ * the state unchanged.  An instance is not thread-safe.
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_bm pkv_bm;
+
+/* free_order: host [num_blocks] permutation of 0..num_blocks-1, or NULL for
+ * 0,1,2,...  Returns NULL on bad arguments (see pkv_last_error). */
+pkv_bm* pkv_bm_create(int num_blocks, int block_size, const int32_t* free_order);
+void pkv_bm_destroy(pkv_bm* bm);
+
+/* Prefill a new sequence of prompt_len >= 1 tokens.  slots_out: host
+ * [prompt_len] or NULL; receives the prompt tokens' slots. */
+int pkv_bm_add_seq(pkv_bm* bm, int64_t seq_id, int prompt_len, int64_t* slots_out);
+
+/* The child shares all of the parent's blocks. */
+int pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child);
+
+/* Slot for the sequence's next token.  *cow_src / *cow_dst receive the block
+ * copy to run first, or -1 / -1. */
+int pkv_bm_append_slot(pkv_bm* bm, int64_t seq_id, int64_t* slot, int32_t* cow_src, int32_t* cow_dst);
+
+/* One append for each of n distinct sequences, in order, all-or-nothing.
+ * slots_out host [n]; cow_pairs_out host [n, 2] int64 receives the copies
+ * (src, dst), *num_cow their number. */
+int pkv_bm_append_slots(pkv_bm* bm, const int64_t* seq_ids, int n, int64_t* slots_out,
+                        int64_t* cow_pairs_out, int* num_cow);
+
+int pkv_bm_free(pkv_bm* bm, int64_t seq_id);
+
+/* A provider-stored prefix of len >= 1 tokens ([guide] 04); slots_out as in
+ * pkv_bm_add_seq. */
+int pkv_bm_register_prefix(pkv_bm* bm, int64_t prefix_id, int len, int64_t* slots_out);
+int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id);
+int pkv_bm_drop_prefix(pkv_bm* bm, int64_t prefix_id);
+
+/* One sequence's physical ids (host out[cap]), block count and token count. */
+int pkv_bm_block_table(const pkv_bm* bm, int64_t seq_id, int32_t* out, int cap, int* n_blocks,
+                       int* ctx_len);
+
+/* Padded tables for a batch: tables_out host [n, max_blocks] int32 (-1 past
+ * each sequence's blocks), ctx_lens_out host [n] int32. */
+int pkv_bm_block_tables(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* tables_out,
+                        int max_blocks, int32_t* ctx_lens_out);
+
+/* Reference count of a physical block (negative status on a bad id). */
+int pkv_bm_ref_count(const pkv_bm* bm, int32_t block);
+
+/* Free blocks, unfilled slots summed over sequences, copies reported so far. */
+int pkv_bm_stats(const pkv_bm* bm, int* free_blocks, int64_t* tail_waste_tokens, int64_t* cow_copies);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,590 @@
+// Paged decode attention for sm_103a: one query per (sequence, head), K/V read
+// block by block through the sequence's block table.
+//
+// What is computed ([note] "vLLM / PagedAttention -- 把 LLM 服务的瓶颈从显存碎片里救出来",
+// section 关键设计 1, both equations): o = sum_t softmax_t(scale * q.k_t) v_t over
+// the sequence's ctx tokens, where token t sits in physical block
+// table[t / B] at row t % B.  Section 关键设计 5 ("fusing block read and
+// attention") has the kernel read the blocks itself, a warp per block.
+//
+// GB300 design (decode attention is a batched GEMV: ~1 flop per byte, so HBM
+// bandwidth is the roofline and no tensor cores are used):
+//  * The context is split into partitions of `part_tokens` tokens; one CTA
+//    handles one (partition, head, sequence).  A second tiny kernel merges the
+//    partitions of a (sequence, head) with the log-sum-exp identity
+//    m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p 2^(m_p - m) / l.
+//  * The unit of work is a chunk of R = min(B, 16) rows of one (block, head)
+//    tile: R*D*2 contiguous bytes of K and as many of V.  Each warp owns a ring
+//    of NST shared-memory stages; lane 0 fills a stage with two 1-D bulk async
+//    copies (cp.async.bulk global->shared, completion counted in bytes on an
+//    mbarrier), so a warp keeps NST chunks in flight while it computes.
+//  * q.k: lane l holds 8 q values (16-byte column l % (D/8)) pre-multiplied by
+//    scale*log2(e); partial dots of the rows it loaded are summed across the
+//    D/8 lanes of a row with a transposing butterfly (R/2 + 1 .. shuffles per
+//    chunk instead of one 4-step reduction per row).
+//  * Online softmax in base 2 (exp2f), fp32 accumulators in registers; rows
+//    past the context are excluded by select/branch, never multiplied by zero,
+//    so stale NaN/Inf in unfilled slots cannot leak into the result.
+//  * Every wait is bounded by a global-timer deadline; on expiry the kernel
+//    records PKV_DEV_WAIT_TIMEOUT, waits (bounded) for its own copies in
+//    flight and returns.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ int g_dev_error_attention = 0;
+
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_dev_error_attention, 0, code); }
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr unsigned long long WAIT_NS = 2000000000ull;  // 2 s: a 16 KB copy takes microseconds
+
+// ---- PTX wrappers --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase of `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u && global_ns() - t0 > WAIT_NS) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ---- configuration ---------------------------------------------------------------------------
+template <int D, int R>
+struct Cfg {
+  static constexpr int CPR = D / 8;                  // lanes per row (16-byte columns)
+  static constexpr int RPI = 32 / CPR;               // rows covered by one warp-wide 16-byte load
+  static constexpr int NJ = R / RPI;                 // rows each lane loads per chunk
+  static constexpr int DUP = CPR / NJ;               // lanes holding the same reduced row
+  static constexpr int CHUNK_BYTES = R * D * 2;      // K (or V) bytes of one chunk
+  static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
+  static constexpr int NW = 4;                       // warps per CTA
+  static constexpr int RING_BYTES = 64 * 1024;       // shared-memory ring per CTA
+  static constexpr int NST = RING_BYTES / (NW * STAGE_BYTES);
+  static_assert(NJ >= 1 && NJ <= CPR, "row split");
+  static_assert(NST >= 1, "stages");
+};
+
+struct AttnParams {
+  const __half* q;
+  const __half* k;
+  const __half* v;
+  const int32_t* tables;
+  const int32_t* lens;
+  __half* out;
+  float* ws_ml;  // [S, H, max_parts, 2] (m, l) in base-2 log domain
+  float* ws_o;   // [S, H, max_parts, D] unnormalised partial outputs
+  int num_heads;
+  int num_blocks;
+  int max_blocks;
+  int block_size;
+  int part_tokens;
+  int max_parts;
+  float scale_log2;
+};
+
+// Number of partitions of a sequence; a bad or empty context has one (which writes zeros).
+__device__ __forceinline__ int num_parts(int ctx, int max_ctx, int part_tokens) {
+  if (ctx <= 0 || ctx > max_ctx) return 1;
+  return (ctx + part_tokens - 1) / part_tokens;
+}
+
+// Sum of per-lane partial dots over the CPR lanes of a row, for NJ rows at once.
+// On return every lane holds the full dot of reduced row jr = (lane % CPR) / DUP.
+template <int NJ, int CPR>
+__device__ __forceinline__ float butterfly_rows(float (&v)[NJ], int lane) {
+#pragma unroll
+  for (int n = NJ, mask = CPR / 2; n > 1; n /= 2, mask /= 2) {
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, send, mask);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int mask = CPR / NJ / 2; mask > 0; mask /= 2) r += __shfl_xor_sync(FULL, r, mask);
+  return r;
+}
+
+__device__ __forceinline__ void dot8(const uint4& raw, const float (&qf)[8], float& acc) {
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h2[e]);
+    acc = fmaf(qf[2 * e], f.x, acc);
+    acc = fmaf(qf[2 * e + 1], f.y, acc);
+  }
+}
+
+__device__ __forceinline__ void axpy8(const uint4& raw, float p, float (&acc)[8]) {
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __half22float2(h2[e]);
+    acc[2 * e] = fmaf(p, f.x, acc[2 * e]);
+    acc[2 * e + 1] = fmaf(p, f.y, acc[2 * e + 1]);
+  }
+}
+
+// One chunk: update (m, l_lane, acc) with `valid` rows of K/V staged at ks/vs.
+template <int D, int R, bool MASKED>
+__device__ __forceinline__ void chunk_update(const unsigned char* ks, const unsigned char* vs, int valid,
+                                             const float (&qf)[8], float& m, float& l_lane, float (&acc)[8],
+                                             int lane) {
+  using C = Cfg<D, R>;
+  const int col = lane % C::CPR;
+  const int grp = lane / C::CPR;
+  float part[C::NJ];
+#pragma unroll
+  for (int j = 0; j < C::NJ; ++j) {
+    const int row = j * C::RPI + grp;
+    const uint4 raw = *reinterpret_cast<const uint4*>(ks + (row * D + col * 8) * 2);
+    part[j] = 0.f;
+    dot8(raw, qf, part[j]);
+  }
+  float x = butterfly_rows<C::NJ, C::CPR>(part, lane);
+  const int rr = ((lane % C::CPR) / C::DUP) * C::RPI + grp;  // reduced row this lane holds
+  if (MASKED && rr >= valid) x = -INFINITY;
+  float cmax = x;
+#pragma unroll
+  for (int o = 16; o > 0; o /= 2) cmax = fmaxf(cmax, __shfl_xor_sync(FULL, cmax, o));
+  const float m_new = fmaxf(m, cmax);
+  const float alpha = exp2f(m - m_new);
+  const float p = exp2f(x - m_new);
+  l_lane = fmaf(l_lane, alpha, p);
+  m = m_new;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[c] *= alpha;
+#pragma unroll
+  for (int j = 0; j < C::NJ; ++j) {
+    const int row = j * C::RPI + grp;
+    const float pj = __shfl_sync(FULL, p, grp * C::CPR + j * C::DUP);
+    if (!MASKED || row < valid) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(vs + (row * D + col * 8) * 2);
+      axpy8(raw, pj, acc);
+    }
+  }
+}
+
+template <int D, int R>
+__global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partition_kernel(const AttnParams p) {
+  using C = Cfg<D, R>;
+  constexpr int NW = C::NW, NST = C::NST;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;                                                   // [NW][NST][K|V]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NST * C::STAGE_BYTES);  // [NW][NST]
+  float* comb = reinterpret_cast<float*>(bars + NW * NST);                      // [NW][D + 2]
+  int64_t* chunk_off = reinterpret_cast<int64_t*>(comb + NW * (D + 2));        // [chunks per part]
+
+  const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = p.block_size;
+  const int H = p.num_heads;
+  const int max_ctx = p.max_blocks * B;
+  const int ctx = p.lens[s];
+  const int nparts = num_parts(ctx, max_ctx, p.part_tokens);
+  if (part >= nparts) return;
+  const size_t out_off = (static_cast<size_t>(s) * H + h) * D;
+  if (ctx <= 0 || ctx > max_ctx) {
+    if (ctx != 0 && tid == 0) record_error(PKV_DEV_BAD_CONTEXT_LEN);
+    for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
+    return;
+  }
+
+  const int chunks_per_block = B / R;
+  const int chunks_per_part = p.part_tokens / R;
+  const int total_chunks = (ctx + R - 1) / R;
+  const int c_begin = part * chunks_per_part;
+  const int n_chunks = min(chunks_per_part, total_chunks - c_begin);
+
+  // Table slice of this partition -> element offset of each chunk's K (and V) tile.
+  int bad = 0;
+  for (int i = tid; i < n_chunks; i += NW * 32) {
+    const int c = c_begin + i;
+    const int j = c / chunks_per_block;
+    const int sub = c - j * chunks_per_block;
+    const int phys = p.tables[static_cast<size_t>(s) * p.max_blocks + j];
+    if (phys < 0 || phys >= p.num_blocks) {
+      bad = 1;
+      chunk_off[i] = 0;
+    } else {
+      chunk_off[i] = ((static_cast<int64_t>(phys) * H + h) * B + sub * R) * D;
+    }
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NW * NST; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    fence_mbar_init();
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
+    if (nparts == 1) {
+      for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
+    } else {
+      const size_t w = (static_cast<size_t>(s) * H + h) * p.max_parts + part;
+      for (int d = tid; d < D; d += NW * 32) p.ws_o[w * D + d] = 0.f;
+      if (tid == 0) {
+        p.ws_ml[2 * w] = -INFINITY;
+        p.ws_ml[2 * w + 1] = 0.f;
+      }
+    }
+    return;
+  }
+
+  // q slice of this lane, scaled into the base-2 log domain.
+  float qf[8];
+  {
+    const uint4 raw = *reinterpret_cast<const uint4*>(p.q + out_off + (lane % C::CPR) * 8);
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h2[e]);
+      qf[2 * e] = f.x * p.scale_log2;
+      qf[2 * e + 1] = f.y * p.scale_log2;
+    }
+  }
+
+  // Warp `warp` takes local chunks warp, warp + NW, ...
+  const int my_n = n_chunks > warp ? (n_chunks - warp + NW - 1) / NW : 0;
+  unsigned char* wring = ring + warp * NST * C::STAGE_BYTES;
+  const uint32_t wbar = smem_u32(&bars[warp * NST]);
+  const unsigned char* kbase = reinterpret_cast<const unsigned char*>(p.k);
+  const unsigned char* vbase = reinterpret_cast<const unsigned char*>(p.v);
+
+  auto issue = [&](int k) {
+    const int stage = k % NST;
+    const int i = warp + k * NW;
+    const int64_t off = chunk_off[i] * 2;
+    const uint32_t bar = wbar + stage * 8;
+    const uint32_t dst = smem_u32(wring + stage * C::STAGE_BYTES);
+    mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+    bulk_copy_g2s(dst, kbase + off, C::CHUNK_BYTES, bar);
+    bulk_copy_g2s(dst + C::CHUNK_BYTES, vbase + off, C::CHUNK_BYTES, bar);
+  };
+
+  int issued = 0;
+  if (lane == 0) {
+    for (; issued < NST && issued < my_n; ++issued) issue(issued);
+  }
+  issued = __shfl_sync(FULL, issued, 0);
+
+  float m = -INFINITY, l_lane = 0.f;
+  float acc[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+
+  int k = 0;
+  bool timed_out = false;
+  for (; k < my_n; ++k) {
+    const int stage = k % NST;
+    const uint32_t parity = (k / NST) & 1;
+    // every lane waits; the vote keeps the warp on one path even at the deadline
+    if (!__all_sync(FULL, mbar_wait_bounded(wbar + stage * 8, parity))) {
+      timed_out = true;
+      break;
+    }
+    const unsigned char* ks = wring + stage * C::STAGE_BYTES;
+    const int c = c_begin + warp + k * NW;
+    const int valid = min(R, ctx - c * R);
+    if (valid == R)
+      chunk_update<D, R, false>(ks, ks + C::CHUNK_BYTES, valid, qf, m, l_lane, acc, lane);
+    else
+      chunk_update<D, R, true>(ks, ks + C::CHUNK_BYTES, valid, qf, m, l_lane, acc, lane);
+    __syncwarp();
+    if (k + NST < my_n) {
+      if (lane == 0) issue(k + NST);
+      ++issued;
+    }
+  }
+  if (timed_out) {
+    if (lane == 0) record_error(PKV_DEV_WAIT_TIMEOUT);
+    // let this warp's outstanding copies land before the CTA's shared memory is released
+    for (int kk = k + 1; kk < issued; ++kk) mbar_wait_bounded(wbar + (kk % NST) * 8, (kk / NST) & 1);
+  }
+
+  // Per-warp results: sum acc over the row groups, l over distinct rows.
+#pragma unroll
+  for (int o = C::CPR; o < 32; o *= 2) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] += __shfl_xor_sync(FULL, acc[c], o);
+  }
+  float l = (lane % C::DUP) == 0 ? l_lane : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o /= 2) l += __shfl_xor_sync(FULL, l, o);
+
+  float* wcomb = comb + warp * (D + 2);
+  if (lane < C::CPR) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) wcomb[lane * 8 + c] = acc[c];
+  }
+  if (lane == 0) {
+    wcomb[D] = m;
+    wcomb[D + 1] = l;
+  }
+  __syncthreads();
+
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, comb[w * (D + 2) + D]);
+  float L = 0.f;
+  float wgt[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    wgt[w] = exp2f(comb[w * (D + 2) + D] - M);
+    L = fmaf(comb[w * (D + 2) + D + 1], wgt[w], L);
+  }
+  if (nparts == 1) {
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int d = tid; d < D; d += NW * 32) {
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) o = fmaf(comb[w * (D + 2) + d], wgt[w], o);
+      p.out[out_off + d] = __float2half_rn(o * inv);
+    }
+  } else {
+    const size_t w0 = (static_cast<size_t>(s) * H + h) * p.max_parts + part;
+    for (int d = tid; d < D; d += NW * 32) {
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) o = fmaf(comb[w * (D + 2) + d], wgt[w], o);
+      p.ws_o[w0 * D + d] = o;
+    }
+    if (tid == 0) {
+      p.ws_ml[2 * w0] = M;
+      p.ws_ml[2 * w0 + 1] = L;
+    }
+  }
+}
+
+// Merge the partitions of every (sequence, head) that has more than one.
+template <int D>
+__global__ void __launch_bounds__(D) paged_attention_merge_kernel(const AttnParams p) {
+  const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
+  const int ctx = p.lens[s];
+  const int nparts = num_parts(ctx, p.max_blocks * p.block_size, p.part_tokens);
+  if (nparts <= 1) return;
+  const size_t w0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_parts;
+  float M = -INFINITY;
+  for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.ws_ml[2 * (w0 + i)]);
+  float L = 0.f, O = 0.f;
+  for (int i = 0; i < nparts; ++i) {
+    const float mi = p.ws_ml[2 * (w0 + i)];
+    const float wgt = mi == -INFINITY ? 0.f : exp2f(mi - M);
+    L = fmaf(p.ws_ml[2 * (w0 + i) + 1], wgt, L);
+    O = fmaf(p.ws_o[(w0 + i) * D + d], wgt, O);
+  }
+  const float o = L > 0.f ? O / L : 0.f;
+  p.out[(static_cast<size_t>(s) * p.num_heads + h) * D + d] = __float2half_rn(o);
+}
+
+// ---- host side ---------------------------------------------------------------------------------
+constexpr int kMinPartTokens = 128;
+
+template <int D, int R>
+constexpr size_t smem_bytes(int part_tokens) {
+  using C = Cfg<D, R>;
+  return static_cast<size_t>(C::NW) * C::NST * C::STAGE_BYTES + C::NW * C::NST * 8 +
+         C::NW * (D + 2) * sizeof(float) + static_cast<size_t>(part_tokens / R) * sizeof(int64_t);
+}
+
+int device_sms(int dev) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  std::lock_guard<std::mutex> g(mu);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+template <int D, int R>
+cudaError_t prepare_kernel(int dev) {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  std::lock_guard<std::mutex> g(mu);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes<D, R>(512)));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
+int choose_part_tokens(int num_seqs, int num_heads, int max_ctx, int sms) {
+  // Enough CTAs for about two full waves at three CTAs per SM; longer partitions
+  // otherwise (less merge traffic, fewer pipeline fills).
+  const long long target = 2LL * 3 * sms;
+  for (int pt : {512, 256}) {
+    const long long ctas = static_cast<long long>(num_seqs) * num_heads * ((max_ctx + pt - 1) / pt);
+    if (ctas >= target) return pt;
+  }
+  return kMinPartTokens;
+}
+
+template <int D, int R>
+int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* ws, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = prepare_kernel<D, R>(dev);
+  if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention setup: %s", cudaGetErrorString(e));
+  const int max_ctx = p.max_blocks * p.block_size;
+  p.part_tokens = part_tokens;
+  p.max_parts = (max_ctx + part_tokens - 1) / part_tokens;
+  if (p.max_parts > 1) {
+    const size_t need = static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts * (D + 2) * sizeof(float);
+    if (ws == nullptr || ws_bytes < need)
+      return pkv::fail(PKV_ERR_WORKSPACE, "paged attention: workspace of %zu bytes needed, %zu given", need,
+                       ws == nullptr ? static_cast<size_t>(0) : ws_bytes);
+    p.ws_ml = static_cast<float*>(ws);
+    p.ws_o = p.ws_ml + static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts * 2;
+  }
+  dim3 grid(p.max_parts, p.num_heads, num_seqs);
+  paged_attention_partition_kernel<D, R>
+      <<<grid, Cfg<D, R>::NW * 32, smem_bytes<D, R>(part_tokens), st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
+  if (p.max_parts > 1) {
+    paged_attention_merge_kernel<D><<<dim3(p.num_heads, num_seqs), D, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention merge launch: %s", cudaGetErrorString(e));
+  }
+  return PKV_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace
+
+namespace pkv {
+int read_device_error_attention(int reset, int* code) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_dev_error_attention, sizeof(int));
+  if (e == cudaSuccess && reset && v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error_attention, &zero, sizeof(int));
+  }
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "reading the attention check word: %s", cudaGetErrorString(e));
+  *code = v;
+  return PKV_OK;
+}
+}  // namespace pkv
+
+extern "C" {
+
+size_t pkv_paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
+                                          int block_size) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0) return 0;
+  const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+  const long long parts = (max_ctx + kMinPartTokens - 1) / kMinPartTokens;
+  if (parts <= 1) return 0;
+  return static_cast<size_t>(num_seqs) * num_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
+int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                               int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq, float scale,
+                               int block_size, uint16_t* out, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG,
+                     "pkv_paged_attention_decode: num_seqs=%d num_heads=%d num_blocks=%d max_blocks_per_seq=%d",
+                     num_seqs, num_heads, num_blocks, max_blocks_per_seq);
+  if (head_dim != 64 && head_dim != 128)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: head_dim %d not in {64, 128}", head_dim);
+  if (block_size != 8 && block_size != 16 && block_size != 32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: block_size %d not in {8, 16, 32}",
+                     block_size);
+  if (num_seqs == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (num_seqs > 65535 || num_heads > 65535)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: num_seqs/num_heads above 65535");
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > (1LL << 30))
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: context capacity above 2^30 tokens");
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: null pointer");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: q, caches, out, workspace must be 16-byte aligned");
+  if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: scale not finite");
+
+  AttnParams p{};
+  p.q = reinterpret_cast<const __half*>(q);
+  p.k = reinterpret_cast<const __half*>(k_cache);
+  p.v = reinterpret_cast<const __half*>(v_cache);
+  p.tables = block_tables;
+  p.lens = context_lens;
+  p.out = reinterpret_cast<__half*>(out);
+  p.num_heads = num_heads;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = block_size;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const int pt = choose_part_tokens(num_seqs, num_heads, max_blocks_per_seq * block_size, device_sms(dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc;
+  if (head_dim == 128) {
+    rc = block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                         : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  } else {
+    rc = block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                         : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  }
+  if (rc == PKV_OK) pkv::clear_error();
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,327 @@
+// Host block manager: block tables, FIFO free list, reference counts, copy-on-write.
+//
+// Rules from [note] "vLLM / PagedAttention -- 把 LLM 服务的瓶颈从显存碎片里救出来",
+// sections 关键设计 2 (block table, on-demand allocation) and 关键设计 3 (sharing,
+// reference counts, copy-on-write); [lecture] "vLLM", sections PagedAttention 原理
+// (single-request walk-through) and Parallel Sampling 场景; [guide] "vLLM /
+// PagedAttention (SOSP 2023)", sections 03 and 04 (shared prefix, step 4).
+//
+// Every mutating call checks everything it needs (ids, free-block count) before
+// it changes anything, so a failing call leaves the state as it was.
+#include <cstdint>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "pkv_internal.h"
+
+namespace {
+
+struct Logical {
+  int32_t phys;
+  int32_t filled;
+};
+
+struct Manager {
+  int num_blocks = 0;
+  int B = 0;
+  std::deque<int32_t> free_list;
+  std::vector<int32_t> ref;
+  std::unordered_map<int64_t, std::vector<Logical>> seqs;
+  std::unordered_map<int64_t, std::vector<Logical>> prefixes;
+  int64_t cow_copies = 0;
+
+  int32_t take() {
+    int32_t b = free_list.front();
+    free_list.pop_front();
+    ref[b] = 1;
+    return b;
+  }
+  void release(int32_t b) {
+    if (--ref[b] == 0) free_list.push_back(b);
+  }
+  // Blocks for `len` fresh tokens, filled left to right; caller checked the count.
+  std::vector<Logical> fresh(int len) {
+    int n = (len + B - 1) / B;
+    std::vector<Logical> out;
+    out.reserve(n);
+    for (int j = 0; j < n; ++j) {
+      int f = len - j * B < B ? len - j * B : B;
+      out.push_back({take(), f});
+    }
+    return out;
+  }
+  void slots_of(const std::vector<Logical>& blocks, int64_t* out) const {
+    int64_t k = 0;
+    for (const Logical& lb : blocks)
+      for (int r = 0; r < lb.filled; ++r) out[k++] = (int64_t)lb.phys * B + r;
+  }
+  // What one append to `blocks` will need, given `extra_dec` references already
+  // given up on the last block by earlier appends in the same batch.
+  bool needs_block(const std::vector<Logical>& blocks, int extra_dec) const {
+    const Logical& last = blocks.back();
+    if (last.filled == B) return true;
+    return ref[last.phys] - extra_dec > 1;
+  }
+  // One append; the caller checked that a free block exists if one is needed.
+  int64_t append(std::vector<Logical>& blocks, int32_t* src, int32_t* dst) {
+    *src = -1;
+    *dst = -1;
+    Logical* last = &blocks.back();
+    if (last->filled == B) {
+      // the last block is full: the token opens a new logical block
+      blocks.push_back({take(), 0});
+      last = &blocks.back();
+    } else if (ref[last->phys] > 1) {
+      // shared and partly filled: move this sequence onto a copy
+      int32_t nb = take();
+      *src = last->phys;
+      *dst = nb;
+      ref[last->phys] -= 1;
+      last->phys = nb;
+      cow_copies += 1;
+    }
+    int64_t slot = (int64_t)last->phys * B + last->filled;
+    last->filled += 1;
+    return slot;
+  }
+};
+
+Manager* M(pkv_bm* bm) { return reinterpret_cast<Manager*>(bm); }
+const Manager* M(const pkv_bm* bm) { return reinterpret_cast<const Manager*>(bm); }
+
+int oom(const Manager* m, int need) {
+  return pkv::fail(PKV_ERR_OOM, "block manager: need %d free blocks, have %d", need,
+                   (int)m->free_list.size());
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_bm* pkv_bm_create(int num_blocks, int block_size, const int32_t* free_order) {
+  if (num_blocks <= 0 || block_size <= 0) {
+    pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_create: num_blocks=%d block_size=%d must be positive",
+              num_blocks, block_size);
+    return nullptr;
+  }
+  Manager* m = new (std::nothrow) Manager();
+  if (!m) {
+    pkv::fail(PKV_ERR_OOM, "pkv_bm_create: out of host memory");
+    return nullptr;
+  }
+  m->num_blocks = num_blocks;
+  m->B = block_size;
+  m->ref.assign(num_blocks, 0);
+  if (free_order) {
+    std::vector<char> seen(num_blocks, 0);
+    for (int i = 0; i < num_blocks; ++i) {
+      int32_t b = free_order[i];
+      if (b < 0 || b >= num_blocks || seen[b]) {
+        delete m;
+        pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_create: free_order is not a permutation (entry %d = %d)", i, b);
+        return nullptr;
+      }
+      seen[b] = 1;
+      m->free_list.push_back(b);
+    }
+  } else {
+    for (int i = 0; i < num_blocks; ++i) m->free_list.push_back(i);
+  }
+  return reinterpret_cast<pkv_bm*>(m);
+}
+
+void pkv_bm_destroy(pkv_bm* bm) { delete M(bm); }
+
+int pkv_bm_add_seq(pkv_bm* bm, int64_t seq_id, int prompt_len, int64_t* slots_out) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq: null manager");
+  Manager* m = M(bm);
+  if (prompt_len <= 0) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq: prompt_len=%d", prompt_len);
+  if (m->seqs.count(seq_id)) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq: sequence %lld exists", (long long)seq_id);
+  int need = (prompt_len + m->B - 1) / m->B;
+  if (need > (int)m->free_list.size()) return oom(m, need);
+  auto& blocks = m->seqs[seq_id];
+  blocks = m->fresh(prompt_len);
+  if (slots_out) m->slots_of(blocks, slots_out);
+  return PKV_OK;
+}
+
+int pkv_bm_fork(pkv_bm* bm, int64_t parent, int64_t child) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_fork: null manager");
+  Manager* m = M(bm);
+  auto it = m->seqs.find(parent);
+  if (it == m->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_fork: no sequence %lld", (long long)parent);
+  if (m->seqs.count(child)) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_fork: sequence %lld exists", (long long)child);
+  std::vector<Logical> copy = it->second;
+  for (const Logical& lb : copy) m->ref[lb.phys] += 1;
+  m->seqs.emplace(child, std::move(copy));
+  return PKV_OK;
+}
+
+int pkv_bm_append_slot(pkv_bm* bm, int64_t seq_id, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+  if (!bm || !slot || !cow_src || !cow_dst) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_append_slot: null argument");
+  Manager* m = M(bm);
+  auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_append_slot: no sequence %lld", (long long)seq_id);
+  if (m->needs_block(it->second, 0) && m->free_list.empty()) return oom(m, 1);
+  *slot = m->append(it->second, cow_src, cow_dst);
+  return PKV_OK;
+}
+
+int pkv_bm_append_slots(pkv_bm* bm, const int64_t* seq_ids, int n, int64_t* slots_out,
+                        int64_t* cow_pairs_out, int* num_cow) {
+  if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out || !cow_pairs_out)) || !num_cow)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_append_slots: bad argument");
+  Manager* m = M(bm);
+  std::vector<std::vector<Logical>*> lists(n);
+  std::unordered_map<int64_t, int> seen;
+  std::unordered_map<int32_t, int> dec;  // references given up on a block earlier in this batch
+  int need = 0;
+  for (int i = 0; i < n; ++i) {
+    auto it = m->seqs.find(seq_ids[i]);
+    if (it == m->seqs.end())
+      return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_append_slots: no sequence %lld", (long long)seq_ids[i]);
+    if (seen.count(seq_ids[i]))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_append_slots: sequence %lld listed twice", (long long)seq_ids[i]);
+    seen[seq_ids[i]] = 1;
+    lists[i] = &it->second;
+    const Logical& last = it->second.back();
+    int d = dec.count(last.phys) ? dec[last.phys] : 0;
+    if (m->needs_block(it->second, d)) {
+      need += 1;
+      if (last.filled != m->B) dec[last.phys] = d + 1;  // a copy gives up one reference
+    }
+  }
+  if (need > (int)m->free_list.size()) return oom(m, need);
+  int c = 0;
+  for (int i = 0; i < n; ++i) {
+    int32_t s, d;
+    slots_out[i] = m->append(*lists[i], &s, &d);
+    if (s >= 0) {
+      cow_pairs_out[2 * c] = s;
+      cow_pairs_out[2 * c + 1] = d;
+      ++c;
+    }
+  }
+  *num_cow = c;
+  return PKV_OK;
+}
+
+int pkv_bm_free(pkv_bm* bm, int64_t seq_id) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_free: null manager");
+  Manager* m = M(bm);
+  auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_free: no sequence %lld", (long long)seq_id);
+  for (const Logical& lb : it->second) m->release(lb.phys);
+  m->seqs.erase(it);
+  return PKV_OK;
+}
+
+int pkv_bm_register_prefix(pkv_bm* bm, int64_t prefix_id, int len, int64_t* slots_out) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_register_prefix: null manager");
+  Manager* m = M(bm);
+  if (len <= 0) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_register_prefix: len=%d", len);
+  if (m->prefixes.count(prefix_id))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_register_prefix: prefix %lld exists", (long long)prefix_id);
+  int need = (len + m->B - 1) / m->B;
+  if (need > (int)m->free_list.size()) return oom(m, need);
+  auto& blocks = m->prefixes[prefix_id];
+  blocks = m->fresh(len);
+  if (slots_out) m->slots_of(blocks, slots_out);
+  return PKV_OK;
+}
+
+int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq_with_prefix: null manager");
+  Manager* m = M(bm);
+  auto it = m->prefixes.find(prefix_id);
+  if (it == m->prefixes.end())
+    return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_add_seq_with_prefix: no prefix %lld", (long long)prefix_id);
+  if (m->seqs.count(seq_id))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq_with_prefix: sequence %lld exists", (long long)seq_id);
+  std::vector<Logical> copy = it->second;
+  for (const Logical& lb : copy) m->ref[lb.phys] += 1;
+  m->seqs.emplace(seq_id, std::move(copy));
+  return PKV_OK;
+}
+
+int pkv_bm_drop_prefix(pkv_bm* bm, int64_t prefix_id) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_drop_prefix: null manager");
+  Manager* m = M(bm);
+  auto it = m->prefixes.find(prefix_id);
+  if (it == m->prefixes.end())
+    return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_drop_prefix: no prefix %lld", (long long)prefix_id);
+  for (const Logical& lb : it->second) m->release(lb.phys);
+  m->prefixes.erase(it);
+  return PKV_OK;
+}
+
+int pkv_bm_block_table(const pkv_bm* bm, int64_t seq_id, int32_t* out, int cap, int* n_blocks, int* ctx_len) {
+  if (!bm || !n_blocks || !ctx_len || cap < 0 || (cap > 0 && !out))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_block_table: bad argument");
+  const Manager* m = M(bm);
+  auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_block_table: no sequence %lld", (long long)seq_id);
+  const auto& blocks = it->second;
+  if ((int)blocks.size() > cap)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_block_table: %d blocks exceed cap %d", (int)blocks.size(), cap);
+  int ctx = 0;
+  for (size_t j = 0; j < blocks.size(); ++j) {
+    out[j] = blocks[j].phys;
+    ctx += blocks[j].filled;
+  }
+  *n_blocks = (int)blocks.size();
+  *ctx_len = ctx;
+  return PKV_OK;
+}
+
+int pkv_bm_block_tables(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* tables_out, int max_blocks,
+                        int32_t* ctx_lens_out) {
+  if (!bm || n < 0 || max_blocks <= 0 || (n > 0 && (!seq_ids || !tables_out || !ctx_lens_out)))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_block_tables: bad argument");
+  const Manager* m = M(bm);
+  for (int i = 0; i < n; ++i) {
+    auto it = m->seqs.find(seq_ids[i]);
+    if (it == m->seqs.end())
+      return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_block_tables: no sequence %lld", (long long)seq_ids[i]);
+    if ((int)it->second.size() > max_blocks)
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_block_tables: sequence %lld has %d blocks > %d",
+                       (long long)seq_ids[i], (int)it->second.size(), max_blocks);
+  }
+  for (int i = 0; i < n; ++i) {
+    const auto& blocks = m->seqs.find(seq_ids[i])->second;
+    int32_t* row = tables_out + (size_t)i * max_blocks;
+    int ctx = 0;
+    for (int j = 0; j < max_blocks; ++j) row[j] = j < (int)blocks.size() ? blocks[j].phys : -1;
+    for (const Logical& lb : blocks) ctx += lb.filled;
+    ctx_lens_out[i] = ctx;
+  }
+  return PKV_OK;
+}
+
+int pkv_bm_ref_count(const pkv_bm* bm, int32_t block) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_ref_count: null manager");
+  const Manager* m = M(bm);
+  if (block < 0 || block >= m->num_blocks)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_ref_count: block %d out of range", block);
+  return m->ref[block];
+}
+
+int pkv_bm_stats(const pkv_bm* bm, int* free_blocks, int64_t* tail_waste_tokens, int64_t* cow_copies) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_stats: null manager");
+  const Manager* m = M(bm);
+  if (free_blocks) *free_blocks = (int)m->free_list.size();
+  if (tail_waste_tokens) {
+    int64_t w = 0;
+    for (const auto& kv : m->seqs)
+      for (const Logical& lb : kv.second) w += m->B - lb.filled;
+    *tail_waste_tokens = w;
+  }
+  if (cow_copies) *cow_copies = m->cow_copies;
+  return PKV_OK;
+}
+
+}  // extern "C"

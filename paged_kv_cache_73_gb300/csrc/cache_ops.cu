@@ -1,0 +1,195 @@
+// The two byte-moving kernels around decode attention, for sm_103a.
+//
+// [note] "vLLM / PagedAttention -- 把 LLM 服务的瓶颈从显存碎片里救出来", section
+// 关键设计 5, names them: "fused reshape and block write" (each new token's
+// key/value rows go to their slot in the block layout, all heads in one
+// launch) and "fused block copy" (the many small copies that copy-on-write
+// triggers, section 关键设计 3, done by one kernel instead of one memcpy each).
+//
+// Both are HBM-bound copies: 16-byte vector loads and stores, 64-bit offsets
+// (a pool can fill most of a 288 GB HBM), every slot and block id checked
+// against the pool before it is used.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ int g_dev_error_cache_ops = 0;
+
+__device__ __forceinline__ void record_error(int code) { atomicCAS(&g_dev_error_cache_ops, 0, code); }
+
+// One thread moves one 16-byte column of one (token, head) row of K and of V.
+// vec_per_row = head_dim / 8.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __restrict__ key,
+                                                                const uint4* __restrict__ value,
+                                                                uint4* __restrict__ k_cache,
+                                                                uint4* __restrict__ v_cache,
+                                                                const int64_t* __restrict__ slot_mapping,
+                                                                int64_t total, int num_heads, int vec_per_row,
+                                                                int block_size, int64_t num_slots) {
+  const int64_t per_token = static_cast<int64_t>(num_heads) * vec_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int64_t rem = i - t * per_token;         // h * vec_per_row + c
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;                        // padding token
+    if (slot >= num_slots) {
+      record_error(PKV_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / block_size;
+    const int64_t row = slot - blk * block_size;
+    const int64_t h = rem / vec_per_row;
+    const int64_t c = rem - h * vec_per_row;
+    const int64_t dst = ((blk * num_heads + h) * block_size + row) * vec_per_row + c;
+    k_cache[dst] = key[i];
+    v_cache[dst] = value[i];
+  }
+}
+
+constexpr int kMaxLayersPerLaunch = 64;
+
+struct LayerPtrs {
+  uint4* k[kMaxLayersPerLaunch];
+  uint4* v[kMaxLayersPerLaunch];
+};
+
+// grid (num_pairs, num_layers, splits): CTA (p, l, z) copies slice z of block pair p in layer l.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const LayerPtrs ptrs, const int64_t* __restrict__ mapping,
+                                                          int64_t vec_per_block, int num_blocks) {
+  const int pair = blockIdx.x;
+  const int layer = blockIdx.y;
+  const int64_t src = mapping[2 * pair];
+  const int64_t dst = mapping[2 * pair + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.z == 0) record_error(PKV_DEV_BAD_COPY_PAIR);
+    return;
+  }
+  const uint4* __restrict__ ks = ptrs.k[layer] + src * vec_per_block;
+  const uint4* __restrict__ vs = ptrs.v[layer] + src * vec_per_block;
+  uint4* __restrict__ kd = ptrs.k[layer] + dst * vec_per_block;
+  uint4* __restrict__ vd = ptrs.v[layer] + dst * vec_per_block;
+  const int64_t stride = static_cast<int64_t>(gridDim.z) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.z) * blockDim.x + threadIdx.x;
+  // four 16-byte loads of K and four of V in flight per thread before the stores
+  for (; i + 3 * stride < vec_per_block; i += 4 * stride) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a[u] = ks[i + u * stride];
+      b[u] = vs[i + u * stride];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      kd[i + u * stride] = a[u];
+      vd[i + u * stride] = b[u];
+    }
+  }
+  for (; i < vec_per_block; i += stride) {
+    kd[i] = ks[i];
+    vd[i] = vs[i];
+  }
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int check_shape(const char* fn, int num_heads, int head_dim, int block_size, int num_blocks) {
+  if (num_heads <= 0 || num_blocks <= 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "%s: num_heads=%d num_blocks=%d", fn, num_heads, num_blocks);
+  if (head_dim != 64 && head_dim != 128)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: head_dim %d not in {64, 128}", fn, head_dim);
+  if (block_size != 8 && block_size != 16 && block_size != 32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: block_size %d not in {8, 16, 32}", fn, block_size);
+  return PKV_OK;
+}
+
+}  // namespace
+
+namespace pkv {
+int read_device_error_cache_ops(int reset, int* code) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_dev_error_cache_ops, sizeof(int));
+  if (e == cudaSuccess && reset && v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error_cache_ops, &zero, sizeof(int));
+  }
+  if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "reading the cache-op check word: %s", cudaGetErrorString(e));
+  *code = v;
+  return PKV_OK;
+}
+}  // namespace pkv
+
+extern "C" {
+
+int pkv_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* k_cache, uint16_t* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_heads, int head_dim, int block_size,
+                          int num_blocks, void* stream) {
+  int rc = check_shape("pkv_reshape_and_cache", num_heads, head_dim, block_size, num_blocks);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache: num_tokens=%d", num_tokens);
+  if (num_tokens == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache: null pointer");
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache: key, value and caches must be 16-byte aligned");
+  const int vec = head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * num_heads * vec;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < (1 << 20) ? want : (1 << 20));
+  reshape_and_cache_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value), reinterpret_cast<uint4*>(k_cache),
+      reinterpret_cast<uint4*>(v_cache), slot_mapping, total, num_heads, vec, block_size,
+      static_cast<int64_t>(num_blocks) * block_size);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_reshape_and_cache launch: %s", cudaGetErrorString(e));
+  pkv::clear_error();
+  return PKV_OK;
+}
+
+int pkv_copy_blocks(uint16_t* const* k_caches, uint16_t* const* v_caches, int num_layers,
+                    const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim, int block_size,
+                    int num_blocks, void* stream) {
+  int rc = check_shape("pkv_copy_blocks", num_heads, head_dim, block_size, num_blocks);
+  if (rc != PKV_OK) return rc;
+  if (num_pairs < 0 || num_layers < 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_copy_blocks: num_pairs=%d num_layers=%d", num_pairs, num_layers);
+  if (num_pairs == 0 || num_layers == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (!k_caches || !v_caches || !block_mapping)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_copy_blocks: null pointer");
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l] || !aligned16(k_caches[l]) || !aligned16(v_caches[l]))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_copy_blocks: layer %d cache pointer null or not 16-byte aligned", l);
+  }
+  const int64_t vec_per_block = static_cast<int64_t>(num_heads) * block_size * head_dim / 8;
+  // enough CTAs per pair to keep every SM streaming even when there are few pairs
+  int splits = static_cast<int>((vec_per_block + 256 * 8 - 1) / (256 * 8));
+  if (splits < 1) splits = 1;
+  if (splits > 64) splits = 64;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+    const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
+    LayerPtrs ptrs{};
+    for (int l = 0; l < nl; ++l) {
+      ptrs.k[l] = reinterpret_cast<uint4*>(k_caches[l0 + l]);
+      ptrs.v[l] = reinterpret_cast<uint4*>(v_caches[l0 + l]);
+    }
+    copy_blocks_kernel<<<dim3(num_pairs, nl, splits), 256, 0, st>>>(ptrs, block_mapping, vec_per_block, num_blocks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_copy_blocks launch: %s", cudaGetErrorString(e));
+  }
+  pkv::clear_error();
+  return PKV_OK;
+}
+
+}  // extern "C"

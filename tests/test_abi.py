@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared symbol,
+and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_73_gb300 import _build
+from paged_kv_cache_73_gb300 import binding as pkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
+
+
+def test_version(lib):
+    assert pkv.version() == 100
+
+
+def _decode(lib, **kw):
+    a = dict(q=16, k=16, v=16, tables=16, lens=16, S=2, H=2, D=64, N=8, maxb=4, scale=0.125, B=16, out=16,
+             ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.pkv_paged_attention_decode(a["q"], a["k"], a["v"], a["tables"], a["lens"], a["S"], a["H"], a["D"],
+                                          a["N"], a["maxb"], a["scale"], a["B"], a["out"], a["ws"], a["ws_bytes"],
+                                          None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(B=12), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(H=0), pkv.PKV_ERR_INVALID_ARG),
+    (dict(S=-1), pkv.PKV_ERR_INVALID_ARG),
+    (dict(q=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(q=24), pkv.PKV_ERR_INVALID_ARG),                 # not 16-byte aligned
+    (dict(scale=float("inf")), pkv.PKV_ERR_INVALID_ARG),
+    (dict(S=0), pkv.PKV_OK),                               # empty batch: nothing to do
+])
+def test_attention_host_validation(lib, kw, status):
+    assert _decode(lib, **kw) == status
+    if status != pkv.PKV_OK:
+        assert lib.pkv_last_error()
+
+
+def test_workspace_size(lib):
+    # one partition (<= 128 tokens of capacity) needs no workspace
+    assert pkv.paged_attention_workspace_size(4, 2, 64, 8, 16) == 0
+    # 2048 tokens of capacity: 16 partitions of 128 tokens, (D + 2) floats each
+    assert pkv.paged_attention_workspace_size(64, 40, 128, 128, 16) == 64 * 40 * 16 * 130 * 4
+
+
+def test_cache_ops_host_validation(lib):
+    assert lib.pkv_reshape_and_cache(16, 16, 16, 16, 16, 4, 2, 80, 16, 8, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_reshape_and_cache(16, 16, 16, 16, 16, 0, 2, 64, 16, 8, None) == pkv.PKV_OK
+    assert lib.pkv_reshape_and_cache(None, 16, 16, 16, 16, 4, 2, 64, 16, 8, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_copy_blocks(None, None, 1, 16, 0, 2, 64, 16, 8, None) == pkv.PKV_OK
+    assert lib.pkv_copy_blocks(None, None, 1, 16, 3, 2, 64, 16, 8, None) == pkv.PKV_ERR_INVALID_ARG
+    arr = (ctypes.c_void_p * 1)(24)
+    assert lib.pkv_copy_blocks(ctypes.cast(arr, ctypes.c_void_p), ctypes.cast(arr, ctypes.c_void_p), 1, 16, 3, 2,
+                               64, 16, 8, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_binding_refuses_missing_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(pkv, "_lib", None)
+    monkeypatch.setattr(pkv, "library_path", lambda: str(tmp_path / "absent.so"))
+    with pytest.raises(pkv.PkvError):
+        pkv.load()

@@ -1,0 +1,190 @@
+"""The C++ block manager (libpkv.so) against the oracle's, on the pages' examples
+and on long random operation sequences: identical slots, copies, tables,
+reference counts and statistics after every step."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import block_manager as obm
+from paged_kv_cache_73_gb300 import _build
+from paged_kv_cache_73_gb300 import binding as pkv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "block_manager_examples.json")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def _free_order(n, head):
+    return list(head) + [b for b in range(n) if b not in head]
+
+
+def test_pages_single_request_example():
+    g = json.load(open(GOLDEN))["single_request"]
+    B = g["block_size"]
+    bm = pkv.BlockManager(16, B, _free_order(16, g["free_order_head"]))
+    slots = bm.add_seq(0, len(g["prompt"]))
+    table, ctx = bm.block_table(0)
+    assert table == g["after_prefill"]["table"] and ctx == 7
+    assert list(slots) == [7 * B + r for r in range(4)] + [1 * B + r for r in range(3)]
+    for step, n_tokens in zip(g["decode"], (8, 9)):
+        slot, src, dst = bm.append_slot(0)
+        assert (src, dst) == (-1, -1)
+        table, ctx = bm.block_table(0)
+        assert len(table) == step["num_logical_blocks"] and ctx == n_tokens
+    assert table[2] == 3 and slot == 3 * B
+    free, waste, copies = bm.stats()
+    assert (free, waste, copies) == (13, 3, 0)
+
+
+def test_pages_parallel_sampling_example():
+    g = json.load(open(GOLDEN))["parallel_sampling"]
+    B = g["block_size"]
+    bm = pkv.BlockManager(16, B, _free_order(16, g["free_order_head"]))
+    bm.add_seq(1, g["prompt_len"])
+    bm.fork(1, 2)
+    for b, r in g["after_prefill"]["ref"].items():
+        assert bm.ref_count(int(b)) == r
+    slot, src, dst = bm.append_slot(1)
+    assert [src, dst] == g["A1_writes_first"]["copy"] and slot == 3 * B + 3
+    for b, r in g["A1_writes_first"]["ref"].items():
+        assert bm.ref_count(int(b)) == r
+    slot, src, dst = bm.append_slot(2)
+    assert (src, dst) == (-1, -1) and slot == 1 * B + 3
+    assert bm.block_table(2)[0] == g["A2_writes_next"]["A2"]
+
+
+def _compare(nat, ora, live, num_blocks):
+    for s in live:
+        assert nat.block_table(s) == ora.block_table(s)
+    for b in range(num_blocks):
+        assert nat.ref_count(b) == ora.ref_count(b)
+    free, waste, copies = nat.stats()
+    assert (free, waste, copies) == (ora.num_free(), ora.tail_waste_tokens(), ora.cow_copies)
+
+
+@pytest.mark.parametrize("B,N,seed", [(4, 64, 0), (16, 300, 1), (8, 40, 2), (1, 50, 3)])
+def test_random_operations_match_oracle(B, N, seed):
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(N)
+    nat = pkv.BlockManager(N, B, order)
+    ora = obm.BlockManager(N, B, order)
+    live, prefixes = [], []
+    nid = 0
+    for step in range(1500):
+        op = int(rng.integers(0, 14))
+        try:
+            if op < 2 or not live:
+                n = int(rng.integers(1, 5 * B))
+                try:
+                    want = ora.add_seq(nid, n)
+                except MemoryError:
+                    with pytest.raises(pkv.PkvOutOfBlocks):
+                        nat.add_seq(nid, n)
+                    continue
+                assert list(nat.add_seq(nid, n)) == want
+                live.append(nid)
+                nid += 1
+            elif op < 4:
+                p = int(rng.choice(live))
+                ora.fork(p, nid)
+                nat.fork(p, nid)
+                live.append(nid)
+                nid += 1
+            elif op < 5 and len(live) > 1:
+                s = int(rng.choice(live))
+                ora.free(s)
+                nat.free(s)
+                live.remove(s)
+            elif op < 6:
+                pid = 1000 + step
+                try:
+                    want = ora.register_prefix(pid, int(rng.integers(1, 3 * B)))
+                except MemoryError:
+                    continue
+                got = nat.register_prefix(pid, len(want))
+                assert list(got) == want
+                prefixes.append(pid)
+            elif op < 7 and prefixes:
+                pid = int(rng.choice(prefixes))
+                ora.add_seq_with_prefix(nid, pid)
+                nat.add_seq_with_prefix(nid, pid)
+                live.append(nid)
+                nid += 1
+            elif op < 8 and prefixes:
+                pid = prefixes.pop(int(rng.integers(0, len(prefixes))))
+                ora.drop_prefix(pid)
+                nat.drop_prefix(pid)
+            elif op < 10:
+                # a batch of distinct sequences, all-or-nothing
+                k = int(rng.integers(1, min(6, len(live)) + 1))
+                batch = [int(x) for x in rng.choice(live, size=k, replace=False)]
+                snapshot_free = ora.num_free()
+                try:
+                    slots, pairs = nat.append_slots(batch)
+                except pkv.PkvOutOfBlocks:
+                    # the oracle, appending one by one, must also run out somewhere in the batch;
+                    # replay on a copy to confirm, leaving the real oracle untouched
+                    import copy
+                    probe = copy.deepcopy(ora)
+                    with pytest.raises(MemoryError):
+                        for s in batch:
+                            probe.append_slot(s)
+                    assert ora.num_free() == snapshot_free
+                    continue
+                want_pairs = []
+                for s, got in zip(batch, slots):
+                    slot, src, dst = ora.append_slot(s)
+                    assert slot == got
+                    if src >= 0:
+                        want_pairs.append([src, dst])
+                assert pairs.tolist() == want_pairs
+            else:
+                s = int(rng.choice(live))
+                try:
+                    want = ora.append_slot(s)
+                except MemoryError:
+                    with pytest.raises(pkv.PkvOutOfBlocks):
+                        nat.append_slot(s)
+                    continue
+                assert nat.append_slot(s) == want
+        finally:
+            pass
+        if step % 50 == 0:
+            _compare(nat, ora, live, N)
+    _compare(nat, ora, live, N)
+
+
+def test_errors_leave_state_unchanged():
+    bm = pkv.BlockManager(4, 4)
+    bm.add_seq(0, 13)
+    with pytest.raises(pkv.PkvOutOfBlocks):
+        bm.add_seq(1, 1)
+    bm.fork(0, 1)
+    with pytest.raises(pkv.PkvOutOfBlocks):
+        bm.append_slot(1)
+    assert bm.block_table(1) == bm.block_table(0)
+    with pytest.raises(pkv.PkvError):
+        bm.fork(0, 1)                         # child exists
+    with pytest.raises(pkv.PkvError):
+        bm.append_slot(99)                    # unknown sequence
+    with pytest.raises(pkv.PkvError):
+        bm.append_slots([0, 0])               # listed twice
+    with pytest.raises(pkv.PkvError):
+        pkv.BlockManager(4, 4, [0, 1, 1, 2])  # not a permutation
+    assert bm.stats()[0] == 0
+
+
+def test_batch_tables_padded():
+    bm = pkv.BlockManager(32, 4, list(range(32)))
+    bm.add_seq(5, 9)
+    bm.add_seq(6, 1)
+    tables, lens = bm.block_tables([6, 5], 4)
+    assert tables.tolist() == [[3, -1, -1, -1], [0, 1, 2, -1]] and lens.tolist() == [1, 9]
+    with pytest.raises(pkv.PkvError):
+        bm.block_tables([5], 2)
