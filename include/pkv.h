@@ -28,7 +28,7 @@
  * `slot` is row slot % block_size of physical block slot / block_size, so one
  * (block, head) tile of a pool is block_size*head_dim*2 contiguous bytes.
  *
- * Supported shapes: head_dim in {64, 128}, block_size in {8, 16, 32}, one K/V
+ * Supported shapes: head_dim in {64, 128}, block_size in {4, 8, 16, 32}, one K/V
  * head per query head.  Other values return PKV_ERR_UNSUPPORTED.
  */
 #ifndef PKV_H_

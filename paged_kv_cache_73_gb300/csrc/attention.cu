@@ -103,7 +103,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
   static constexpr int NW = 4;                       // warps per CTA
   static constexpr int RING_BYTES = 64 * 1024;       // shared-memory ring per CTA
-  static constexpr int NST = RING_BYTES / (NW * STAGE_BYTES);
+  static constexpr int NST = RING_BYTES / (NW * STAGE_BYTES) < 8 ? RING_BYTES / (NW * STAGE_BYTES) : 8;
   static_assert(NJ >= 1 && NJ <= CPR, "row split");
   static_assert(NST >= 1, "stages");
 };
@@ -540,8 +540,8 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
                      num_seqs, num_heads, num_blocks, max_blocks_per_seq);
   if (head_dim != 64 && head_dim != 128)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: head_dim %d not in {64, 128}", head_dim);
-  if (block_size != 8 && block_size != 16 && block_size != 32)
-    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: block_size %d not in {8, 16, 32}",
+  if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: block_size %d not in {4, 8, 16, 32}",
                      block_size);
   if (num_seqs == 0) {
     pkv::clear_error();
@@ -576,12 +576,15 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
   const int pt = choose_part_tokens(num_seqs, num_heads, max_blocks_per_seq * block_size, device_sms(dev));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc;
+  // chunk rows R = min(B, 16): a block of 32 rows is read as two chunks
   if (head_dim == 128) {
-    rc = block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
-                         : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+    rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
+         : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                           : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
   } else {
-    rc = block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
-                         : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+    rc = block_size == 4   ? launch<64, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
+         : block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                           : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
   }
   if (rc == PKV_OK) pkv::clear_error();
   return rc;

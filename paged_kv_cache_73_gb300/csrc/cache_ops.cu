@@ -102,8 +102,8 @@ int check_shape(const char* fn, int num_heads, int head_dim, int block_size, int
     return pkv::fail(PKV_ERR_INVALID_ARG, "%s: num_heads=%d num_blocks=%d", fn, num_heads, num_blocks);
   if (head_dim != 64 && head_dim != 128)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: head_dim %d not in {64, 128}", fn, head_dim);
-  if (block_size != 8 && block_size != 16 && block_size != 32)
-    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: block_size %d not in {8, 16, 32}", fn, block_size);
+  if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: block_size %d not in {4, 8, 16, 32}", fn, block_size);
   return PKV_OK;
 }
 

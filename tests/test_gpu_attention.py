@@ -31,10 +31,10 @@ def test_tiny_batch(cuda_device):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("B", [4, 8, 16, 32])
 def test_ragged_lengths_every_shape(cuda_device, D, B):
     # lengths around chunk, block and partition edges: 1, B-1, B, B+1, 127..129, 255..257, 511..513, 1000
-    lens = [1, B - 1, B, B + 1, 16, 17, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1000]
+    lens = [1, B - 1, B, B + 1, 16, 17, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1000, 2049]
     w = wl.custom(100 + D + B, lens, num_heads=3, head_dim=D, block_size=B, name=f"ragged_D{D}_B{B}")
     _full_check(w, cuda_device)
 

@@ -15,7 +15,7 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("B", [4, 8, 16, 32])
 def test_reshape_and_cache_bit_exact(cuda_device, D, B):
     w = wl.custom(200 + D + B, [30, 7, 64, 1], num_heads=5, head_dim=D, block_size=B, num_blocks=40)
     k, v = w.pools(cuda_device)
