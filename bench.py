@@ -1,0 +1,454 @@
+"""Decode-step benchmark of the paged K/V-cache path on GB300.
+
+One step = one decode step of the OPT-13B-shaped single-layer batch (64
+sequences, 40 heads x 128, block size 16, context lengths ~ U[128, 2048],
+physical blocks shuffled): copy_blocks of the step's copy-on-write pairs,
+reshape_and_cache of the 64 new tokens, paged decode attention (partition
+kernel + merge kernel).  Slot assignment (the host block manager) runs once
+at set-up; its host time is reported separately.
+
+Prints ONE JSON line (rank 0).  `value` is effective KV GB/s: the K/V bytes
+attention reads per step (logical, a shared block counted per reader) over
+the device-timed step.  `e2e` is the same metric with every step's inputs
+copied host->device from pinned memory and the output copied back, through
+the same C-ABI calls.  `roofline` is the paged attention call alone against
+the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the CPU oracle on the host cores instead (a bounded
+sample of the same workload per step) and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention effective KV GB/s (% of HBM peak) and decode tokens/s"
+UNIT = "GB/s"
+WORKLOAD = ("opt13b_decode_step: 64 seqs, 40 heads x 128, block 16, ctx ~ U[128,2048], shuffled blocks, "
+            "+ reshape_and_cache of 64 new tokens")
+SEED = 1002
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call (partition + merge
+# kernels) from an ncu capture of this workload, keyed by the sha256 of the attention source it
+# was taken on; a changed kernel reports null until it is captured again.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop (profiling runs)")
+    return ap.parse_args()
+
+
+def attention_source_sha() -> str:
+    path = os.path.join(ROOT, "paged_kv_cache_73_gb300", "csrc", "attention.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: torch copy, read+write bytes)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows), "reasons": sorted(reasons)}
+
+
+# ---- workload ----------------------------------------------------------------------------------
+
+H, D, B, S = 40, 128, 16, 64
+MAX_BLOCKS = 2048 // B
+
+
+def attention_algorithmic_bytes(lens) -> int:
+    """K/V rows read + q read + out written + table entries + context lengths, per call."""
+    total = 0
+    for c in lens:
+        c = int(c)
+        total += H * (2 * c * D * 2 + 2 * D * 2) + 4 * math.ceil(c / B) + 4
+    return total
+
+
+def build_step_inputs(seed: int):
+    """Block tables and new-token slots from the host block manager, over the recipe's lengths."""
+    from paged_kv_cache_73_gb300 import binding as pkv
+    from paged_kv_cache_73_gb300 import workloads as wl
+    recipe = wl.opt13b(seed=seed)
+    lens = recipe.context_lens
+    N = recipe.num_blocks
+    bm = pkv.BlockManager(N, B, wl.free_list_order(N, seed))
+    for s in range(S):
+        bm.add_seq(s, int(lens[s]) - 1)                 # prompt and earlier tokens
+    t0 = time.perf_counter()
+    slots, pairs = bm.append_slots(list(range(S)))      # slot assignment of this step's token
+    host_us = (time.perf_counter() - t0) * 1e6
+    tables, ctx = bm.block_tables(list(range(S)), MAX_BLOCKS)
+    assert np.array_equal(ctx, lens)
+    w = wl.from_tables("opt13b_decode_step", seed, H, D, B, N, tables, ctx, recipe.notes)
+    return w, slots, pairs, host_us
+
+
+def run_gpu(args, rank, world, dev):
+    import torch
+    from paged_kv_cache_73_gb300 import binding as pkv
+    from paged_kv_cache_73_gb300 import workloads as wl
+
+    seed = SEED + 7919 * rank                           # weak scaling: each rank its own batch
+    w, slots, pairs, host_us = build_step_inputs(seed)
+    k, v = w.pools(dev)
+    q = w.q(dev)
+    key, value = wl.new_tokens(S, H, D, seed, dev)
+    tables = torch.from_numpy(w.block_tables).to(dev)
+    lens = torch.from_numpy(w.context_lens).to(dev)
+    slots_d = torch.from_numpy(slots).to(dev)
+    pairs_d = torch.from_numpy(np.ascontiguousarray(pairs)).to(dev)
+    out = torch.empty_like(q)
+    ws = pkv.workspace_for(S, H, D, MAX_BLOCKS, B, dev)
+    part_tokens, attn_kernels = pkv.paged_attention_plan(S, H, D, MAX_BLOCKS, B)
+    stream = torch.cuda.current_stream()
+    n_pairs = int(pairs.shape[0])
+
+    def step(ev0=None, ev1=None):
+        if n_pairs:
+            pkv.copy_blocks([k], [v], pairs_d, stream=stream)
+        pkv.reshape_and_cache(key, value, k, v, slots_d, stream=stream)
+        if ev0 is not None:
+            ev0.record(stream)
+        pkv.paged_attention_decode(q, k, v, tables, lens, w.scale, B, out=out, workspace=ws, stream=stream)
+        if ev1 is not None:
+            ev1.record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
+        start.record(stream)
+        for i in range(K):
+            step(*ev[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    step_ms = start.elapsed_time(stop) / K
+    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_mean = sum(attn_ms) / K
+    code = pkv.device_error()
+    assert code == 0, f"device check {code}"
+
+    res = {"step_ms": step_ms, "attn_ms": attn_mean, "attn_ms_median": statistics.median(attn_ms),
+           "kv_bytes": w.logical_kv_bytes(), "attn_bytes": attention_algorithmic_bytes(w.context_lens),
+           "launches": K * ((1 if n_pairs else 0) + 1 + attn_kernels), "part_tokens": part_tokens,
+           "host_slot_us": host_us, "clocks": clocks.summary(), "n_pairs": n_pairs}
+
+    if not args.no_e2e:
+        res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws))
+    return res
+
+
+def physical_gpu_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if local < len(ids) and ids[local].isdigit():
+        return int(ids[local])
+    return local
+
+
+def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
+    """Same step through the C ABI, with the step's inputs in pinned host memory.
+
+    Every step copies q, the new keys/values, slot mapping, copy pairs, block
+    tables and context lengths host->device, runs the kernels, copies the
+    attention output back and waits for it (wall clock).
+    """
+    import torch
+    from paged_kv_cache_73_gb300 import binding as pkv
+
+    host = {
+        "q": q.cpu().pin_memory(), "key": key.cpu().pin_memory(), "value": value.cpu().pin_memory(),
+        "slots": torch.from_numpy(slots).pin_memory(),
+        "pairs": torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory(),
+        "tables": torch.from_numpy(w.block_tables).pin_memory(),
+        "lens": torch.from_numpy(w.context_lens).pin_memory(),
+    }
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
+    out_d = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+    n_pairs = int(pairs.shape[0])
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for n, t in host.items():
+            dbuf[n].copy_(t, non_blocking=True)
+        if n_pairs:
+            pkv.copy_blocks([k], [v], dbuf["pairs"], stream=stream)
+        pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=stream)
+        pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, B, out=out_d,
+                                   workspace=ws, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    K = args.steps
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    dt = (time.perf_counter() - t0) / K
+    return {"e2e_step_ms": dt * 1e3, "h2d": h2d, "d2h": d2h}
+
+
+def prepare_cpu_sample(w, seqs, slots, seed):
+    """Host inputs of the oracle for sequences `seqs` of the step (generated once, untimed)."""
+    from paged_kv_cache_73_gb300 import workloads as wl
+
+    kc, vc, tabs, lens = w.compact_pools(seqs)
+    key, value = wl.new_tokens(S, H, D, seed, "cpu")
+    # the new tokens' slots re-expressed in the compact pool's block numbering
+    ids = sorted({int(x) for x in w.block_tables[seqs].ravel() if x >= 0})
+    remap = {b: i for i, b in enumerate(ids)}
+    local = [remap[int(slots[s]) // B] * B + int(slots[s]) % B for s in seqs]
+    return {"k": kc.numpy(), "v": vc.numpy(), "tables": tabs, "lens": lens, "slots": local,
+            "key": key.numpy()[seqs], "value": value.numpy()[seqs], "q": w.q("cpu").numpy()[seqs],
+            "scale": w.scale, "kv_bytes": int(lens.astype(np.int64).sum()) * H * D * 2 * 2}
+
+
+def cpu_sample_seconds(x):
+    """Oracle (fp64, host) over a prepared sample: the new-token writes, then attention."""
+    from oracle import attention as oracle_attention
+    from oracle import cache_ops as oracle_cache_ops
+
+    t0 = time.perf_counter()
+    oracle_cache_ops.reshape_and_cache(x["key"], x["value"], x["k"], x["v"], x["slots"])
+    oracle_attention.paged_decode_attention(x["q"], x["k"], x["v"], x["tables"], x["lens"], x["scale"])
+    return time.perf_counter() - t0
+
+
+def run_cpu_baseline(seed: int, budget_s: float = 12.0):
+    w, slots, pairs, _ = build_step_inputs(seed)
+    order = [int(x) for x in np.argsort(w.context_lens)[::-1]]
+    seqs = []
+    for a, b in zip(order, order[::-1]):               # alternate long and short sequences
+        for s in (a, b):
+            if s not in seqs:
+                seqs.append(s)
+    probe = cpu_sample_seconds(prepare_cpu_sample(w, seqs[:2], slots, seed))
+    n = max(2, min(S, int(budget_s / max(probe / 2, 1e-3))))
+    x = prepare_cpu_sample(w, seqs[:n], slots, seed)
+    secs = cpu_sample_seconds(x)
+    return {"value": x["kv_bytes"] / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of the {S} sequences (all 40 heads, {int(x['lens'].sum())} tokens), "
+                      f"new-token writes + fp64 attention, numpy single-threaded, {secs:.1f} s"}
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def config_block(extra=None):
+    c = {"workload": WORKLOAD, "num_seqs": S, "num_heads": H, "head_dim": D, "block_size": B,
+         "context_lens": "U[128,2048] seed 1002 (+7919*rank)", "kv_storage": "f16",
+         "l2": "inputs larger than L2: ~1.4 GB of K/V read per step vs 129 MB L2"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args, rank):
+    """The oracle, as it stands, on the host cores: each step one sequence of the workload."""
+    if rank != 0:
+        return None
+    w, slots, pairs, _ = build_step_inputs(SEED)
+    order = [int(x) for x in np.random.default_rng(0).permutation(S)][:8]
+    samples = [prepare_cpu_sample(w, [s], slots, SEED) for s in order]   # generated once, untimed
+    for i in range(args.warmup):
+        cpu_sample_seconds(samples[i % len(samples)])
+    secs, kv = 0.0, 0
+    for i in range(args.steps):
+        x = samples[i % len(samples)]
+        secs += cpu_sample_seconds(x)
+        kv += x["kv_bytes"]
+    value = kv / secs / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": config_block({"reference_sample": "one sequence (all 40 heads) of the batch per step, 8 cycled"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "one sequence per step, cycling over 8 of the 64; new-token write + fp64 attention"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}), flush=True)
+        sys.exit(1)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(SEED)                      # before any timing: the oracle runs alone
+
+    from paged_kv_cache_73_gb300 import binding as pkv
+    pkv.load()
+    r = run_gpu(args, rank, world, dev)
+
+    # whole-job numbers: bytes of all ranks over the slowest rank's time
+    t = torch.tensor([r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"]], dtype=torch.float64, device=dev)
+    b = torch.tensor([float(r["kv_bytes"])], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    step_ms, e2e_ms, attn_ms = (float(x) for x in t.tolist())
+    kv_total = float(b.item())
+
+    if rank == 0:
+        peak, peak_src = measured_hbm_peak()
+        achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
+        sha = attention_source_sha()
+        traffic = NCU_TRAFFIC.get(sha)
+        value = kv_total / (step_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
+            "config": config_block({"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                    "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"]}),
+            "hbm_frac_of_measured": value / peak,
+            "tokens_per_s": S * world / (step_ms * 1e-3),
+            "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
+            "host_slot_assignment_us": r["host_slot_us"],
+            "roofline": {"bound": "hbm", "kernel": "paged attention call (partition + merge kernels)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
+                         "launch_ms": attn_ms, "peak_source": peak_src + ", of measured"},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+        }
+        if "e2e_step_ms" in r:
+            line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                           "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                           "ms_per_step": e2e_ms}
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -107,6 +107,14 @@ int pkv_device_error(void* stream, int reset, int* code);
 size_t pkv_paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
                                           int max_blocks_per_seq, int block_size);
 
+/* The launch plan pkv_paged_attention_decode uses on the current device for
+ * these sizes: *part_tokens receives the context partition length (tokens per
+ * CTA) and *num_kernels the kernels one call launches (1, or 2 when a
+ * sequence may span several partitions and a merge pass follows).  Host only;
+ * queries the device's SM count once. */
+int pkv_paged_attention_plan(int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
+                             int block_size, int* part_tokens, int* num_kernels);
+
 int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                                const int32_t* block_tables, const int32_t* context_lens,
                                int num_seqs, int num_heads, int head_dim, int num_blocks,

@@ -51,6 +51,7 @@ _SIGNATURES = {
     "pkv_version": (_I, []),
     "pkv_device_error": (_I, [_P, _I, _c.POINTER(_I)]),
     "pkv_paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_plan": (_I, [_I, _I, _I, _I, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I, _P, _P, _SZ, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
@@ -141,6 +142,16 @@ def paged_attention_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
                                    block_size: int) -> int:
     return int(load().pkv_paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_blocks_per_seq,
                                                          block_size))
+
+
+def paged_attention_plan(num_seqs: int, num_heads: int, head_dim: int, max_blocks_per_seq: int,
+                         block_size: int) -> Tuple[int, int]:
+    """(partition tokens, kernels per call) that paged_attention_decode will use on this device."""
+    pt = _c.c_int(0)
+    nk = _c.c_int(0)
+    _check(load().pkv_paged_attention_plan(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size,
+                                           ctypes.byref(pt), ctypes.byref(nk)))
+    return pt.value, nk.value
 
 
 def workspace_for(num_seqs: int, num_heads: int, head_dim: int, max_blocks_per_seq: int, block_size: int,

@@ -529,6 +529,24 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_heads, int head_
   return static_cast<size_t>(num_seqs) * num_heads * parts * (head_dim + 2) * sizeof(float);
 }
 
+int pkv_paged_attention_plan(int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq, int block_size,
+                             int* part_tokens, int* num_kernels) {
+  if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || !part_tokens || !num_kernels)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_plan: bad argument");
+  if ((head_dim != 64 && head_dim != 128) ||
+      (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32))
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_plan: head_dim %d / block_size %d", head_dim,
+                     block_size);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const int max_ctx = max_blocks_per_seq * block_size;
+  const int pt = choose_part_tokens(num_seqs, num_heads, max_ctx, device_sms(dev));
+  *part_tokens = pt;
+  *num_kernels = num_seqs == 0 ? 0 : ((max_ctx + pt - 1) / pt > 1 ? 2 : 1);
+  pkv::clear_error();
+  return PKV_OK;
+}
+
 int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                                const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq, float scale,

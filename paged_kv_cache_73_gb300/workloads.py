@@ -359,3 +359,16 @@ def new_tokens(num_tokens: int, num_heads: int, head_dim: int, seed: int, device
 def free_list_order(num_blocks: int, seed: int) -> np.ndarray:
     """The seeded order in which a block manager hands out physical ids (the 'shuffled pool')."""
     return np.random.default_rng(seed).permutation(num_blocks).astype(np.int32)
+
+
+def from_tables(name: str, seed: int, num_heads: int, head_dim: int, block_size: int, num_blocks: int,
+                block_tables: np.ndarray, context_lens: np.ndarray, notes: str = "") -> DecodeWorkload:
+    """A workload over tables made elsewhere (e.g. by a block manager); -1 pads each row."""
+    rows = []
+    for s in range(block_tables.shape[0]):
+        ctx = int(context_lens[s])
+        nb = _blocks_for(ctx, block_size)
+        rows.append((ctx, [int(b) for b in block_tables[s, :nb]]))
+    w = _assemble(name, seed, num_heads, head_dim, block_size, num_blocks, rows, notes)
+    w.block_tables = np.ascontiguousarray(block_tables.astype(np.int32))
+    return w
