@@ -335,6 +335,18 @@ def run_cpu_baseline(seed: int, budget_s: float = 12.0):
                       f"new-token writes + fp64 attention, numpy single-threaded, {secs:.1f} s"}
 
 
+def reduce_over_ranks(maxed, summed, world, device):
+    """Max over ranks of `maxed` (times), sum over ranks of `summed` (bytes)."""
+    import torch
+    t = torch.tensor(list(maxed), dtype=torch.float64, device=device)
+    b = torch.tensor(list(summed), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], [float(x) for x in b.tolist()]
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -406,14 +418,8 @@ def main():
     r = run_gpu(args, rank, world, dev)
 
     # whole-job numbers: bytes of all ranks over the slowest rank's time
-    t = torch.tensor([r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"]], dtype=torch.float64, device=dev)
-    b = torch.tensor([float(r["kv_bytes"])], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(b, op=dist.ReduceOp.SUM)
-    step_ms, e2e_ms, attn_ms = (float(x) for x in t.tolist())
-    kv_total = float(b.item())
+    (step_ms, e2e_ms, attn_ms), (kv_total,) = reduce_over_ranks(
+        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"]], [float(r["kv_bytes"])], world, dev)
 
     if rank == 0:
         peak, peak_src = measured_hbm_peak()
