@@ -122,6 +122,38 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged decode attention with the library's own scratch (no counterpart in the
+ * paper: an addition of this library for callers that cannot allocate).
+ *
+ * Callers without a device allocator of their own (a plain C host program, a
+ * plugin inside an engine that has reserved all device memory for its block
+ * pools) or on a path that must not pay for the device-wide synchronisation of
+ * cudaMalloc/cudaFree use this instead of pkv_paged_attention_decode.  It takes
+ * the same arguments minus the workspace, computes the same result, and keeps
+ * the scratch in a fixed array of pkv_paged_attention_static_workspace_bytes()
+ * bytes (16 MiB) inside the library; every device that loads the library holds
+ * that array until the process exits.  It allocates nothing.
+ *
+ *   - A batch whose scratch would exceed the array is rejected with
+ *     PKV_ERR_WORKSPACE (and a message) before anything is launched.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress with the device current); make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Nothing in it needs clearing: each call writes every partial
+ *     result before reading it.  Calls whose kernels overlap on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race on the array: order them on one stream.
+ * ------------------------------------------------------------------------- */
+size_t pkv_paged_attention_static_workspace_bytes(void);
+
+int pkv_paged_attention_decode_static_workspace(const uint16_t* q, const uint16_t* k_cache,
+                                                const uint16_t* v_cache, const int32_t* block_tables,
+                                                const int32_t* context_lens, int num_seqs, int num_heads,
+                                                int head_dim, int num_blocks, int max_blocks_per_seq,
+                                                float scale, int block_size, uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Reshape and cache ([note] 关键设计 5, "fused reshape and block write").
  *
  * For every token t < num_tokens with slot = slot_mapping[t] >= 0:

@@ -53,6 +53,9 @@ _SIGNATURES = {
     "pkv_paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_plan": (_I, [_I, _I, _I, _I, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I, _P, _P, _SZ, _P]),
+    "pkv_paged_attention_static_workspace_bytes": (_SZ, []),
+    "pkv_paged_attention_decode_static_workspace": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I,
+                                                         _P, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_bm_create": (_P, [_I, _I, _P]),
@@ -188,6 +191,33 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     _check(load().pkv_paged_attention_decode(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
         S, H, D, N, max_blocks, float(scale), block_size, out.data_ptr(), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+    return out
+
+
+def paged_attention_static_workspace_bytes() -> int:
+    return int(load().pkv_paged_attention_static_workspace_bytes())
+
+
+def paged_attention_decode_static_workspace(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                            block_size: int, out: Optional[torch.Tensor] = None,
+                                            stream=None) -> torch.Tensor:
+    """paged_attention_decode for callers that cannot allocate device memory: the library's
+    fixed scratch array replaces the workspace (see include/pkv.h for its limit and sharing)."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    S, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, 3)
+    _check(load().pkv_paged_attention_decode_static_workspace(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+        S, H, D, k_cache.shape[0], block_tables.shape[1], float(scale), block_size, out.data_ptr(),
         _stream(stream)))
     return out
 

@@ -609,3 +609,82 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
 }
 
 }  // extern "C"
+
+// ---- decode attention with library-owned scratch ------------------------------------------------
+//
+// Some callers cannot allocate device memory for the workspace: a plain C host
+// program or a plugin that has no device allocator of its own, an engine that
+// has already reserved all device memory for its block pools, or a path that
+// must not pay for the device-wide synchronisation cudaMalloc/cudaFree imply.
+// For them this entry point keeps the split-over-context scratch in a fixed
+// array inside the library instead.
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;  // 16 MiB, held on every device that loads the library
+
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+// Device address of g_static_workspace on `dev` (looked up once per device, with
+// that device current); nullptr with the status in *rc on failure.
+void* static_workspace_address(int dev, int* rc) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  std::lock_guard<std::mutex> g(mu);
+  if (dev < 0 || dev >= 64) {
+    *rc = pkv::fail(PKV_ERR_UNSUPPORTED, "static-workspace attention: device ordinal %d above 63", dev);
+    return nullptr;
+  }
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+    if (e != cudaSuccess || ptr == nullptr) {
+      *rc = pkv::fail(PKV_ERR_CUDA, "static-workspace attention: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      return nullptr;
+    }
+    addr[dev] = ptr;
+  }
+  *rc = PKV_OK;
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_paged_attention_static_workspace_bytes(void) { return kStaticWorkspaceBytes; }
+
+int pkv_paged_attention_decode_static_workspace(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                int num_seqs, int num_heads, int head_dim, int num_blocks,
+                                                int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
+                                                void* stream) {
+  if (num_seqs <= 0 || num_heads <= 0 || max_blocks_per_seq <= 0)
+    return pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
+                                      head_dim, num_blocks, max_blocks_per_seq, scale, block_size, out, nullptr, 0,
+                                      stream);
+  int part_tokens = 0, kernels = 0;
+  int rc = pkv_paged_attention_plan(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size, &part_tokens,
+                                    &kernels);
+  if (rc != PKV_OK) return rc;
+  const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+  const long long parts = (max_ctx + part_tokens - 1) / part_tokens;
+  const unsigned long long need =
+      parts > 1 ? static_cast<unsigned long long>(num_seqs) * num_heads * parts * (head_dim + 2) * sizeof(float) : 0;
+  if (need > kStaticWorkspaceBytes)
+    return pkv::fail(PKV_ERR_WORKSPACE,
+                     "pkv_paged_attention_decode_static_workspace: this batch needs %llu bytes of scratch, above "
+                     "the library's fixed %zu; use pkv_paged_attention_decode with a caller workspace",
+                     need, kStaticWorkspaceBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return pkv::fail(PKV_ERR_CUDA, "pkv_paged_attention_decode_static_workspace: cudaGetDevice: %s",
+                     cudaGetErrorString(e));
+  void* ws = static_workspace_address(dev, &rc);
+  if (!ws) return rc;
+  return pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads, head_dim,
+                                    num_blocks, max_blocks_per_seq, scale, block_size, out, ws,
+                                    kStaticWorkspaceBytes, stream);
+}
+
+}  // extern "C"
