@@ -15,6 +15,13 @@ the same C-ABI calls.  `roofline` is the paged attention call alone against
 the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                  [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity]
+                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F]
+
+The default workload is the headline one above.  The others build their batch
+through the same block manager (prompt forks with copy-on-write, a shared
+prefix, full 2048-token contexts); their copy-on-write copies are timed as
+one copy_blocks call (`copy_blocks_setup`).
 
 --impl reference times the CPU oracle on the host cores instead (a bounded
 sample of the same workload per step) and prints the same metric.
@@ -44,10 +51,11 @@ WORKLOAD = ("opt13b_decode_step: 64 seqs, 40 heads x 128, block 16, ctx ~ U[128,
             "+ reshape_and_cache of 64 new tokens")
 SEED = 1002
 FALLBACK_HBM_GBS = 6800.0
+EVENT_EVERY = 16
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call (partition + merge
-# kernels) from an ncu capture of this workload, keyed by the sha256 of the attention source it
-# was taken on; a changed kernel reports null until it is captured again.
+# kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
+# on); a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {}
 
 
@@ -59,6 +67,12 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop (profiling runs)")
+    ap.add_argument("--workload", choices=WORKLOADS, default="opt13b",
+                    help="opt13b (the headline batch) or another decode batch of the same shape family")
+    ap.add_argument("--capacity-seqs", type=int, default=64, help="capacity workload: sequences (ctx 2048 each)")
+    ap.add_argument("--capacity-block", type=int, default=16, help="capacity workload: block size")
+    ap.add_argument("--pool-frac", type=float, default=0.0,
+                    help="capacity workload: size the pool to this fraction of free HBM (0 = just enough)")
     return ap.parse_args()
 
 
@@ -140,38 +154,97 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows), "reasons": sorted(reasons)}
 
 
-# ---- workload ----------------------------------------------------------------------------------
 
-H, D, B, S = 40, 128, 16, 64
-MAX_BLOCKS = 2048 // B
+# ---- workloads -------------------------------------------------------------------------------------
+
+WORKLOADS = ("opt13b", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity")
 
 
-def attention_algorithmic_bytes(lens) -> int:
+def attention_algorithmic_bytes(w) -> int:
     """K/V rows read + q read + out written + table entries + context lengths, per call."""
+    H, D, B = w.num_heads, w.head_dim, w.block_size
     total = 0
-    for c in lens:
+    for c in w.context_lens:
         c = int(c)
         total += H * (2 * c * D * 2 + 2 * D * 2) + 4 * math.ceil(c / B) + 4
     return total
 
 
-def build_step_inputs(seed: int):
-    """Block tables and new-token slots from the host block manager, over the recipe's lengths."""
+def _grow(bm, seqs, targets):
+    """Append tokens to `seqs` until each holds targets[i] - 1 tokens; returns the copies made."""
+    copies = []
+    have = {s: bm.block_table(s)[1] for s in seqs}
+    while True:
+        live = [s for s, t in zip(seqs, targets) if have[s] < t - 1]
+        if not live:
+            return copies
+        _, pairs = bm.append_slots(live)
+        copies += [tuple(int(x) for x in p) for p in pairs]
+        for s in live:
+            have[s] += 1
+
+
+def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 64, capacity_block: int = 16,
+                      pool_blocks=None):
+    """A decode step's batch built through the host block manager over the recipe's lengths.
+
+    Every sequence is grown to ctx - 1 tokens (prefill, forks, copy-on-write and
+    earlier decode tokens as the workload prescribes), then one append per
+    sequence gives this step's new-token slots and copy pairs.
+    Returns a dict: w (DecodeWorkload over the manager's tables), slots, pairs
+    (this step's copies), setup_pairs (copies made while growing), host_us,
+    desc.
+    """
     from paged_kv_cache_73_gb300 import binding as pkv
     from paged_kv_cache_73_gb300 import workloads as wl
-    recipe = wl.opt13b(seed=seed)
+
+    if workload == "opt13b":
+        recipe = wl.opt13b(seed=seed)
+    elif workload in ("parallel_sampling", "parallel_sampling_cow"):
+        recipe = wl.parallel_sampling(seed=seed, prompt_len=512 if workload == "parallel_sampling" else 511)
+    elif workload == "shared_prefix":
+        recipe = wl.shared_prefix(seed=seed)
+    elif workload == "capacity":
+        recipe = wl.capacity(seed=seed, num_seqs=capacity_seqs, block_size=capacity_block, num_blocks=pool_blocks)
+    else:
+        raise ValueError(workload)
+    H, D, B = recipe.num_heads, recipe.head_dim, recipe.block_size
     lens = recipe.context_lens
+    S = len(lens)
     N = recipe.num_blocks
     bm = pkv.BlockManager(N, B, wl.free_list_order(N, seed))
-    for s in range(S):
-        bm.add_seq(s, int(lens[s]) - 1)                 # prompt and earlier tokens
+    seqs = list(range(S))
+    setup = []
+    if workload.startswith("parallel_sampling"):
+        n, prompt = 4, 512 if workload == "parallel_sampling" else 511
+        for base in range(0, S, n):
+            bm.add_seq(base, prompt)
+            for i in range(1, n):
+                bm.fork(base, base + i)
+        setup = _grow(bm, seqs, lens)
+    elif workload == "shared_prefix":
+        bm.register_prefix(0, 1024)
+        for s in seqs:
+            bm.add_seq_with_prefix(s, 0)
+        setup = _grow(bm, seqs, lens)
+    else:
+        for s in seqs:
+            bm.add_seq(s, int(lens[s]) - 1)
     t0 = time.perf_counter()
-    slots, pairs = bm.append_slots(list(range(S)))      # slot assignment of this step's token
+    slots, pairs = bm.append_slots(seqs)                # slot assignment of this step's token
     host_us = (time.perf_counter() - t0) * 1e6
-    tables, ctx = bm.block_tables(list(range(S)), MAX_BLOCKS)
+    max_blocks = -(-2048 // B) if workload == "opt13b" else -(-int(lens.max()) // B)
+    tables, ctx = bm.block_tables(seqs, max_blocks)
     assert np.array_equal(ctx, lens)
-    w = wl.from_tables("opt13b_decode_step", seed, H, D, B, N, tables, ctx, recipe.notes)
-    return w, slots, pairs, host_us
+    w = wl.from_tables(f"{workload}_decode_step", seed, H, D, B, N, tables, ctx, recipe.notes)
+    if workload == "capacity":
+        desc = f"capacity: {S} seqs x ctx 2048, 40 x 128, block {B}, {N} pool blocks, shuffled"
+    elif workload == "opt13b":
+        desc = WORKLOAD
+    else:
+        desc = f"{workload}: {recipe.notes}, 40 x 128, block {B}, shuffled blocks"
+    return {"w": w, "slots": slots, "pairs": pairs, "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2),
+            "host_us": host_us, "desc": desc, "workload": workload}
 
 
 def run_gpu(args, rank, world, dev):
@@ -180,7 +253,10 @@ def run_gpu(args, rank, world, dev):
     from paged_kv_cache_73_gb300 import workloads as wl
 
     seed = SEED + 7919 * rank                           # weak scaling: each rank its own batch
-    w, slots, pairs, host_us = build_step_inputs(seed)
+    x = build_step_inputs(seed, args.workload, args.capacity_seqs, args.capacity_block,
+                          pool_blocks_for(args, dev))
+    w, slots, pairs = x["w"], x["slots"], x["pairs"]
+    S, H, D, B, MB = w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq
     k, v = w.pools(dev)
     q = w.q(dev)
     key, value = wl.new_tokens(S, H, D, seed, dev)
@@ -189,10 +265,26 @@ def run_gpu(args, rank, world, dev):
     slots_d = torch.from_numpy(slots).to(dev)
     pairs_d = torch.from_numpy(np.ascontiguousarray(pairs)).to(dev)
     out = torch.empty_like(q)
-    ws = pkv.workspace_for(S, H, D, MAX_BLOCKS, B, dev)
-    part_tokens, attn_kernels = pkv.paged_attention_plan(S, H, D, MAX_BLOCKS, B)
+    ws = pkv.workspace_for(S, H, D, MB, B, dev)
+    part_tokens, attn_kernels = pkv.paged_attention_plan(S, H, D, MB, B)
     stream = torch.cuda.current_stream()
     n_pairs = int(pairs.shape[0])
+
+    copy = None
+    if len(x["setup_pairs"]):
+        # the copy-on-write copies made while the batch grew, as one copy_blocks call
+        sp = torch.from_numpy(np.ascontiguousarray(x["setup_pairs"])).to(dev)
+        for _ in range(5):
+            pkv.copy_blocks([k], [v], sp, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(20):
+            pkv.copy_blocks([k], [v], sp, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / 20
+        moved = 2 * 2 * len(sp) * H * B * D * 2           # K and V, read and written
+        copy = {"pairs": int(len(sp)), "ms": ms, "GB/s": moved / (ms * 1e-3) / 1e9}
 
     def step(ev0=None, ev1=None):
         if n_pairs:
@@ -210,31 +302,48 @@ def run_gpu(args, rank, world, dev):
     assert pkv.device_error() == 0
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # events around the attention call on every EVENT_EVERY-th step only: an event between two
+    # kernels stops the next launch from overlapping the previous kernel's tail (PDL)
+    n_ev = (K + EVENT_EVERY - 1) // EVENT_EVERY
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
         start.record(stream)
         for i in range(K):
-            step(*ev[i])
+            if i % EVENT_EVERY == 0:
+                step(*ev[i // EVENT_EVERY])
+            else:
+                step()
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     step_ms = start.elapsed_time(stop) / K
     attn_ms = [a.elapsed_time(b) for a, b in ev]
-    attn_mean = sum(attn_ms) / K
     code = pkv.device_error()
     assert code == 0, f"device check {code}"
 
-    res = {"step_ms": step_ms, "attn_ms": attn_mean, "attn_ms_median": statistics.median(attn_ms),
-           "kv_bytes": w.logical_kv_bytes(), "attn_bytes": attention_algorithmic_bytes(w.context_lens),
+    res = {"step_ms": step_ms, "attn_ms": sum(attn_ms) / len(attn_ms), "attn_ms_median": statistics.median(attn_ms),
+           "kv_bytes": w.logical_kv_bytes(), "phys_bytes": w.physical_kv_bytes(),
+           "attn_bytes": attention_algorithmic_bytes(w), "num_seqs": S,
            "launches": K * ((1 if n_pairs else 0) + 1 + attn_kernels), "part_tokens": part_tokens,
-           "host_slot_us": host_us, "clocks": clocks.summary(), "n_pairs": n_pairs}
-
+           "host_slot_us": x["host_us"], "clocks": clocks.summary(), "n_pairs": n_pairs, "copy": copy,
+           "desc": x["desc"], "num_blocks": w.num_blocks}
     if not args.no_e2e:
         res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws))
     return res
+
+
+def pool_blocks_for(args, dev):
+    """Pool size for the capacity workload: a fraction of free HBM, or just enough."""
+    if args.workload != "capacity" or args.pool_frac <= 0:
+        return None
+    import torch
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info(dev)
+    per_block = 2 * 40 * args.capacity_block * 128 * 2
+    return int(args.pool_frac * free / per_block)
 
 
 def physical_gpu_index(local: int) -> int:
@@ -276,7 +385,7 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
         if n_pairs:
             pkv.copy_blocks([k], [v], dbuf["pairs"], stream=stream)
         pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=stream)
-        pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, B, out=out_d,
+        pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, w.block_size, out=out_d,
                                    workspace=ws, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
         stream.synchronize()
@@ -296,6 +405,7 @@ def prepare_cpu_sample(w, seqs, slots, seed):
     """Host inputs of the oracle for sequences `seqs` of the step (generated once, untimed)."""
     from paged_kv_cache_73_gb300 import workloads as wl
 
+    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
     kc, vc, tabs, lens = w.compact_pools(seqs)
     key, value = wl.new_tokens(S, H, D, seed, "cpu")
     # the new tokens' slots re-expressed in the compact pool's block numbering
@@ -318,20 +428,22 @@ def cpu_sample_seconds(x):
     return time.perf_counter() - t0
 
 
-def run_cpu_baseline(seed: int, budget_s: float = 12.0):
-    w, slots, pairs, _ = build_step_inputs(seed)
+def run_cpu_baseline(args, budget_s: float = 12.0):
+    x0 = build_step_inputs(SEED, args.workload, args.capacity_seqs, args.capacity_block)
+    w, slots = x0["w"], x0["slots"]
+    S = w.num_seqs
     order = [int(x) for x in np.argsort(w.context_lens)[::-1]]
     seqs = []
     for a, b in zip(order, order[::-1]):               # alternate long and short sequences
         for s in (a, b):
             if s not in seqs:
                 seqs.append(s)
-    probe = cpu_sample_seconds(prepare_cpu_sample(w, seqs[:2], slots, seed))
+    probe = cpu_sample_seconds(prepare_cpu_sample(w, seqs[:2], slots, SEED))
     n = max(2, min(S, int(budget_s / max(probe / 2, 1e-3))))
-    x = prepare_cpu_sample(w, seqs[:n], slots, seed)
+    x = prepare_cpu_sample(w, seqs[:n], slots, SEED)
     secs = cpu_sample_seconds(x)
     return {"value": x["kv_bytes"] / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} of the {S} sequences (all 40 heads, {int(x['lens'].sum())} tokens), "
+            "sample": f"{n} of the {S} sequences (all {w.num_heads} heads, {int(x['lens'].sum())} tokens), "
                       f"new-token writes + fp64 attention, numpy single-threaded, {secs:.1f} s"}
 
 
@@ -353,10 +465,11 @@ def barrier(world):
         dist.barrier()
 
 
-def config_block(extra=None):
-    c = {"workload": WORKLOAD, "num_seqs": S, "num_heads": H, "head_dim": D, "block_size": B,
-         "context_lens": "U[128,2048] seed 1002 (+7919*rank)", "kv_storage": "f16",
-         "l2": "inputs larger than L2: ~1.4 GB of K/V read per step vs 129 MB L2"}
+def config_block(args, desc, num_seqs, extra=None):
+    c = {"workload": desc, "num_seqs": num_seqs, "num_heads": 40, "head_dim": 128,
+         "block_size": args.capacity_block if args.workload == "capacity" else 16,
+         "seed": f"{SEED} (+7919*rank)", "kv_storage": "f16",
+         "l2": "inputs larger than L2: the step reads far more K/V than the 129 MB L2"}
     if extra:
         c.update(extra)
     return c
@@ -366,8 +479,9 @@ def run_reference(args, rank):
     """The oracle, as it stands, on the host cores: each step one sequence of the workload."""
     if rank != 0:
         return None
-    w, slots, pairs, _ = build_step_inputs(SEED)
-    order = [int(x) for x in np.random.default_rng(0).permutation(S)][:8]
+    x0 = build_step_inputs(SEED, args.workload, args.capacity_seqs, args.capacity_block)
+    w, slots = x0["w"], x0["slots"]
+    order = [int(x) for x in np.random.default_rng(0).permutation(w.num_seqs)][:8]
     samples = [prepare_cpu_sample(w, [s], slots, SEED) for s in order]   # generated once, untimed
     for i in range(args.warmup):
         cpu_sample_seconds(samples[i % len(samples)])
@@ -377,13 +491,14 @@ def run_reference(args, rank):
         secs += cpu_sample_seconds(x)
         kv += x["kv_bytes"]
     value = kv / secs / 1e9
+    sample = f"one sequence (all {w.num_heads} heads) per step, cycling over {len(samples)} of the {w.num_seqs}"
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded counter-based generator)",
-            "config": config_block({"reference_sample": "one sequence (all 40 heads) of the batch per step, 8 cycled"}),
+            "config": config_block(args, x0["desc"], w.num_seqs, {"reference_sample": sample}),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "one sequence per step, cycling over 8 of the 64; new-token write + fp64 attention"},
+                             "sample": sample + "; new-token write + fp64 attention"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -411,39 +526,46 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = run_cpu_baseline(SEED)                      # before any timing: the oracle runs alone
+        cpu = run_cpu_baseline(args)                      # before any timing: the oracle runs alone
 
     from paged_kv_cache_73_gb300 import binding as pkv
     pkv.load()
     r = run_gpu(args, rank, world, dev)
 
     # whole-job numbers: bytes of all ranks over the slowest rank's time
-    (step_ms, e2e_ms, attn_ms), (kv_total,) = reduce_over_ranks(
-        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"]], [float(r["kv_bytes"])], world, dev)
+    (step_ms, e2e_ms, attn_ms), (kv_total, phys_total) = reduce_over_ranks(
+        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"]], [float(r["kv_bytes"]), float(r["phys_bytes"])],
+        world, dev)
 
     if rank == 0:
         peak, peak_src = measured_hbm_peak()
         achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
-        sha = attention_source_sha()
-        traffic = NCU_TRAFFIC.get(sha)
+        traffic = NCU_TRAFFIC.get((args.workload, attention_source_sha()))
         value = kv_total / (step_ms * 1e-3) / 1e9
+        S = r["num_seqs"]
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
-            "config": config_block({"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                    "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"]}),
+            "config": config_block(args, r["desc"], S,
+                                   {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                    "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"],
+                                    "pool_blocks": r["num_blocks"]}),
             "hbm_frac_of_measured": value / peak,
+            "physical_kv_GBps": phys_total / (step_ms * 1e-3) / 1e9,
             "tokens_per_s": S * world / (step_ms * 1e-3),
             "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
             "host_slot_assignment_us": r["host_slot_us"],
             "roofline": {"bound": "hbm", "kernel": "paged attention call (partition + merge kernels)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
-                         "launch_ms": attn_ms, "peak_source": peak_src + ", of measured"},
+                         "launch_ms": attn_ms, "timed_launches": (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
+                         "peak_source": peak_src + ", of measured"},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
+        if r["copy"] is not None:
+            line["copy_blocks_setup"] = r["copy"]
         if "e2e_step_ms" in r:
             line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                            "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],

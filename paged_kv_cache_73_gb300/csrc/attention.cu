@@ -9,7 +9,7 @@
 //
 // GB300 design (decode attention is a batched GEMV: ~1 flop per byte, so HBM
 // bandwidth is the roofline and no tensor cores are used):
-//  * The context is split into partitions of `part_tokens` tokens; one CTA
+//  * The context is split into partitions of `part_tokens` (128..1024) tokens; one CTA
 //    handles one (partition, head, sequence).  A second tiny kernel merges the
 //    partitions of a (sequence, head) with the log-sum-exp identity
 //    m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p 2^(m_p - m) / l.
@@ -35,6 +35,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "launch.cuh"
 #include "pkv_internal.h"
 
 namespace {
@@ -85,10 +86,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   }
   return false;
 }
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+// 1-D bulk copy global -> this CTA's shared memory, completion counted on `bar`.
+// K/V tiles are streamed once per (sequence, head), so they are marked first to
+// leave L2 (evict_first); a block shared by many sequences still hits in L2
+// while it is being reused.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -224,6 +236,8 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
 
   const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pkv::pdl_trigger();
+  pkv::pdl_wait();  // inputs may come from the previous kernel on the stream
   const int B = p.block_size;
   const int H = p.num_heads;
   const int max_ctx = p.max_blocks * B;
@@ -297,6 +311,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const unsigned char* kbase = reinterpret_cast<const unsigned char*>(p.k);
   const unsigned char* vbase = reinterpret_cast<const unsigned char*>(p.v);
 
+  const uint64_t policy = l2_evict_first_policy();
   auto issue = [&](int k) {
     const int stage = k % NST;
     const int i = warp + k * NW;
@@ -304,8 +319,8 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     const uint32_t bar = wbar + stage * 8;
     const uint32_t dst = smem_u32(wring + stage * C::STAGE_BYTES);
     mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
-    bulk_copy_g2s(dst, kbase + off, C::CHUNK_BYTES, bar);
-    bulk_copy_g2s(dst + C::CHUNK_BYTES, vbase + off, C::CHUNK_BYTES, bar);
+    bulk_copy_g2s(dst, kbase + off, C::CHUNK_BYTES, bar, policy);
+    bulk_copy_g2s(dst + C::CHUNK_BYTES, vbase + off, C::CHUNK_BYTES, bar, policy);
   };
 
   int issued = 0;
@@ -402,29 +417,66 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   }
 }
 
-// Merge the partitions of every (sequence, head) that has more than one.
+// Merge the partitions of every (sequence, head) that has more than one: one
+// warp per (sequence, head); lanes read the partitions' (m, l) in parallel and
+// each lane owns D/32 output columns, read as one vector per partition.
 template <int D>
-__global__ void __launch_bounds__(D) paged_attention_merge_kernel(const AttnParams p) {
-  const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
+__global__ void __launch_bounds__(128) paged_attention_merge_kernel(const AttnParams p) {
+  pkv::pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 4 + warp, s = blockIdx.y;
+  if (h >= p.num_heads) return;
   const int ctx = p.lens[s];
   const int nparts = num_parts(ctx, p.max_blocks * p.block_size, p.part_tokens);
   if (nparts <= 1) return;
   const size_t w0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_parts;
   float M = -INFINITY;
-  for (int i = 0; i < nparts; ++i) M = fmaxf(M, p.ws_ml[2 * (w0 + i)]);
-  float L = 0.f, O = 0.f;
-  for (int i = 0; i < nparts; ++i) {
-    const float mi = p.ws_ml[2 * (w0 + i)];
-    const float wgt = mi == -INFINITY ? 0.f : exp2f(mi - M);
-    L = fmaf(p.ws_ml[2 * (w0 + i) + 1], wgt, L);
-    O = fmaf(p.ws_o[(w0 + i) * D + d], wgt, O);
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[2 * (w0 + i)]);
+#pragma unroll
+  for (int o = 16; o > 0; o /= 2) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+  constexpr int V = D / 32;
+  float acc[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) acc[c] = 0.f;
+  float L = 0.f;
+  for (int base = 0; base < nparts; base += 32) {
+    const int i = base + lane;
+    const float mi = i < nparts ? p.ws_ml[2 * (w0 + i)] : -INFINITY;
+    const float wi = mi == -INFINITY ? 0.f : exp2f(mi - M);
+    if (i < nparts) L = fmaf(p.ws_ml[2 * (w0 + i) + 1], wi, L);
+    const int n = min(32, nparts - base);
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(FULL, wi, j);
+      const float* src = p.ws_o + (w0 + base + j) * D + lane * V;
+      if constexpr (V == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] = fmaf(wj, x.x, acc[0]);
+        acc[1] = fmaf(wj, x.y, acc[1]);
+        acc[2] = fmaf(wj, x.z, acc[2]);
+        acc[3] = fmaf(wj, x.w, acc[3]);
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(wj, x.x, acc[0]);
+        acc[1] = fmaf(wj, x.y, acc[1]);
+      }
+    }
   }
-  const float o = L > 0.f ? O / L : 0.f;
-  p.out[(static_cast<size_t>(s) * p.num_heads + h) * D + d] = __float2half_rn(o);
+#pragma unroll
+  for (int o = 16; o > 0; o /= 2) L += __shfl_xor_sync(FULL, L, o);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __half* dst = p.out + (static_cast<size_t>(s) * p.num_heads + h) * D + lane * V;
+#pragma unroll
+  for (int c = 0; c < V; c += 2) {
+    *reinterpret_cast<__half2*>(dst + c) = __floats2half2_rn(acc[c] * inv, acc[c + 1] * inv);
+  }
 }
+
+// Floats of the (m, l) block of the workspace, padded so the partial outputs start 16-byte aligned.
+__host__ __device__ constexpr size_t ws_ml_floats(size_t pairs) { return (pairs * 2 + 3) / 4 * 4; }
 
 // ---- host side ---------------------------------------------------------------------------------
 constexpr int kMinPartTokens = 128;
+constexpr int kMaxPartTokens = 1024;
 
 template <int D, int R>
 constexpr size_t smem_bytes(int part_tokens) {
@@ -454,16 +506,16 @@ cudaError_t prepare_kernel(int dev) {
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes<D, R>(512)));
+                                       static_cast<int>(smem_bytes<D, R>(kMaxPartTokens)));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
 int choose_part_tokens(int num_seqs, int num_heads, int max_ctx, int sms) {
-  // Enough CTAs for about two full waves at three CTAs per SM; longer partitions
-  // otherwise (less merge traffic, fewer pipeline fills).
+  // The longest partition that still gives about two full waves at three CTAs
+  // per SM (fewer pipeline fills and less merge traffic per byte read).
   const long long target = 2LL * 3 * sms;
-  for (int pt : {512, 256}) {
+  for (int pt : {1024, 512, 256}) {
     const long long ctas = static_cast<long long>(num_seqs) * num_heads * ((max_ctx + pt - 1) / pt);
     if (ctas >= target) return pt;
   }
@@ -480,21 +532,23 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
   p.part_tokens = part_tokens;
   p.max_parts = (max_ctx + part_tokens - 1) / part_tokens;
   if (p.max_parts > 1) {
-    const size_t need = static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts * (D + 2) * sizeof(float);
+    const size_t pairs = static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts;
+    const size_t need = (ws_ml_floats(pairs) + pairs * D) * sizeof(float);
     if (ws == nullptr || ws_bytes < need)
       return pkv::fail(PKV_ERR_WORKSPACE, "paged attention: workspace of %zu bytes needed, %zu given", need,
                        ws == nullptr ? static_cast<size_t>(0) : ws_bytes);
     p.ws_ml = static_cast<float*>(ws);
-    p.ws_o = p.ws_ml + static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts * 2;
+    p.ws_o = p.ws_ml + ws_ml_floats(pairs);
   }
   dim3 grid(p.max_parts, p.num_heads, num_seqs);
-  paged_attention_partition_kernel<D, R>
-      <<<grid, Cfg<D, R>::NW * 32, smem_bytes<D, R>(part_tokens), st>>>(p);
-  e = cudaGetLastError();
+  e = pkv::launch_pdl(paged_attention_partition_kernel<D, R>, grid, dim3(Cfg<D, R>::NW * 32),
+                      smem_bytes<D, R>(part_tokens), st, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
   if (p.max_parts > 1) {
-    paged_attention_merge_kernel<D><<<dim3(p.num_heads, num_seqs), D, 0, st>>>(p);
-    e = cudaGetLastError();
+    e = pkv::launch_pdl(paged_attention_merge_kernel<D>, dim3((p.num_heads + 3) / 4, num_seqs), dim3(128), 0, st,
+                        p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention merge launch: %s", cudaGetErrorString(e));
   }
   return PKV_OK;
@@ -526,7 +580,8 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_heads, int head_
   const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
   const long long parts = (max_ctx + kMinPartTokens - 1) / kMinPartTokens;
   if (parts <= 1) return 0;
-  return static_cast<size_t>(num_seqs) * num_heads * parts * (head_dim + 2) * sizeof(float);
+  const size_t pairs = static_cast<size_t>(num_seqs) * num_heads * parts;
+  return (ws_ml_floats(pairs) + pairs * head_dim) * sizeof(float);
 }
 
 int pkv_paged_attention_plan(int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq, int block_size,
@@ -668,8 +723,8 @@ int pkv_paged_attention_decode_static_workspace(const uint16_t* q, const uint16_
   if (rc != PKV_OK) return rc;
   const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
   const long long parts = (max_ctx + part_tokens - 1) / part_tokens;
-  const unsigned long long need =
-      parts > 1 ? static_cast<unsigned long long>(num_seqs) * num_heads * parts * (head_dim + 2) * sizeof(float) : 0;
+  const size_t pairs = static_cast<size_t>(num_seqs) * num_heads * parts;
+  const unsigned long long need = parts > 1 ? (ws_ml_floats(pairs) + pairs * head_dim) * sizeof(float) : 0;
   if (need > kStaticWorkspaceBytes)
     return pkv::fail(PKV_ERR_WORKSPACE,
                      "pkv_paged_attention_decode_static_workspace: this batch needs %llu bytes of scratch, above "

@@ -13,6 +13,7 @@
 
 #include <cstdint>
 
+#include "launch.cuh"
 #include "pkv_internal.h"
 
 namespace {
@@ -30,6 +31,8 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
                                                                 const int64_t* __restrict__ slot_mapping,
                                                                 int64_t total, int num_heads, int vec_per_row,
                                                                 int block_size, int64_t num_slots) {
+  pkv::pdl_trigger();
+  pkv::pdl_wait();  // key/value/slots may come from the previous kernel on the stream
   const int64_t per_token = static_cast<int64_t>(num_heads) * vec_per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -61,6 +64,8 @@ struct LayerPtrs {
 // grid (num_pairs, num_layers, splits): CTA (p, l, z) copies slice z of block pair p in layer l.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(const LayerPtrs ptrs, const int64_t* __restrict__ mapping,
                                                           int64_t vec_per_block, int num_blocks) {
+  pkv::pdl_trigger();
+  pkv::pdl_wait();
   const int pair = blockIdx.x;
   const int layer = blockIdx.y;
   const int64_t src = mapping[2 * pair];
@@ -144,11 +149,12 @@ int pkv_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* 
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = static_cast<int>(want < (1 << 20) ? want : (1 << 20));
-  reshape_and_cache_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+  cudaError_t e = pkv::launch_pdl(
+      reshape_and_cache_kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream),
       reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value), reinterpret_cast<uint4*>(k_cache),
       reinterpret_cast<uint4*>(v_cache), slot_mapping, total, num_heads, vec, block_size,
       static_cast<int64_t>(num_blocks) * block_size);
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_reshape_and_cache launch: %s", cudaGetErrorString(e));
   pkv::clear_error();
   return PKV_OK;
@@ -184,8 +190,9 @@ int pkv_copy_blocks(uint16_t* const* k_caches, uint16_t* const* v_caches, int nu
       ptrs.k[l] = reinterpret_cast<uint4*>(k_caches[l0 + l]);
       ptrs.v[l] = reinterpret_cast<uint4*>(v_caches[l0 + l]);
     }
-    copy_blocks_kernel<<<dim3(num_pairs, nl, splits), 256, 0, st>>>(ptrs, block_mapping, vec_per_block, num_blocks);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = pkv::launch_pdl(copy_blocks_kernel, dim3(num_pairs, nl, splits), dim3(256), 0, st, ptrs,
+                                    block_mapping, vec_per_block, num_blocks);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_copy_blocks launch: %s", cudaGetErrorString(e));
   }
   pkv::clear_error();

@@ -1,0 +1,35 @@
+// Kernel launch with programmatic dependent launch (PDL) enabled, shared by the .cu files.
+//
+// A kernel launched this way may be scheduled while the previous kernel on the
+// stream is still finishing; every kernel of this library therefore executes
+// griddepcontrol.wait before it reads any input (which waits for the previous
+// grid to complete and its writes to be visible) and griddepcontrol.launch_dependents
+// at its start, so the next kernel's launch overlaps this one's tail.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <utility>
+
+namespace pkv {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace pkv

@@ -4,7 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 
 namespace pkv {
 

@@ -24,7 +24,8 @@ def _worker(rank, world, port, out_dir):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     seed = bench.SEED + 7919 * rank
-    w, slots, pairs, _ = bench.build_step_inputs(seed)
+    x = bench.build_step_inputs(seed)
+    w, slots = x["w"], x["slots"]
     # per-rank step time and bytes: stand-ins with known max / sum
     (step_ms, e2e_ms, attn_ms), (kv_total,) = bench.reduce_over_ranks(
         [1.0 + rank, 3.0 - rank, 0.5], [float(w.logical_kv_bytes())], world, "cpu")
