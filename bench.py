@@ -56,7 +56,11 @@ EVENT_EVERY = 16
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call (partition + merge
 # kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
 # on); a changed kernel reports null until it is captured again.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # partition kernel 1,373,116,000 B read + 4,396,800 B written, merge kernel 1,259,000 B read
+    # (mean of two launches; profiles/paged_attention_opt13b_decode.md)
+    ("opt13b", "32959b3faba081b7e5918c7d365fa69eada500069d1eb08c38d8c9f13fbed3ce"): 1_378_772_000,
+}
 
 
 def parse():
