@@ -15,7 +15,7 @@ the same C-ABI calls.  `roofline` is the paged attention call alone against
 the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity]
+                  [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity|beam_search]
                   [--capacity-seqs S] [--capacity-block B] [--pool-frac F]
 
 The default workload is the headline one above.  The others build their batch
@@ -161,7 +161,7 @@ class ClockSampler:
 
 # ---- workloads -------------------------------------------------------------------------------------
 
-WORKLOADS = ("opt13b", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity")
+WORKLOADS = ("opt13b", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity", "beam_search")
 
 
 def attention_algorithmic_bytes(w) -> int:
@@ -202,6 +202,8 @@ def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 
     from paged_kv_cache_73_gb300 import binding as pkv
     from paged_kv_cache_73_gb300 import workloads as wl
 
+    if workload == "beam_search":
+        return build_beam_step(seed)
     if workload == "opt13b":
         recipe = wl.opt13b(seed=seed)
     elif workload in ("parallel_sampling", "parallel_sampling_cow"):
@@ -249,6 +251,57 @@ def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 
         desc = f"{workload}: {recipe.notes}, 40 x 128, block {B}, shuffled blocks"
     return {"w": w, "slots": slots, "pairs": pairs, "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2),
             "host_us": host_us, "desc": desc, "workload": workload}
+
+
+def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: int = 128, B: int = 16):
+    """Beam search through the block manager: each request keeps `width` candidates; every step
+    each new candidate picks a parent among the current ones (seeded), the old beam is retired and
+    shared partly filled blocks are copied once per extra sibling.  The measured step is one more
+    beam step: its copies, its new tokens' writes and attention over all candidates."""
+    from paged_kv_cache_73_gb300 import binding as pkv
+    from paged_kv_cache_73_gb300 import workloads as wl
+
+    H, D = 40, 128
+    rng = np.random.default_rng(seed)
+    prompts = rng.integers(256, 1025, size=requests)
+    N = int(2 * (sum(-(-int(p) // B) for p in prompts) + requests * width * (beam_steps // B + 3)))
+    bm = pkv.BlockManager(N, B, wl.free_list_order(N, seed))
+    beams, nid = [], 0
+    for r in range(requests):
+        bm.add_seq(nid, int(prompts[r]))
+        beams.append([nid])
+        nid += 1
+    setup = []
+
+    def one_step():
+        nonlocal nid
+        slots, pairs = [], []
+        for r in range(requests):
+            parents = [int(x) for x in rng.choice(beams[r], size=width)]
+            children = list(range(nid, nid + width))
+            nid += width
+            sl, pr = bm.beam_step(parents, children, beams[r])
+            beams[r] = children
+            slots += [int(x) for x in sl]
+            pairs += [tuple(int(y) for y in p) for p in pr]
+        return slots, pairs
+
+    for _ in range(beam_steps):
+        setup += one_step()[1]
+    t0 = time.perf_counter()
+    slots, pairs = one_step()
+    host_us = (time.perf_counter() - t0) * 1e6
+    seqs = [c for beam in beams for c in beam]
+    lens = np.array([bm.block_table(c)[1] for c in seqs], dtype=np.int32)
+    max_blocks = -(-int(lens.max()) // B)
+    tables, ctx = bm.block_tables(seqs, max_blocks)
+    w = wl.from_tables("beam_search_decode_step", seed, H, D, B, N, tables, ctx,
+                       f"{requests} requests x beam width {width}, prompts U[256,1024], {beam_steps} beam steps")
+    desc = f"beam_search: {w.notes}, 40 x 128, block {B}, shuffled blocks"
+    return {"w": w, "slots": np.array(slots, dtype=np.int64),
+            "pairs": np.array(pairs, dtype=np.int64).reshape(-1, 2),
+            "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2), "host_us": host_us, "desc": desc,
+            "workload": "beam_search"}
 
 
 def run_gpu(args, rank, world, dev):

@@ -253,6 +253,18 @@ int pkv_bm_block_table(const pkv_bm* bm, int64_t seq_id, int32_t* out, int cap, 
 int pkv_bm_block_tables(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_t* tables_out,
                         int max_blocks, int32_t* ctx_lens_out);
 
+/* One beam-search step ([lecture] Beam Search 场景; [guide] 04): child i
+ * forks parent i (shares all its blocks); then every retired sequence (the
+ * previous beam) is freed, returning the blocks no candidate still holds;
+ * then each child appends one token, copying a shared partly filled last
+ * block (reported in cow_pairs_out, host [k, 2] int64; *num_cow copies).
+ * parents/children: host [k]; children are new distinct ids; retire: host
+ * [n_retire] existing distinct ids (parents may be among them).
+ * slots_out: host [k].  All-or-nothing. */
+int pkv_bm_beam_step(pkv_bm* bm, const int64_t* parents, const int64_t* children, int k,
+                     const int64_t* retire, int n_retire, int64_t* slots_out, int64_t* cow_pairs_out,
+                     int* num_cow);
+
 /* Reference count of a physical block (negative status on a bad id). */
 int pkv_bm_ref_count(const pkv_bm* bm, int32_t block);
 

@@ -191,3 +191,36 @@ class BlockManager:
     def tail_waste_tokens(self) -> int:
         """Sum over sequences of the unfilled slots of their blocks."""
         return sum(self.B * len(bl) - sum(b.filled for b in bl) for bl in self.seqs.values())
+
+    # -- beam search ---------------------------------------------------------
+    def beam_step(self, parents, children, retire):
+        """One beam-search step ([lecture] Beam Search 场景; [guide] 04, beam search).
+
+        Each new candidate children[i] shares every block of parents[i] (a fork);
+        then the retired candidates (the previous beam, dropped or not) are freed,
+        so blocks no candidate still holds return to the free list -- back up the
+        tree to, but not including, blocks the survivors share; then every new
+        candidate appends its token, copying a shared partly filled last block
+        (the one-block copy of beam search).  All or nothing: on MemoryError
+        nothing has changed.
+        Returns [(slot, copy_src, copy_dst)] in the order of ``children``.
+        """
+        import copy
+        if len(parents) != len(children):
+            raise ValueError("parents and children differ in length")
+        if len(set(children)) != len(children) or any(c in self.seqs for c in children):
+            raise ValueError("children must be new, distinct ids")
+        if any(p not in self.seqs for p in parents) or any(r not in self.seqs for r in retire):
+            raise KeyError("unknown parent or retired sequence")
+        if len(set(retire)) != len(retire):
+            raise ValueError("a sequence is retired twice")
+        trial = copy.deepcopy(self)
+        trial._beam_step_unchecked(parents, children, retire)       # raises MemoryError if short
+        return self._beam_step_unchecked(parents, children, retire)
+
+    def _beam_step_unchecked(self, parents, children, retire):
+        for p, c in zip(parents, children):
+            self.fork(p, c)
+        for r in retire:
+            self.free(r)
+        return [self.append_slot(c) for c in children]

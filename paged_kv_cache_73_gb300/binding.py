@@ -70,6 +70,7 @@ _SIGNATURES = {
     "pkv_bm_drop_prefix": (_I, [_P, _I64]),
     "pkv_bm_block_table": (_I, [_P, _I64, _P, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_bm_block_tables": (_I, [_P, _P, _I, _P, _I, _P]),
+    "pkv_bm_beam_step": (_I, [_P, _P, _P, _I, _P, _I, _P, _P, _c.POINTER(_I)]),
     "pkv_bm_ref_count": (_I, [_P, _c.c_int32]),
     "pkv_bm_stats": (_I, [_P, _c.POINTER(_I), _c.POINTER(_I64), _c.POINTER(_I64)]),
 }
@@ -344,6 +345,22 @@ class BlockManager:
         lens = np.empty(n, dtype=np.int32)
         _check(self._lib.pkv_bm_block_tables(self._h, _np_ptr(ids), n, _np_ptr(tables), max_blocks, _np_ptr(lens)))
         return tables, lens
+
+    def beam_step(self, parents: Sequence[int], children: Sequence[int],
+                  retire: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
+        """Fork children from parents, free the retired beam, append one token per child."""
+        par = np.ascontiguousarray(np.asarray(parents, dtype=np.int64))
+        chi = np.ascontiguousarray(np.asarray(children, dtype=np.int64))
+        ret = np.ascontiguousarray(np.asarray(retire, dtype=np.int64))
+        k = chi.shape[0]
+        if par.shape[0] != k:
+            raise PkvError(PKV_ERR_INVALID_ARG, "parents and children differ in length")
+        slots = np.empty(max(k, 1), dtype=np.int64)
+        pairs = np.empty((max(k, 1), 2), dtype=np.int64)
+        nc = _c.c_int(0)
+        _check(self._lib.pkv_bm_beam_step(self._h, _np_ptr(par), _np_ptr(chi), k, _np_ptr(ret), ret.shape[0],
+                                          _np_ptr(slots), _np_ptr(pairs), ctypes.byref(nc)))
+        return slots[:k], pairs[:nc.value]
 
     def ref_count(self, block: int) -> int:
         r = self._lib.pkv_bm_ref_count(self._h, block)

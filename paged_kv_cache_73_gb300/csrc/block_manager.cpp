@@ -302,6 +302,78 @@ int pkv_bm_block_tables(const pkv_bm* bm, const int64_t* seq_ids, int n, int32_t
   return PKV_OK;
 }
 
+int pkv_bm_beam_step(pkv_bm* bm, const int64_t* parents, const int64_t* children, int k, const int64_t* retire,
+                     int n_retire, int64_t* slots_out, int64_t* cow_pairs_out, int* num_cow) {
+  if (!bm || k < 0 || n_retire < 0 || (k > 0 && (!parents || !children || !slots_out || !cow_pairs_out)) ||
+      (n_retire > 0 && !retire) || !num_cow)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_beam_step: bad argument");
+  Manager* m = M(bm);
+  std::unordered_map<int64_t, int> seen;
+  for (int i = 0; i < k; ++i) {
+    if (!m->seqs.count(parents[i]))
+      return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_beam_step: no parent sequence %lld", (long long)parents[i]);
+    if (m->seqs.count(children[i]) || seen.count(children[i]))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_beam_step: child %lld exists or is listed twice",
+                       (long long)children[i]);
+    seen[children[i]] = 1;
+  }
+  std::unordered_map<int64_t, int> retired;
+  for (int i = 0; i < n_retire; ++i) {
+    if (!m->seqs.count(retire[i]))
+      return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_beam_step: no retired sequence %lld", (long long)retire[i]);
+    if (retired.count(retire[i]))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_beam_step: sequence %lld retired twice", (long long)retire[i]);
+    retired[retire[i]] = 1;
+  }
+  // Reference counts after the forks and frees, and the blocks those frees return.
+  std::unordered_map<int32_t, int> delta;
+  for (int i = 0; i < k; ++i)
+    for (const Logical& lb : m->seqs[parents[i]]) delta[lb.phys] += 1;
+  for (int i = 0; i < n_retire; ++i)
+    for (const Logical& lb : m->seqs[retire[i]]) delta[lb.phys] -= 1;
+  int returned = 0;
+  for (const auto& kv : delta)
+    if (m->ref[kv.first] > 0 && m->ref[kv.first] + kv.second == 0) ++returned;
+  // Blocks the appends will take: one per child whose last block is full or still shared.
+  std::unordered_map<int32_t, int> dec;
+  int need = 0;
+  for (int i = 0; i < k; ++i) {
+    const Logical& last = m->seqs[parents[i]].back();
+    if (last.filled == m->B) {
+      ++need;
+    } else {
+      const int r = m->ref[last.phys] + delta[last.phys] - dec[last.phys];
+      if (r > 1) {
+        ++need;
+        dec[last.phys] += 1;
+      }
+    }
+  }
+  if (need > (int)m->free_list.size() + returned) return oom(m, need - returned);
+  for (int i = 0; i < k; ++i) {
+    std::vector<Logical> copy = m->seqs[parents[i]];
+    for (const Logical& lb : copy) m->ref[lb.phys] += 1;
+    m->seqs.emplace(children[i], std::move(copy));
+  }
+  for (int i = 0; i < n_retire; ++i) {
+    auto it = m->seqs.find(retire[i]);
+    for (const Logical& lb : it->second) m->release(lb.phys);
+    m->seqs.erase(it);
+  }
+  int c = 0;
+  for (int i = 0; i < k; ++i) {
+    int32_t src, dst;
+    slots_out[i] = m->append(m->seqs[children[i]], &src, &dst);
+    if (src >= 0) {
+      cow_pairs_out[2 * c] = src;
+      cow_pairs_out[2 * c + 1] = dst;
+      ++c;
+    }
+  }
+  *num_cow = c;
+  return PKV_OK;
+}
+
 int pkv_bm_ref_count(const pkv_bm* bm, int32_t block) {
   if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_ref_count: null manager");
   const Manager* m = M(bm);

@@ -188,3 +188,79 @@ def test_batch_tables_padded():
     assert tables.tolist() == [[3, -1, -1, -1], [0, 1, 2, -1]] and lens.tolist() == [1, 9]
     with pytest.raises(pkv.PkvError):
         bm.block_tables([5], 2)
+
+
+# ---- beam search --------------------------------------------------------------------------------
+
+def _beam_tree(bm):
+    c0, c1, c2, c3 = 10, 11, 12, 13
+    bm.add_seq(c0, 1)
+    bm.fork(c0, c3)
+    for c in (c0, c3, c0, c3):
+        bm.append_slot(c)
+    bm.fork(c0, c1)
+    bm.fork(c0, c2)
+    for c in (c0, c1, c2, c3):
+        bm.append_slot(c)
+    return {"cand0": c0, "cand1": c1, "cand2": c2, "cand3": c3}
+
+
+def test_pages_beam_search_example():
+    g = json.load(open(GOLDEN))["beam_search"]
+    bm = pkv.BlockManager(32, g["block_size"])
+    ids = _beam_tree(bm)
+    for name, lineage in g["lineages_before"].items():
+        assert bm.block_table(ids[name])[0] == lineage
+    new = [20, 21, 22, 23]
+    slots, pairs = bm.beam_step([ids[p] for p in g["step"]["parents"]], new, [ids[r] for r in g["step"]["retire"]])
+    assert len(pairs) == 0
+    for i, lineage in enumerate(g["lineages_after"].values()):
+        assert bm.block_table(new[i])[0] == lineage
+    assert list(slots) == [9, 10, 11, 12]
+    for b, r in g["ref_after"].items():
+        assert bm.ref_count(int(b)) == r
+    assert bm.stats()[0] == 32 - 9
+
+
+@pytest.mark.parametrize("B,width,seed", [(16, 4, 0), (16, 6, 1), (4, 4, 2), (1, 3, 3)])
+def test_random_beam_search_matches_oracle(B, width, seed):
+    rng = np.random.default_rng(seed)
+    N = 400
+    order = rng.permutation(N)
+    nat = pkv.BlockManager(N, B, order)
+    ora = obm.BlockManager(N, B, order)
+    nat.add_seq(0, 37)
+    ora.add_seq(0, 37)
+    beam = [0]
+    nid = 1
+    for step in range(60):
+        parents = [int(rng.choice(beam)) for _ in range(width)]
+        children = list(range(nid, nid + width))
+        nid += width
+        try:
+            want = ora.beam_step(parents, children, beam)
+        except MemoryError:
+            with pytest.raises(pkv.PkvOutOfBlocks):
+                nat.beam_step(parents, children, beam)
+            break
+        slots, pairs = nat.beam_step(parents, children, beam)
+        assert list(slots) == [w[0] for w in want]
+        assert pairs.tolist() == [[w[1], w[2]] for w in want if w[1] >= 0]
+        beam = children
+        _compare(nat, ora, beam, N)
+
+
+def test_beam_step_errors_leave_state_unchanged():
+    bm = pkv.BlockManager(4, 4)
+    bm.add_seq(0, 6)
+    with pytest.raises(pkv.PkvOutOfBlocks):
+        bm.beam_step([0, 0, 0, 0], [1, 2, 3, 4], [0])
+    with pytest.raises(pkv.PkvError):
+        bm.beam_step([0], [0], [])                # child exists
+    with pytest.raises(pkv.PkvError):
+        bm.beam_step([9], [1], [])                # unknown parent
+    with pytest.raises(pkv.PkvError):
+        bm.beam_step([0], [1], [0, 0])            # retired twice
+    assert bm.block_table(0) == ([0, 1], 6) and bm.stats()[0] == 2
+    slots, pairs = bm.beam_step([0, 0, 0], [1, 2, 3], [0])
+    assert len(pairs) == 2 and bm.stats()[0] == 0

@@ -173,3 +173,24 @@ def test_capacity_pool_filling_most_of_hbm(cuda_device):
     finally:
         del inputs
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shards", [2, 4])
+def test_head_sharded_pools_match_unsharded(cuda_device, shards):
+    # tensor parallelism as the pages describe it: every shard keeps the same block table and
+    # holds only its heads of every block; concatenating the shards' outputs gives the
+    # unsharded result (bit for bit while the launch plan is the same)
+    w = wl.opt13b(seed=9, num_seqs=64)
+    q, k, v, tables, lens = device_inputs(w, cuda_device)
+    full = gpu_attention(w, cuda_device, (q, k, v, tables, lens))
+    H = w.num_heads
+    step = H // shards
+    plan = pkv.paged_attention_plan(64, H, 128, w.max_blocks_per_seq, 16)
+    parts = []
+    for r in range(shards):
+        hs = slice(r * step, (r + 1) * step)
+        qs, ks, vs = q[:, hs].contiguous(), k[:, hs].contiguous(), v[:, hs].contiguous()
+        parts.append(pkv.paged_attention_decode(qs, ks, vs, tables, lens, w.scale, 16))
+        assert pkv.paged_attention_plan(64, step, 128, w.max_blocks_per_seq, 16) == plan
+    assert pkv.device_error() == 0
+    assert torch.equal(torch.cat(parts, dim=1), full)

@@ -127,3 +127,33 @@ def test_shared_prefix_decode(cuda_device):
     assert x.ora.cow_copies == len(seqs)                    # every request copies the partial prefix block
     assert x.pools_equal()
     assert x.attend(seqs) <= ATOL
+
+
+@pytest.mark.parametrize("width,B", [(4, 16), (6, 8)])
+def test_beam_search_decode(cuda_device, width, B):
+    # a beam step forks the survivors, retires the old beam and appends one token per candidate;
+    # the one-block copies run through copy_blocks before the writes
+    H, D, requests = 4, 128, 3
+    rng = np.random.default_rng(width)
+    x = TwoSides(cuda_device, 600, H, D, B, seed=2000 + width)
+    beams, nid = [], 0
+    for r in range(requests):
+        n = int(rng.integers(20, 90))
+        x.write(x.nat.add_seq(nid, n), x.ora.add_seq(nid, n))
+        beams.append([nid])
+        nid += 1
+    copies = 0
+    for step in range(40):
+        for r in range(requests):
+            parents = [int(p) for p in rng.choice(beams[r], size=width)]
+            children = list(range(nid, nid + width))
+            nid += width
+            slots, pairs = x.nat.beam_step(parents, children, beams[r])
+            want = x.ora.beam_step(parents, children, beams[r])
+            x.copy(pairs, [(s, d) for _, s, d in want if s >= 0])
+            x.write(slots, [w[0] for w in want])
+            copies += len(pairs)
+            beams[r] = children
+    assert copies > 0
+    assert x.pools_equal()
+    assert x.attend([c for b in beams for c in b]) <= ATOL

@@ -286,3 +286,60 @@ def test_free_returns_blocks_only_when_unreferenced():
     bm.free(1)
     assert bm.num_free() == 32
     assert list(bm.free_list)[-3:] == [0, 1, 2]              # FIFO: freed blocks go to the back
+
+
+# ---- beam search ----------------------------------------------------------------------------
+
+def _beam_tree(bm):
+    """The figure's tree: with B = 1, ids are taken in the order 0..8 of the figure."""
+    c0, c1, c2, c3 = 10, 11, 12, 13
+    bm.add_seq(c0, 1)               # block 0
+    bm.fork(c0, c3)
+    bm.append_slot(c0)              # block 1
+    bm.append_slot(c3)              # block 2
+    bm.append_slot(c0)              # block 3
+    bm.append_slot(c3)              # block 4
+    bm.fork(c0, c1)
+    bm.fork(c0, c2)
+    for c in (c0, c1, c2, c3):      # blocks 5, 6, 7, 8
+        bm.append_slot(c)
+    return {"cand0": c0, "cand1": c1, "cand2": c2, "cand3": c3}
+
+
+def test_beam_search_walkthrough():
+    g = _golden()["beam_search"]
+    bm = obm.BlockManager(32, g["block_size"])
+    ids = _beam_tree(bm)
+    for name, lineage in g["lineages_before"].items():
+        assert bm.block_table(ids[name])[0] == lineage
+    new = [20, 21, 22, 23]
+    out = bm.beam_step([ids[p] for p in g["step"]["parents"]], new, [ids[r] for r in g["step"]["retire"]])
+    assert all(src == -1 for _, src, _ in out)                       # B = 1: every token opens a block
+    for i, (name, lineage) in enumerate(g["lineages_after"].items()):
+        assert bm.block_table(new[i])[0] == lineage
+    assert list(bm.free_list)[-4:] == g["freed_in_order"]
+    for b, r in g["ref_after"].items():
+        assert bm.ref_count(int(b)) == r
+
+
+def test_beam_step_copies_one_block_per_extra_sibling():
+    B = 16
+    bm = obm.BlockManager(64, B)
+    bm.add_seq(0, 40)                                                 # last block holds 8 tokens
+    bm.fork(0, 1)
+    out = bm.beam_step([0, 0, 0, 1], [2, 3, 4, 5], [0, 1])
+    copies = [(s, d) for _, s, d in out if s >= 0]
+    # four candidates now share the partial block: three copy it, the last writes in place
+    assert len(copies) == 3 and all(s == bm.block_table(5)[0][-1] for s, _ in copies)
+    assert bm.ref_count(bm.block_table(5)[0][0]) == 4
+
+
+def test_beam_step_all_or_nothing():
+    bm = obm.BlockManager(4, 4)
+    bm.add_seq(0, 6)                                                  # 2 blocks, last has 2 tokens
+    before = (list(bm.free_list), dict(bm.seqs))
+    with pytest.raises(MemoryError):
+        bm.beam_step([0, 0, 0, 0], [1, 2, 3, 4], [0])                 # needs 3 copies, 2 free
+    assert list(bm.free_list) == before[0] and set(bm.seqs) == {0}
+    out = bm.beam_step([0, 0, 0], [1, 2, 3], [0])                    # needs 2 copies: fits
+    assert sum(1 for _, s, _ in out if s >= 0) == 2 and bm.num_free() == 0
