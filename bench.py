@@ -15,8 +15,13 @@ the same C-ABI calls.  `roofline` is the paged attention call alone against
 the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity|beam_search]
+                  [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity|beam_search
+                              |swap|layers40]
                   [--capacity-seqs S] [--capacity-block B] [--pool-frac F]
+
+`--workload swap` and `--workload layers40` print their own lines (swap_blocks
+between HBM and page-locked host memory; 40-layer copy_blocks and
+reshape_and_cache in one launch) with their own metric names.
 
 The default workload is the headline one above.  The others build their batch
 through the same block manager (prompt forks with copy-on-write, a shared
@@ -71,7 +76,7 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop (profiling runs)")
-    ap.add_argument("--workload", choices=WORKLOADS, default="opt13b",
+    ap.add_argument("--workload", choices=WORKLOADS + AUX_WORKLOADS, default="opt13b",
                     help="opt13b (the headline batch) or another decode batch of the same shape family")
     ap.add_argument("--capacity-seqs", type=int, default=64, help="capacity workload: sequences (ctx 2048 each)")
     ap.add_argument("--capacity-block", type=int, default=16, help="capacity workload: block size")
@@ -392,6 +397,105 @@ def run_gpu(args, rank, world, dev):
     return res
 
 
+AUX_WORKLOADS = ("swap", "layers40")
+
+
+def _timed(fn, reps=10, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def run_swap(args, dev):
+    """swap_blocks: the blocks of 16 sequences x 2048 tokens (one layer, 40 x 128, block 16)
+    out to page-locked host memory and back, one launch each way, against one
+    cudaMemcpyAsync per block (the pattern the fused kernel replaces)."""
+    import torch
+    from paged_kv_cache_73_gb300 import binding as pkv
+    from paged_kv_cache_73_gb300 import workloads as wl
+    H, D, B, n = 40, 128, 16, 16 * 128
+    N = n + 512
+    dk = wl.dense_tensor((N, H, B, D), SEED, wl.STREAM_K, dev)
+    dv = wl.dense_tensor((N, H, B, D), SEED, wl.STREAM_V, dev)
+    hk = torch.empty((n, H, B, D), dtype=torch.float16, pin_memory=True)
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(SEED)
+    src = rng.permutation(N)[:n]
+    out_map = torch.from_numpy(np.stack([src, np.arange(n)], 1).astype(np.int64)).to(dev)
+    back = rng.permutation(np.setdiff1d(np.arange(N), src))
+    spare = np.concatenate([back, src])[:n]
+    in_map = torch.from_numpy(np.stack([np.arange(n), spare], 1).astype(np.int64)).to(dev)
+    payload = 2 * n * H * B * D * 2                          # K and V bytes moved each way
+    t_out = _timed(lambda: pkv.swap_blocks([dk], [dv], [hk], [hv], out_map))
+    t_in = _timed(lambda: pkv.swap_blocks([hk], [hv], [dk], [dv], in_map))
+    assert pkv.device_error() == 0
+    ok = torch.equal(dk[torch.from_numpy(spare).to(dev)].cpu(), hk)
+    src_l, spare_l = src.tolist(), spare.tolist()
+
+    def per_block_out():
+        for i, s_ in enumerate(src_l):
+            hk[i].copy_(dk[s_], non_blocking=True)
+            hv[i].copy_(dv[s_], non_blocking=True)
+
+    def per_block_in():
+        for i, d_ in enumerate(spare_l):
+            dk[d_].copy_(hk[i], non_blocking=True)
+            dv[d_].copy_(hv[i], non_blocking=True)
+
+    m_out = _timed(per_block_out, reps=3, warm=1)
+    m_in = _timed(per_block_in, reps=3, warm=1)
+    gbs = lambda ms: payload / (ms * 1e-3) / 1e9
+    value = 2 * payload / ((t_out + t_in) * 1e-3) / 1e9
+    return {"metric": "swap_blocks GB/s (HBM <-> page-locked Grace memory, both directions)", "value": value,
+            "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f16 (bit copy)",
+            "data": "synthetic (seeded counter-based generator)", "round_trip_bit_exact": bool(ok),
+            "config": {"workload": "swap: 2048 blocks (16 seqs x 2048 tokens), 40 x 128, block 16, one layer",
+                       "bytes_each_way": payload},
+            "swap_out": {"ms": t_out, "GB/s": gbs(t_out), "launches": 1},
+            "swap_in": {"ms": t_in, "GB/s": gbs(t_in), "launches": 1},
+            "per_block_memcpy": {"out_ms": m_out, "in_ms": m_in, "out_GB/s": gbs(m_out), "in_GB/s": gbs(m_in),
+                                 "copies_each_way": 2 * n}}
+
+
+def run_layers40(args, dev):
+    """The OPT-13B layer count: reshape_and_cache of 64 tokens and 96 copy-on-write copies over 40
+    layers, each as one launch, against one launch per layer."""
+    import torch
+    from paged_kv_cache_73_gb300 import binding as pkv
+    H, D, B, N, L, T = 40, 128, 16, 1024, 40, 64
+    ks = [torch.zeros((N, H, B, D), dtype=torch.float16, device=dev) for _ in range(L)]
+    vs = [torch.zeros((N, H, B, D), dtype=torch.float16, device=dev) for _ in range(L)]
+    keys = [torch.ones((T, H, D), dtype=torch.float16, device=dev) for _ in range(L)]
+    vals = [torch.ones((T, H, D), dtype=torch.float16, device=dev) for _ in range(L)]
+    rng = np.random.default_rng(SEED)
+    slots = torch.from_numpy(rng.choice(N * B, size=T, replace=False).astype(np.int64)).to(dev)
+    perm = rng.permutation(N)
+    pairs = torch.from_numpy(np.stack([perm[:96], perm[96:192]], 1).astype(np.int64)).to(dev)
+    t_r1 = _timed(lambda: pkv.reshape_and_cache_layers(keys, vals, ks, vs, slots), reps=50)
+    t_rL = _timed(lambda: [pkv.reshape_and_cache(keys[l], vals[l], ks[l], vs[l], slots) for l in range(L)], reps=50)
+    t_c1 = _timed(lambda: pkv.copy_blocks(ks, vs, pairs), reps=20)
+    t_cL = _timed(lambda: [pkv.copy_blocks([ks[l]], [vs[l]], pairs) for l in range(L)], reps=20)
+    assert pkv.device_error() == 0
+    r_bytes = 2 * 2 * L * T * H * D * 2                      # K and V, read and written
+    c_bytes = 2 * 2 * L * 96 * H * B * D * 2
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    return {"metric": "multi-layer cache ops GB/s (40 layers, one launch)", "value": gbs(c_bytes, t_c1),
+            "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f16 (bit copy)", "data": "synthetic",
+            "config": {"workload": "layers40: 40 layers x [1024 blocks, 40, 16, 128]; 64 new tokens; 96 copy pairs"},
+            "copy_blocks": {"one_launch_ms": t_c1, "one_launch_GB/s": gbs(c_bytes, t_c1),
+                            "per_layer_launches_ms": t_cL, "per_layer_GB/s": gbs(c_bytes, t_cL)},
+            "reshape_and_cache": {"one_launch_ms": t_r1, "one_launch_GB/s": gbs(r_bytes, t_r1),
+                                  "per_layer_launches_ms": t_rL, "per_layer_GB/s": gbs(r_bytes, t_rL)}}
+
+
 def pool_blocks_for(args, dev):
     """Pool size for the capacity workload: a fraction of free HBM, or just enough."""
     if args.workload != "capacity" or args.pool_frac <= 0:
@@ -580,6 +684,14 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+
+    if args.workload in AUX_WORKLOADS:
+        from paged_kv_cache_73_gb300 import binding as pkv
+        pkv.load()
+        line = (run_swap if args.workload == "swap" else run_layers40)(args, dev)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -171,6 +171,14 @@ int pkv_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* 
                           uint16_t* v_cache, const int64_t* slot_mapping, int num_tokens,
                           int num_heads, int head_dim, int block_size, int num_blocks, void* stream);
 
+/* reshape_and_cache over num_layers layers in one launch (all layers' new
+ * tokens share one slot mapping).  keys, values, k_caches, v_caches: HOST
+ * arrays of num_layers device pointers, each laid out as above. */
+int pkv_reshape_and_cache_layers(const uint16_t* const* keys, const uint16_t* const* values,
+                                 uint16_t* const* k_caches, uint16_t* const* v_caches, int num_layers,
+                                 const int64_t* slot_mapping, int num_tokens, int num_heads, int head_dim,
+                                 int block_size, int num_blocks, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Batched block copy ([note] 关键设计 3 copy-on-write; 关键设计 5, "fused block
  * copy": many small block copies in one kernel instead of one memcpy each).
@@ -188,6 +196,31 @@ int pkv_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* 
 int pkv_copy_blocks(uint16_t* const* k_caches, uint16_t* const* v_caches, int num_layers,
                     const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
                     int block_size, int num_blocks, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Block swap between two pools ([lecture] 调度和抢占, Swapping: the blocks of a
+ * preempted sequence move to CPU memory and back; [guide] 05).
+ *
+ * For every pair p < num_pairs and every layer l < num_layers:
+ *   dst_k_caches[l][dst_p] = src_k_caches[l][src_p]   (V likewise)
+ * with (src_p, dst_p) = (block_mapping[2p], block_mapping[2p+1]); whole blocks.
+ * Bit-exact.  One launch moves every pair of every layer (no per-block memcpy).
+ *
+ *   src_*, dst_*  HOST arrays of num_layers pool pointers.  Each pool is
+ *                 [num_blocks, num_heads, block_size, head_dim] fp16, 16-byte
+ *                 aligned, in device memory OR in page-locked host memory
+ *                 (cudaHostAlloc / cudaHostRegister), which the kernel reads or
+ *                 writes directly over the host link.  Swap-out: device source,
+ *                 host destination; swap-in: the reverse.  Pageable host memory
+ *                 is refused (PKV_ERR_INVALID_ARG).
+ *   block_mapping [num_pairs, 2] int64 in device or page-locked host memory;
+ *                 src ids in [0, src_num_blocks), dst ids in [0, dst_num_blocks).
+ *                 Destinations must be distinct and must not overlap sources.
+ * ------------------------------------------------------------------------- */
+int pkv_swap_blocks(const uint16_t* const* src_k_caches, const uint16_t* const* src_v_caches,
+                    uint16_t* const* dst_k_caches, uint16_t* const* dst_v_caches, int num_layers,
+                    const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,
+                    int block_size, int src_num_blocks, int dst_num_blocks, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Host block manager ([note] 关键设计 2 and 3; [lecture] PagedAttention 原理 and

@@ -51,3 +51,14 @@ def copy_blocks(k_caches: Sequence[np.ndarray], v_caches: Sequence[np.ndarray],
         for k_cache, v_cache in zip(k_caches, v_caches):
             k_cache[int(dst)] = k_cache[int(src)]
             v_cache[int(dst)] = v_cache[int(src)]
+
+
+def swap_blocks(src_k: Sequence[np.ndarray], src_v: Sequence[np.ndarray], dst_k: Sequence[np.ndarray],
+                dst_v: Sequence[np.ndarray], block_mapping: Sequence[Sequence[int]]) -> None:
+    """Swapping ([lecture] 调度和抢占, Swapping; [guide] 05): for every (src, dst) pair and layer,
+    block dst of the destination pools becomes a copy of block src of the source pools (the two
+    sides are different pools, e.g. GPU memory and CPU memory)."""
+    for src, dst in block_mapping:
+        for sk, sv, dk, dv in zip(src_k, src_v, dst_k, dst_v):
+            dk[int(dst)] = sk[int(src)]
+            dv[int(dst)] = sv[int(src)]

@@ -57,7 +57,9 @@ _SIGNATURES = {
     "pkv_paged_attention_decode_static_workspace": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I,
                                                          _P, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "pkv_reshape_and_cache_layers": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "pkv_swap_blocks": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_bm_create": (_P, [_I, _I, _P]),
     "pkv_bm_destroy": (None, [_P]),
     "pkv_bm_add_seq": (_I, [_P, _I64, _I, _P]),
@@ -239,6 +241,31 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
                                         slot_mapping.data_ptr(), T, H, D, B, N, _stream(stream)))
 
 
+def reshape_and_cache_layers(keys: Sequence[torch.Tensor], values: Sequence[torch.Tensor],
+                             k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor],
+                             slot_mapping: torch.Tensor, stream=None) -> None:
+    """reshape_and_cache for every layer in one launch (one slot mapping for all layers)."""
+    L = len(keys)
+    if not (len(values) == len(k_caches) == len(v_caches) == L) or L == 0:
+        raise PkvError(PKV_ERR_INVALID_ARG, "reshape_and_cache_layers: need as many keys, values and pools")
+    for t in list(keys) + list(values):
+        _need(t, "key/value", torch.float16, 3)
+        if t.shape != keys[0].shape:
+            raise PkvError(PKV_ERR_INVALID_ARG, "reshape_and_cache_layers: keys/values differ in shape")
+    for t in list(k_caches) + list(v_caches):
+        _need(t, "cache", torch.float16, 4)
+        if t.shape != k_caches[0].shape:
+            raise PkvError(PKV_ERR_INVALID_ARG, "reshape_and_cache_layers: pools differ in shape")
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    T, H, D = keys[0].shape
+    N, H2, B, D2 = k_caches[0].shape
+    if (H2, D2) != (H, D) or slot_mapping.shape[0] != T:
+        raise PkvError(PKV_ERR_INVALID_ARG, "reshape_and_cache_layers: inconsistent shapes")
+    arr = lambda ts: ctypes.cast((ctypes.c_void_p * L)(*[t.data_ptr() for t in ts]), ctypes.c_void_p)
+    _check(load().pkv_reshape_and_cache_layers(arr(keys), arr(values), arr(k_caches), arr(v_caches), L,
+                                               slot_mapping.data_ptr(), T, H, D, B, N, _stream(stream)))
+
+
 def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], block_mapping: torch.Tensor,
                 stream=None) -> None:
     """For each (src, dst) row of block_mapping and each layer: block dst := block src (K and V)."""
@@ -257,6 +284,35 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
     vp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
     _check(load().pkv_copy_blocks(ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p), L,
                                   block_mapping.data_ptr(), block_mapping.shape[0], H, D, B, N, _stream(stream)))
+
+
+def swap_blocks(src_k: Sequence[torch.Tensor], src_v: Sequence[torch.Tensor], dst_k: Sequence[torch.Tensor],
+                dst_v: Sequence[torch.Tensor], block_mapping: torch.Tensor, stream=None) -> None:
+    """Whole blocks src -> dst between two pools per layer; a pool may be a CUDA tensor or a
+    pinned CPU tensor (swap-out: GPU -> pinned host, swap-in: the reverse)."""
+    L = len(src_k)
+    if not (len(src_v) == len(dst_k) == len(dst_v) == L) or L == 0:
+        raise PkvError(PKV_ERR_INVALID_ARG, "swap_blocks: need the same number (>= 1) of pools on each side")
+    for t in list(src_k) + list(src_v) + list(dst_k) + list(dst_v):
+        _need(t, "pool", torch.float16, 4, cuda=False)
+        if not (t.is_cuda or t.is_pinned()):
+            raise PkvError(PKV_ERR_INVALID_ARG, "swap_blocks: a CPU pool must be pinned")
+    for side in (src_k, src_v):
+        if any(t.shape != side[0].shape for t in side):
+            raise PkvError(PKV_ERR_INVALID_ARG, "swap_blocks: source pools differ in shape")
+    for side in (dst_k, dst_v):
+        if any(t.shape != side[0].shape for t in side):
+            raise PkvError(PKV_ERR_INVALID_ARG, "swap_blocks: destination pools differ in shape")
+    Ns, H, B, D = src_k[0].shape
+    Nd = dst_k[0].shape[0]
+    if tuple(dst_k[0].shape[1:]) != (H, B, D):
+        raise PkvError(PKV_ERR_INVALID_ARG, "swap_blocks: pools differ in [H, B, D]")
+    _need(block_mapping, "block_mapping", torch.int64, 2, cuda=False)
+    if block_mapping.shape[1] != 2 or not (block_mapping.is_cuda or block_mapping.is_pinned()):
+        raise PkvError(PKV_ERR_INVALID_ARG, "swap_blocks: block_mapping must be [P, 2], on the GPU or pinned")
+    arr = lambda ts: ctypes.cast((ctypes.c_void_p * L)(*[t.data_ptr() for t in ts]), ctypes.c_void_p)
+    _check(load().pkv_swap_blocks(arr(src_k), arr(src_v), arr(dst_k), arr(dst_v), L, block_mapping.data_ptr(),
+                                  block_mapping.shape[0], H, D, B, Ns, Nd, _stream(stream)))
 
 
 # ---- host block manager -----------------------------------------------------------------------

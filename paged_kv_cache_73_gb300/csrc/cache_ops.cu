@@ -56,6 +56,46 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
 
 constexpr int kMaxLayersPerLaunch = 64;
 
+struct TokenLayerPtrs {
+  const uint4* key[kMaxLayersPerLaunch];
+  const uint4* value[kMaxLayersPerLaunch];
+  uint4* k_cache[kMaxLayersPerLaunch];
+  uint4* v_cache[kMaxLayersPerLaunch];
+};
+
+// reshape_and_cache for many layers at once: grid.y is the layer; the same slots for every layer.
+__global__ void __launch_bounds__(256) reshape_and_cache_layers_kernel(const TokenLayerPtrs ptrs,
+                                                                       const int64_t* __restrict__ slot_mapping,
+                                                                       int64_t total, int num_heads, int vec_per_row,
+                                                                       int block_size, int64_t num_slots) {
+  pkv::pdl_trigger();
+  pkv::pdl_wait();
+  const int layer = blockIdx.y;
+  const uint4* __restrict__ key = ptrs.key[layer];
+  const uint4* __restrict__ value = ptrs.value[layer];
+  uint4* __restrict__ k_cache = ptrs.k_cache[layer];
+  uint4* __restrict__ v_cache = ptrs.v_cache[layer];
+  const int64_t per_token = static_cast<int64_t>(num_heads) * vec_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int64_t rem = i - t * per_token;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      record_error(PKV_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / block_size;
+    const int64_t row = slot - blk * block_size;
+    const int64_t h = rem / vec_per_row;
+    const int64_t c = rem - h * vec_per_row;
+    const int64_t dst = ((blk * num_heads + h) * block_size + row) * vec_per_row + c;
+    k_cache[dst] = key[i];
+    v_cache[dst] = value[i];
+  }
+}
+
 struct LayerPtrs {
   uint4* k[kMaxLayersPerLaunch];
   uint4* v[kMaxLayersPerLaunch];
@@ -100,7 +140,66 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const LayerPtrs ptrs, 
   }
 }
 
+struct PoolPairPtrs {
+  const uint4* src_k[kMaxLayersPerLaunch];
+  const uint4* src_v[kMaxLayersPerLaunch];
+  uint4* dst_k[kMaxLayersPerLaunch];
+  uint4* dst_v[kMaxLayersPerLaunch];
+};
+
+// grid (num_pairs, num_layers, splits): CTA (p, l, z) copies slice z of block src_p of layer l's
+// source pools into block dst_p of its destination pools.  Either side may be page-locked host
+// memory (reached over the C2C link) or device memory.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const PoolPairPtrs ptrs, const int64_t* __restrict__ mapping,
+                                                          int64_t vec_per_block, int src_blocks, int dst_blocks) {
+  pkv::pdl_trigger();
+  pkv::pdl_wait();
+  const int pair = blockIdx.x;
+  const int layer = blockIdx.y;
+  const int64_t src = mapping[2 * pair];
+  const int64_t dst = mapping[2 * pair + 1];
+  if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+    if (threadIdx.x == 0 && blockIdx.z == 0) record_error(PKV_DEV_BAD_COPY_PAIR);
+    return;
+  }
+  const uint4* __restrict__ ks = ptrs.src_k[layer] + src * vec_per_block;
+  const uint4* __restrict__ vs = ptrs.src_v[layer] + src * vec_per_block;
+  uint4* __restrict__ kd = ptrs.dst_k[layer] + dst * vec_per_block;
+  uint4* __restrict__ vd = ptrs.dst_v[layer] + dst * vec_per_block;
+  const int64_t stride = static_cast<int64_t>(gridDim.z) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.z) * blockDim.x + threadIdx.x;
+  // eight 16-byte loads in flight per thread: reads over the host link have a long latency
+  for (; i + 3 * stride < vec_per_block; i += 4 * stride) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a[u] = ks[i + u * stride];
+      b[u] = vs[i + u * stride];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      kd[i + u * stride] = a[u];
+      vd[i + u * stride] = b[u];
+    }
+  }
+  for (; i < vec_per_block; i += stride) {
+    kd[i] = ks[i];
+    vd[i] = vs[i];
+  }
+}
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// A pointer a kernel may dereference: device, managed or page-locked (registered) host memory.
+bool device_accessible(const void* ptr) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+         (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+}
 
 int check_shape(const char* fn, int num_heads, int head_dim, int block_size, int num_blocks) {
   if (num_heads <= 0 || num_blocks <= 0)
@@ -194,6 +293,102 @@ int pkv_copy_blocks(uint16_t* const* k_caches, uint16_t* const* v_caches, int nu
                                     block_mapping, vec_per_block, num_blocks);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_copy_blocks launch: %s", cudaGetErrorString(e));
+  }
+  pkv::clear_error();
+  return PKV_OK;
+}
+
+int pkv_swap_blocks(const uint16_t* const* src_k_caches, const uint16_t* const* src_v_caches,
+                    uint16_t* const* dst_k_caches, uint16_t* const* dst_v_caches, int num_layers,
+                    const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim, int block_size,
+                    int src_num_blocks, int dst_num_blocks, void* stream) {
+  int rc = check_shape("pkv_swap_blocks", num_heads, head_dim, block_size, src_num_blocks);
+  if (rc != PKV_OK) return rc;
+  if (dst_num_blocks <= 0 || num_pairs < 0 || num_layers < 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_swap_blocks: dst_num_blocks=%d num_pairs=%d num_layers=%d",
+                     dst_num_blocks, num_pairs, num_layers);
+  if (num_pairs == 0 || num_layers == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (!src_k_caches || !src_v_caches || !dst_k_caches || !dst_v_caches || !block_mapping)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_swap_blocks: null pointer");
+  if (!device_accessible(block_mapping))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_swap_blocks: block_mapping is not device-accessible memory");
+  for (int l = 0; l < num_layers; ++l) {
+    const void* p4[4] = {src_k_caches[l], src_v_caches[l], dst_k_caches[l], dst_v_caches[l]};
+    for (const void* ptr : p4) {
+      if (!ptr || !aligned16(ptr))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_swap_blocks: layer %d pool pointer null or not 16-byte aligned", l);
+      if (!device_accessible(ptr))
+        return pkv::fail(PKV_ERR_INVALID_ARG,
+                         "pkv_swap_blocks: layer %d pool is neither device memory nor page-locked host memory", l);
+    }
+  }
+  const int64_t vec_per_block = static_cast<int64_t>(num_heads) * block_size * head_dim / 8;
+  int splits = static_cast<int>((vec_per_block + 256 * 8 - 1) / (256 * 8));
+  if (splits < 1) splits = 1;
+  if (splits > 64) splits = 64;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+    const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
+    PoolPairPtrs ptrs{};
+    for (int l = 0; l < nl; ++l) {
+      ptrs.src_k[l] = reinterpret_cast<const uint4*>(src_k_caches[l0 + l]);
+      ptrs.src_v[l] = reinterpret_cast<const uint4*>(src_v_caches[l0 + l]);
+      ptrs.dst_k[l] = reinterpret_cast<uint4*>(dst_k_caches[l0 + l]);
+      ptrs.dst_v[l] = reinterpret_cast<uint4*>(dst_v_caches[l0 + l]);
+    }
+    cudaError_t e = pkv::launch_pdl(swap_blocks_kernel, dim3(num_pairs, nl, splits), dim3(256), 0, st, ptrs,
+                                    block_mapping, vec_per_block, src_num_blocks, dst_num_blocks);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_swap_blocks launch: %s", cudaGetErrorString(e));
+  }
+  pkv::clear_error();
+  return PKV_OK;
+}
+
+int pkv_reshape_and_cache_layers(const uint16_t* const* keys, const uint16_t* const* values, uint16_t* const* k_caches,
+                                 uint16_t* const* v_caches, int num_layers, const int64_t* slot_mapping, int num_tokens,
+                                 int num_heads, int head_dim, int block_size, int num_blocks, void* stream) {
+  int rc = check_shape("pkv_reshape_and_cache_layers", num_heads, head_dim, block_size, num_blocks);
+  if (rc != PKV_OK) return rc;
+  if (num_tokens < 0 || num_layers < 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache_layers: num_tokens=%d num_layers=%d", num_tokens,
+                     num_layers);
+  if (num_tokens == 0 || num_layers == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (!keys || !values || !k_caches || !v_caches || !slot_mapping)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache_layers: null pointer");
+  for (int l = 0; l < num_layers; ++l) {
+    const void* p4[4] = {keys[l], values[l], k_caches[l], v_caches[l]};
+    for (const void* ptr : p4)
+      if (!ptr || !aligned16(ptr))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache_layers: layer %d pointer null or not 16-byte aligned", l);
+  }
+  const int vec = head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * num_heads * vec;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < (1 << 16) ? want : (1 << 16));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+    const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
+    TokenLayerPtrs ptrs{};
+    for (int l = 0; l < nl; ++l) {
+      ptrs.key[l] = reinterpret_cast<const uint4*>(keys[l0 + l]);
+      ptrs.value[l] = reinterpret_cast<const uint4*>(values[l0 + l]);
+      ptrs.k_cache[l] = reinterpret_cast<uint4*>(k_caches[l0 + l]);
+      ptrs.v_cache[l] = reinterpret_cast<uint4*>(v_caches[l0 + l]);
+    }
+    cudaError_t e = pkv::launch_pdl(reshape_and_cache_layers_kernel, dim3(blocks, nl), dim3(threads), 0, st, ptrs,
+                                    slot_mapping, total, num_heads, vec, block_size,
+                                    static_cast<int64_t>(num_blocks) * block_size);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess)
+      return pkv::fail(PKV_ERR_CUDA, "pkv_reshape_and_cache_layers launch: %s", cudaGetErrorString(e));
   }
   pkv::clear_error();
   return PKV_OK;

@@ -133,3 +133,41 @@ def test_copy_blocks_bad_pair_recorded(cuda_device):
     v = torch.zeros_like(k)
     pkv.copy_blocks([k], [v], torch.tensor([[0, 9]], dtype=torch.int64, device=cuda_device))
     assert pkv.device_error() == 4
+
+
+def test_forty_layer_reshape_and_copy_in_one_launch(cuda_device):
+    # the OPT-13B layer count: every layer's new tokens and copy-on-write copies in one launch each
+    L, H, D, B, N, T = 40, 8, 128, 16, 24, 20
+    ks = [wl.dense_tensor((N, H, B, D), 600 + l, wl.STREAM_K, cuda_device) for l in range(L)]
+    vs = [wl.dense_tensor((N, H, B, D), 600 + l, wl.STREAM_V, cuda_device) for l in range(L)]
+    keys = [wl.dense_tensor((T, H, D), 700 + l, wl.STREAM_NEW_K, cuda_device) for l in range(L)]
+    vals = [wl.dense_tensor((T, H, D), 700 + l, wl.STREAM_NEW_V, cuda_device) for l in range(L)]
+    rng = np.random.default_rng(40)
+    slots = rng.choice(N * B, size=T, replace=False).astype(np.int64)
+    slots[5] = -1
+    k_ref = [_bits(x).copy() for x in ks]
+    v_ref = [_bits(x).copy() for x in vs]
+    pkv.reshape_and_cache_layers(keys, vals, ks, vs, torch.from_numpy(slots).to(cuda_device))
+    assert pkv.device_error() == 0
+    for l in range(L):
+        oracle_cache_ops.reshape_and_cache(_bits(keys[l]), _bits(vals[l]), k_ref[l], v_ref[l], slots)
+        assert np.array_equal(_bits(ks[l]), k_ref[l]) and np.array_equal(_bits(vs[l]), v_ref[l])
+    pairs = np.array([[3, 20], [4, 21], [3, 22]], dtype=np.int64)
+    pkv.copy_blocks(ks, vs, torch.from_numpy(pairs).to(cuda_device))
+    assert pkv.device_error() == 0
+    oracle_cache_ops.copy_blocks(k_ref, v_ref, pairs.tolist())
+    for l in range(L):
+        assert np.array_equal(_bits(ks[l]), k_ref[l]) and np.array_equal(_bits(vs[l]), v_ref[l])
+
+
+def test_more_layers_than_one_launch_holds(cuda_device):
+    L, H, D, B, N = 70, 2, 64, 8, 6                    # two launches of up to 64 layers
+    ks = [wl.dense_tensor((N, H, B, D), 800 + l, wl.STREAM_K, cuda_device) for l in range(L)]
+    vs = [wl.dense_tensor((N, H, B, D), 800 + l, wl.STREAM_V, cuda_device) for l in range(L)]
+    k_ref = [_bits(x).copy() for x in ks]
+    v_ref = [_bits(x).copy() for x in vs]
+    pairs = np.array([[0, 5], [2, 4]], dtype=np.int64)
+    pkv.copy_blocks(ks, vs, torch.from_numpy(pairs).to(cuda_device))
+    oracle_cache_ops.copy_blocks(k_ref, v_ref, pairs.tolist())
+    assert all(np.array_equal(_bits(ks[l]), k_ref[l]) for l in range(L))
+    assert all(np.array_equal(_bits(vs[l]), v_ref[l]) for l in range(L))

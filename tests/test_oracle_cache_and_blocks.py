@@ -343,3 +343,27 @@ def test_beam_step_all_or_nothing():
     assert list(bm.free_list) == before[0] and set(bm.seqs) == {0}
     out = bm.beam_step([0, 0, 0], [1, 2, 3], [0])                    # needs 2 copies: fits
     assert sum(1 for _, s, _ in out if s >= 0) == 2 and bm.num_free() == 0
+
+
+def test_swap_out_and_back_restores_blocks():
+    rng = np.random.default_rng(8)
+    L, N, M, H, B, D = 2, 10, 6, 2, 4, 8
+    dev_k = [rng.standard_normal((N, H, B, D)).astype(np.float16) for _ in range(L)]
+    dev_v = [rng.standard_normal((N, H, B, D)).astype(np.float16) for _ in range(L)]
+    orig_k = [x.copy() for x in dev_k]
+    host_k = [np.zeros((M, H, B, D), np.float16) for _ in range(L)]
+    host_v = [np.zeros((M, H, B, D), np.float16) for _ in range(L)]
+    out_map = [(3, 0), (7, 1), (9, 2)]
+    oc.swap_blocks(dev_k, dev_v, host_k, host_v, out_map)
+    for layer in range(L):
+        for s, d in out_map:
+            np.testing.assert_array_equal(host_k[layer][d], dev_k[layer][s])
+            np.testing.assert_array_equal(host_v[layer][d], dev_v[layer][s])
+        np.testing.assert_array_equal(host_k[layer][3:], 0)
+    for layer in range(L):                      # the device blocks are reused meanwhile
+        dev_k[layer][[3, 7, 9]] = 0
+    back_map = [(0, 1), (1, 4), (2, 5)]         # swapped back in, into other free blocks
+    oc.swap_blocks(host_k, host_v, dev_k, dev_v, back_map)
+    for layer in range(L):
+        for (s0, _), (_, d1) in zip(out_map, back_map):
+            np.testing.assert_array_equal(dev_k[layer][d1], orig_k[layer][s0])
