@@ -22,36 +22,47 @@ __device__ int g_dev_error_cache_ops = 0;
 
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_dev_error_cache_ops, 0, code); }
 
-// One thread moves one 16-byte column of one (token, head) row of K and of V.
-// vec_per_row = head_dim / 8.
+// Token t's key and value rows (all heads) go to slot slot_mapping[t]: one CTA per token, its
+// threads walking the H * D/8 16-byte columns.  head_dim/8 and block_size are powers of two, so
+// every index is a shift or a mask.
+__device__ __forceinline__ void store_tokens(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                                             uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                             const int64_t* __restrict__ slot_mapping, int num_tokens,
+                                             int num_heads, int log2_vec, int log2_block, int64_t num_slots) {
+  const int per_token = num_heads << log2_vec;
+  const int vec_mask = (1 << log2_vec) - 1;
+  const int row_mask = (1 << log2_block) - 1;
+  for (int t = blockIdx.x; t < num_tokens; t += gridDim.x) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;                        // padding token
+    if (slot >= num_slots) {
+      if (threadIdx.x == 0) record_error(PKV_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot >> log2_block;
+    const int row = static_cast<int>(slot & row_mask);
+    const uint4* __restrict__ ksrc = key + static_cast<int64_t>(t) * per_token;
+    const uint4* __restrict__ vsrc = value + static_cast<int64_t>(t) * per_token;
+    for (int e = threadIdx.x; e < per_token; e += blockDim.x) {
+      const int h = e >> log2_vec;
+      const int c = e & vec_mask;
+      const int64_t dst = ((((blk * num_heads + h) << log2_block) + row) << log2_vec) + c;
+      k_cache[dst] = ksrc[e];
+      v_cache[dst] = vsrc[e];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __restrict__ key,
                                                                 const uint4* __restrict__ value,
                                                                 uint4* __restrict__ k_cache,
                                                                 uint4* __restrict__ v_cache,
                                                                 const int64_t* __restrict__ slot_mapping,
-                                                                int64_t total, int num_heads, int vec_per_row,
-                                                                int block_size, int64_t num_slots) {
+                                                                int num_tokens, int num_heads, int log2_vec,
+                                                                int log2_block, int64_t num_slots) {
   pkv::pdl_trigger();
   pkv::pdl_wait();  // key/value/slots may come from the previous kernel on the stream
-  const int64_t per_token = static_cast<int64_t>(num_heads) * vec_per_row;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = i / per_token;
-    const int64_t rem = i - t * per_token;         // h * vec_per_row + c
-    const int64_t slot = slot_mapping[t];
-    if (slot < 0) continue;                        // padding token
-    if (slot >= num_slots) {
-      record_error(PKV_DEV_BAD_SLOT);
-      continue;
-    }
-    const int64_t blk = slot / block_size;
-    const int64_t row = slot - blk * block_size;
-    const int64_t h = rem / vec_per_row;
-    const int64_t c = rem - h * vec_per_row;
-    const int64_t dst = ((blk * num_heads + h) * block_size + row) * vec_per_row + c;
-    k_cache[dst] = key[i];
-    v_cache[dst] = value[i];
-  }
+  store_tokens(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_heads, log2_vec, log2_block, num_slots);
 }
 
 constexpr int kMaxLayersPerLaunch = 64;
@@ -66,34 +77,13 @@ struct TokenLayerPtrs {
 // reshape_and_cache for many layers at once: grid.y is the layer; the same slots for every layer.
 __global__ void __launch_bounds__(256) reshape_and_cache_layers_kernel(const TokenLayerPtrs ptrs,
                                                                        const int64_t* __restrict__ slot_mapping,
-                                                                       int64_t total, int num_heads, int vec_per_row,
-                                                                       int block_size, int64_t num_slots) {
+                                                                       int num_tokens, int num_heads, int log2_vec,
+                                                                       int log2_block, int64_t num_slots) {
   pkv::pdl_trigger();
   pkv::pdl_wait();
   const int layer = blockIdx.y;
-  const uint4* __restrict__ key = ptrs.key[layer];
-  const uint4* __restrict__ value = ptrs.value[layer];
-  uint4* __restrict__ k_cache = ptrs.k_cache[layer];
-  uint4* __restrict__ v_cache = ptrs.v_cache[layer];
-  const int64_t per_token = static_cast<int64_t>(num_heads) * vec_per_row;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = i / per_token;
-    const int64_t rem = i - t * per_token;
-    const int64_t slot = slot_mapping[t];
-    if (slot < 0) continue;
-    if (slot >= num_slots) {
-      record_error(PKV_DEV_BAD_SLOT);
-      continue;
-    }
-    const int64_t blk = slot / block_size;
-    const int64_t row = slot - blk * block_size;
-    const int64_t h = rem / vec_per_row;
-    const int64_t c = rem - h * vec_per_row;
-    const int64_t dst = ((blk * num_heads + h) * block_size + row) * vec_per_row + c;
-    k_cache[dst] = key[i];
-    v_cache[dst] = value[i];
-  }
+  store_tokens(ptrs.key[layer], ptrs.value[layer], ptrs.k_cache[layer], ptrs.v_cache[layer], slot_mapping,
+               num_tokens, num_heads, log2_vec, log2_block, num_slots);
 }
 
 struct LayerPtrs {
@@ -201,6 +191,20 @@ bool device_accessible(const void* ptr) {
          (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
 }
 
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << (r + 1)) <= x) ++r;
+  return r;
+}
+
+// One CTA per token (grid-stride beyond 2^20 tokens); threads cover a token's H * D/8 columns.
+void reshape_launch_shape(int num_tokens, int num_heads, int head_dim, int* threads, int* grid) {
+  const int per_token = num_heads * (head_dim / 8);
+  int t = per_token < 256 ? (per_token + 31) / 32 * 32 : 256;
+  *threads = t;
+  *grid = num_tokens < (1 << 20) ? num_tokens : (1 << 20);
+}
+
 int check_shape(const char* fn, int num_heads, int head_dim, int block_size, int num_blocks) {
   if (num_heads <= 0 || num_blocks <= 0)
     return pkv::fail(PKV_ERR_INVALID_ARG, "%s: num_heads=%d num_blocks=%d", fn, num_heads, num_blocks);
@@ -243,16 +247,13 @@ int pkv_reshape_and_cache(const uint16_t* key, const uint16_t* value, uint16_t* 
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache: null pointer");
   if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache: key, value and caches must be 16-byte aligned");
-  const int vec = head_dim / 8;
-  const int64_t total = static_cast<int64_t>(num_tokens) * num_heads * vec;
-  const int threads = 256;
-  const int64_t want = (total + threads - 1) / threads;
-  const int blocks = static_cast<int>(want < (1 << 20) ? want : (1 << 20));
-  cudaError_t e = pkv::launch_pdl(
-      reshape_and_cache_kernel, dim3(blocks), dim3(threads), 0, static_cast<cudaStream_t>(stream),
-      reinterpret_cast<const uint4*>(key), reinterpret_cast<const uint4*>(value), reinterpret_cast<uint4*>(k_cache),
-      reinterpret_cast<uint4*>(v_cache), slot_mapping, total, num_heads, vec, block_size,
-      static_cast<int64_t>(num_blocks) * block_size);
+  int threads = 0, grid = 0;
+  reshape_launch_shape(num_tokens, num_heads, head_dim, &threads, &grid);
+  cudaError_t e = pkv::launch_pdl(reshape_and_cache_kernel, dim3(grid), dim3(threads), 0,
+                                  static_cast<cudaStream_t>(stream), reinterpret_cast<const uint4*>(key),
+                                  reinterpret_cast<const uint4*>(value), reinterpret_cast<uint4*>(k_cache),
+                                  reinterpret_cast<uint4*>(v_cache), slot_mapping, num_tokens, num_heads,
+                                  ilog2(head_dim / 8), ilog2(block_size), static_cast<int64_t>(num_blocks) * block_size);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "pkv_reshape_and_cache launch: %s", cudaGetErrorString(e));
   pkv::clear_error();
@@ -368,11 +369,8 @@ int pkv_reshape_and_cache_layers(const uint16_t* const* keys, const uint16_t* co
       if (!ptr || !aligned16(ptr))
         return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_reshape_and_cache_layers: layer %d pointer null or not 16-byte aligned", l);
   }
-  const int vec = head_dim / 8;
-  const int64_t total = static_cast<int64_t>(num_tokens) * num_heads * vec;
-  const int threads = 256;
-  const int64_t want = (total + threads - 1) / threads;
-  const int blocks = static_cast<int>(want < (1 << 16) ? want : (1 << 16));
+  int threads = 0, grid = 0;
+  reshape_launch_shape(num_tokens, num_heads, head_dim, &threads, &grid);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
     const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
@@ -383,8 +381,8 @@ int pkv_reshape_and_cache_layers(const uint16_t* const* keys, const uint16_t* co
       ptrs.k_cache[l] = reinterpret_cast<uint4*>(k_caches[l0 + l]);
       ptrs.v_cache[l] = reinterpret_cast<uint4*>(v_caches[l0 + l]);
     }
-    cudaError_t e = pkv::launch_pdl(reshape_and_cache_layers_kernel, dim3(blocks, nl), dim3(threads), 0, st, ptrs,
-                                    slot_mapping, total, num_heads, vec, block_size,
+    cudaError_t e = pkv::launch_pdl(reshape_and_cache_layers_kernel, dim3(grid, nl), dim3(threads), 0, st, ptrs,
+                                    slot_mapping, num_tokens, num_heads, ilog2(head_dim / 8), ilog2(block_size),
                                     static_cast<int64_t>(num_blocks) * block_size);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess)
