@@ -80,3 +80,36 @@ def paged_decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarr
         values = gather_sequence(v_cache, block_tables[s], ctx)
         out[s] = contiguous_attention(q[s], keys, values, scale)
     return out
+
+
+def paged_prefill_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                            block_tables: np.ndarray, context_lens: np.ndarray,
+                            query_start: np.ndarray, scale: float) -> np.ndarray:
+    """Attention of every new token of every sequence over its cached context, float64.
+
+    The prompt phase over the task input only ([guide] 04, shared prefix: the
+    request maps its first logical blocks onto the cached prefix blocks and the
+    prompt phase runs only over its own tokens), with the attention of [note]
+    关键设计 1 for each of those tokens: token i of the n_s new tokens of sequence
+    s sits at position p = ctx_s - n_s + i and attends to positions t <= p
+    (the sum to t = i of the first equation).
+
+    q [T_total, H, D]: the new tokens of sequence s are rows
+    query_start[s] .. query_start[s+1] - 1.  context_lens[s] counts the cached
+    tokens and the new ones (whose keys and values are already in the pool).
+    Returns [T_total, H, D].
+    """
+    T, H, D = q.shape
+    out = np.zeros((T, H, D), dtype=np.float64)
+    for s in range(len(context_lens)):
+        ctx = int(context_lens[s])
+        q0, q1 = int(query_start[s]), int(query_start[s + 1])
+        n = q1 - q0
+        if n == 0:
+            continue
+        keys = gather_sequence(k_cache, block_tables[s], ctx)
+        values = gather_sequence(v_cache, block_tables[s], ctx)
+        for i in range(n):
+            p = ctx - n + i
+            out[q0 + i] = contiguous_attention(q[q0 + i], keys[:p + 1], values[:p + 1], scale)
+    return out
