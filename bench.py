@@ -16,12 +16,13 @@ the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity|beam_search
-                              |swap|layers40]
+                              |swap|layers40|prefill]
                   [--capacity-seqs S] [--capacity-block B] [--pool-frac F]
 
-`--workload swap` and `--workload layers40` print their own lines (swap_blocks
-between HBM and page-locked host memory; 40-layer copy_blocks and
-reshape_and_cache in one launch) with their own metric names.
+`--workload swap`, `--workload layers40` and `--workload prefill` print their
+own lines (swap_blocks between HBM and page-locked host memory; 40-layer
+copy_blocks and reshape_and_cache in one launch; prefill attention over a
+cached prefix on the tensor cores) with their own metric names.
 
 The default workload is the headline one above.  The others build their batch
 through the same block manager (prompt forks with copy-on-write, a shared
@@ -397,7 +398,7 @@ def run_gpu(args, rank, world, dev):
     return res
 
 
-AUX_WORKLOADS = ("swap", "layers40")
+AUX_WORKLOADS = ("swap", "layers40", "prefill")
 
 
 def _timed(fn, reps=10, warm=3):
@@ -494,6 +495,69 @@ def run_layers40(args, dev):
                             "per_layer_launches_ms": t_cL, "per_layer_GB/s": gbs(c_bytes, t_cL)},
             "reshape_and_cache": {"one_launch_ms": t_r1, "one_launch_GB/s": gbs(r_bytes, t_r1),
                                   "per_layer_launches_ms": t_rL, "per_layer_GB/s": gbs(r_bytes, t_rL)}}
+
+
+def run_prefill(args, dev):
+    """Prefill over a cached prefix: the shared-prefix batch (256 requests, one cached 1024-token
+    prefix, suffixes U[32, 512]) writes every suffix token's K/V (reshape_and_cache) and runs
+    paged prefill attention for the suffix tokens over prefix + causal suffix."""
+    import torch
+    from paged_kv_cache_73_gb300 import binding as pkv
+    from paged_kv_cache_73_gb300 import workloads as wl
+    w = wl.shared_prefix(seed=SEED)
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    news = np.array([int(c) - 1024 for c in w.context_lens])
+    qs = np.concatenate([[0], np.cumsum(news)]).astype(np.int32)
+    T = int(qs[-1])
+    slots = []
+    for s_, (c, n) in enumerate(zip(w.context_lens, news)):
+        for pos in range(int(c) - int(n), int(c)):
+            slots.append(int(w.block_tables[s_, pos // B]) * B + pos % B)
+    k, v = w.pools(dev)
+    q = wl.dense_tensor((T, H, D), SEED, wl.STREAM_Q, dev)
+    key, value = wl.new_tokens(T, H, D, SEED, dev)
+    tables = torch.from_numpy(w.block_tables).to(dev)
+    lens = torch.from_numpy(w.context_lens).to(dev)
+    qsd = torch.from_numpy(qs).to(dev)
+    slots_d = torch.tensor(slots, dtype=torch.int64, device=dev)
+    out = torch.empty_like(q)
+    maxq = int(news.max())
+    flops = sum(4 * D * H * int((np.arange(int(c) - int(n), int(c)) + 1).sum()) for c, n in zip(w.context_lens, news))
+    attn = lambda: pkv.paged_attention_prefill(q, k, v, tables, lens, qsd, w.scale, B, maxq, out=out)
+
+    def step():
+        pkv.reshape_and_cache(key, value, k, v, slots_d)
+        attn()
+
+    steps = max(3, min(args.steps, 50))
+    with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
+        t_step = _timed(step, reps=steps, warm=max(args.warmup, 3))
+        t_attn = _timed(attn, reps=steps, warm=3)
+    assert pkv.device_error() == 0
+    peak = measured_tensor_peak()
+    achieved = flops / (t_attn * 1e-3) / 1e12
+    return {"metric": "paged prefill attention TFLOP/s (new tokens over cached prefix + causal suffix)",
+            "value": flops / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": t_step, "higher_is_better": True, "dtype": "f16 in, f32 acc",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": "prefill: 256 requests, cached 1024-token prefix (shared blocks), suffixes "
+                                   "U[32,512] prefilled; 40 x 128, block 16", "new_tokens": T,
+                       "attention_flops": flops},
+            "tokens_per_s": T / (t_step * 1e-3),
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel", "achieved": achieved,
+                         "peak": peak[0], "unit": "TFLOP/s", "frac": achieved / peak[0], "traffic": None,
+                         "launch_ms": t_attn, "peak_source": peak[1]},
+            "clocks": clocks.summary()}
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured bf16 dense burst (MEASURED_PEAKS.json bf16_tflops; fp16 has the same nominal rate), of measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 burst"
 
 
 def pool_blocks_for(args, dev):
@@ -688,7 +752,7 @@ def main():
     if args.workload in AUX_WORKLOADS:
         from paged_kv_cache_73_gb300 import binding as pkv
         pkv.load()
-        line = (run_swap if args.workload == "swap" else run_layers40)(args, dev)
+        line = {"swap": run_swap, "layers40": run_layers40, "prefill": run_prefill}[args.workload](args, dev)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return

@@ -59,7 +59,8 @@ enum {
   PKV_DEV_BAD_CONTEXT_LEN = 2,  /* a context length < 0 or > max_blocks_per_seq*block_size */
   PKV_DEV_BAD_SLOT = 3,         /* a slot >= num_blocks*block_size */
   PKV_DEV_BAD_COPY_PAIR = 4,    /* a copy pair with an id outside [0, num_blocks) */
-  PKV_DEV_WAIT_TIMEOUT = 5      /* a shared-memory copy did not complete in time */
+  PKV_DEV_WAIT_TIMEOUT = 5,     /* a shared-memory copy did not complete in time */
+  PKV_DEV_BAD_QUERY_RANGE = 6   /* prefill: new tokens outside [0, context_len] or outside q */
 };
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
@@ -120,6 +121,35 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
                                int num_seqs, int num_heads, int head_dim, int num_blocks,
                                int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Paged prefill attention: the new tokens of each sequence (the task input)
+ * over its cached context plus, causally, themselves ([guide] 04: the prompt
+ * phase runs only over the task input, the request's first logical blocks
+ * mapped onto cached prefix blocks; [note] 关键设计 1, first equation).
+ *
+ * Sequence s has n_s = query_start[s+1] - query_start[s] new tokens, rows
+ * query_start[s] .. query_start[s+1]-1 of q and out; their keys and values are
+ * already in the pools (reshape_and_cache), and context_lens[s] counts the
+ * cached tokens plus the new ones.  New token i (position p = ctx_s - n_s + i):
+ *   out[query_start[s] + i, h, :] = sum_{t <= p} softmax_t(scale * q . k_t) v_t
+ * with k_t read through block_tables as in pkv_paged_attention_decode.
+ * Tensor cores: fp16 products, fp32 accumulation; the softmax weights are
+ * rounded to fp16 before they multiply V.
+ *
+ *   q, out        device [total_q, num_heads, head_dim] fp16, 16-byte aligned
+ *   query_start   device [num_seqs + 1] int32, non-decreasing, last = total_q
+ *   max_query_len host: the largest n_s (sizes the grid; larger n_s are not
+ *                 fully processed)
+ *   pools, tables, context_lens as for pkv_paged_attention_decode.
+ * A sequence with n_s = 0 is skipped; n_s > ctx_s or rows outside q record
+ * PKV_DEV_BAD_QUERY_RANGE.  No workspace.
+ * ------------------------------------------------------------------------- */
+int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* query_start, int num_seqs, int total_q, int max_query_len,
+                                int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq,
+                                float scale, int block_size, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Paged decode attention with the library's own scratch (no counterpart in the

@@ -27,7 +27,7 @@ PKV_ERR_DEVICE_CHECK = -6
 PKV_ERR_NOT_FOUND = -7
 
 DEV_CODES = {0: "ok", 1: "bad block id", 2: "bad context length", 3: "bad slot", 4: "bad copy pair",
-             5: "wait timeout"}
+             5: "wait timeout", 6: "bad query range"}
 
 
 class PkvError(RuntimeError):
@@ -56,6 +56,8 @@ _SIGNATURES = {
     "pkv_paged_attention_static_workspace_bytes": (_SZ, []),
     "pkv_paged_attention_decode_static_workspace": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I,
                                                          _P, _P]),
+    "pkv_paged_attention_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _c.c_float, _I, _P,
+                                         _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_reshape_and_cache_layers": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
@@ -195,6 +197,34 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
         S, H, D, N, max_blocks, float(scale), block_size, out.data_ptr(), _ptr(workspace), ws_bytes,
         _stream(stream)))
+    return out
+
+
+def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, query_start: torch.Tensor,
+                            scale: float, block_size: int, max_query_len: int,
+                            out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The new tokens of each sequence over its cached context plus, causally, themselves."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(query_start, "query_start", torch.int32, 1)
+    T, H, D = q.shape
+    S = context_lens.shape[0]
+    if query_start.shape[0] != S + 1 or block_tables.shape[0] != S:
+        raise PkvError(PKV_ERR_INVALID_ARG, "query_start must have num_seqs + 1 entries")
+    if tuple(k_cache.shape[1:]) != (H, block_size, D) or v_cache.shape != k_cache.shape:
+        raise PkvError(PKV_ERR_INVALID_ARG, "cache shape does not match [N, H, B, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, 3)
+    _check(load().pkv_paged_attention_prefill(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+        query_start.data_ptr(), S, T, int(max_query_len), H, D, k_cache.shape[0], block_tables.shape[1],
+        float(scale), block_size, out.data_ptr(), _stream(stream)))
     return out
 
 

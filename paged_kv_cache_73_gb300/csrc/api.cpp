@@ -35,12 +35,14 @@ int pkv_device_error(void* stream, int reset, int* code) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess)
     return pkv::fail(PKV_ERR_CUDA, "pkv_device_error: cudaStreamSynchronize: %s", cudaGetErrorString(e));
-  int a = 0, c = 0;
+  int a = 0, c = 0, f = 0;
   int st = pkv::read_device_error_attention(reset, &a);
   if (st != PKV_OK) return st;
   st = pkv::read_device_error_cache_ops(reset, &c);
   if (st != PKV_OK) return st;
-  int first = a ? a : c;
+  st = pkv::read_device_error_prefill(reset, &f);
+  if (st != PKV_OK) return st;
+  int first = a ? a : (c ? c : f);
   if (code) *code = first;
   if (first) return pkv::fail(PKV_ERR_DEVICE_CHECK, "a kernel recorded device check code %d", first);
   return PKV_OK;

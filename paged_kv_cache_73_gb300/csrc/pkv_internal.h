@@ -22,5 +22,6 @@ void clear_error();
 // launches kernels defines one.  They synchronise nothing themselves.
 int read_device_error_attention(int reset, int* code);
 int read_device_error_cache_ops(int reset, int* code);
+int read_device_error_prefill(int reset, int* code);
 
 }  // namespace pkv
