@@ -9,15 +9,14 @@
 // sequence s, at position p = ctx_s - n_s + i, gets
 // o = sum_{t <= p} softmax_t(scale * q.k_t) v_t.
 //
-// Design: a dense contraction, so it runs on the tensor cores (mma.sync
-// m16n8k16, fp16 inputs, fp32 accumulation).  One CTA (4 warps) owns 64 new
-// tokens of one (sequence, head); each warp owns 16 of them.  Key tiles of 64
-// positions are gathered block by block through the table with 16-byte
-// cp.async copies into XOR-swizzled shared memory (conflict-free ldmatrix),
-// double-buffered.  S = Q K^T and O += P V per tile with an online softmax in
-// base 2; P is rounded to fp16 for the second product, as flash attention does.
-// Key rows past the context are zero-filled (never read), so stale NaN/Inf in
-// unfilled slots cannot reach a product.
+// Design: a dense contraction, so it runs on the fifth-generation tensor cores
+// (tcgen05.mma, fp16 inputs, fp32 accumulation in tensor memory); see the
+// kernel's comment below.  Key tiles of 64 positions are gathered block by
+// block through the table with 16-byte cp.async copies into the 128-byte
+// swizzled layout the tensor cores read, double-buffered.  P is rounded to
+// fp16 for the second product, as flash attention does.  Key rows past the
+// context are zero-filled (never read), so stale NaN/Inf in unfilled slots
+// cannot reach a product.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -33,10 +32,6 @@ namespace {
 __device__ int g_dev_error_prefill = 0;
 __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_dev_error_prefill, 0, code); }
 
-constexpr unsigned FULL = 0xffffffffu;
-constexpr int BM = 64;   // new tokens per CTA
-constexpr int BN = 64;   // key positions per tile
-constexpr int NWARP = 4;
 
 struct PrefillParams {
   const __half* q;
@@ -67,77 +62,191 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in a [rows][D] fp16 tile whose chunks are
-// XOR-swizzled by the row's low three bits.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return static_cast<uint32_t>((row * (D / 8) + (chunk ^ (row & 7))) * 16);
+// ---- fifth-generation tensor cores (tcgen05): S, P and O live in tensor memory ---------------
+//
+// One CTA (4 warps, 128 threads) owns 128 new tokens of one (sequence, head); thread t owns
+// token row t, which is TMEM lane t.  Per key tile of 64 positions:
+//   1. one thread issues S = Q K^T (tcgen05.mma, M=128, N=64, fp16 in, fp32 in TMEM) and commits
+//      it to an mbarrier;
+//   2. every thread reads its row of S from TMEM (tcgen05.ld), masks it, updates its running
+//      max/sum and writes P = 2^(S - m) as fp16 back to TMEM (tcgen05.st);
+//   3. one thread issues O += P V (A = P from TMEM, B = V from shared memory, MN-major) into the
+//      TMEM accumulator and commits it.
+// The running max m of a row is only moved (and O rescaled) when a tile raises it by more than
+// 2^8, so P stays within fp16 range while most tiles skip the O read-modify-write.
+// Q, K and V tiles sit in shared memory in the canonical K-major / MN-major layouts with 128-byte
+// swizzle: rows of 64 elements (128 B), 16-byte chunks XOR-ed with the row's low three bits,
+// 8-row groups 1024 B apart, head-dimension halves in separate regions.
+constexpr int TC_BM = 128;  // new tokens per CTA (MMA M)
+constexpr int TC_BN = 64;   // key positions per tile (S MMA N, PV MMA K)
+constexpr float TC_RESCALE = 8.f;
+
+__device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  // start >> 4 | LBO >> 4 | SBO >> 4 | fixed 0b001 at bit 46 | swizzle mode 2 (128-byte) at bit 61
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+// kind::f16 instruction descriptor: fp32 accumulate, fp16 A and B, dense.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init1(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_parity(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait (2 s): false if the phase did not complete in time.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_parity(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait_parity(bar, parity)) return true;
+    if ((it & 255u) == 255u && global_ns() - t0 > 2000000000ull) return false;
+  }
+  return false;
+}
+
+// Byte offset of (row, 16-byte chunk) in a K-major / MN-major tile with 128-byte swizzle whose
+// head-dimension halves are regions of `rows` x 128 B.
+__device__ __forceinline__ uint32_t sw128(int row, int chunk, int rows) {
+  return static_cast<uint32_t>((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
 template <int D>
-__global__ void __launch_bounds__(NWARP * 32, 2) paged_prefill_kernel(const PrefillParams p) {
-  constexpr int CPR = D / 8;                     // 16-byte chunks per row
-  constexpr int KSTEPS = D / 16;                 // k16 steps over the head dimension
-  constexpr int TILE = BN * D * 2;               // bytes of one K (or V) tile
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* sq = smem;                      // [BM][D]
-  unsigned char* sk = smem + BM * D * 2;         // [2][BN][D]
-  unsigned char* sv = sk + 2 * TILE;             // [2][BN][D]
+struct TcCfg {
+  static constexpr int Q_BYTES = TC_BM * D * 2;
+  static constexpr int KV_BYTES = TC_BN * D * 2;
+  // sized as for D = 128 whatever D is: at most two CTAs per SM, so their 2 x 256 tensor-memory
+  // columns always fit in the SM's 512
+  static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 64;
+  static constexpr uint32_t TMEM_COLS = 256;    // S: 64, P: 32, O: D (<= 128)
+  static constexpr uint32_t S_COL = 0, P_COL = 64, O_COL = 128;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillParams p) {
+  using C = TcCfg<D>;
+  constexpr int CPR = D / 8;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (base - raw);
+  const uint32_t sq = base;
+  const uint32_t sk0 = sq + C::Q_BYTES, sv0 = sk0 + 2 * C::KV_BYTES;
+  const uint32_t bar_s = sv0 + 2 * C::KV_BYTES, bar_o = bar_s + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_o + 8 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
   const int qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int H = p.num_heads;
   const int B = 1 << p.log2_block;
   const int ctx = p.lens[s];
   const int q0 = p.qstart[s];
   const int n = p.qstart[s + 1] - q0;
-  const int i0 = qt * BM;
+  const int i0 = qt * TC_BM;
   if (n < 0 || n > ctx || ctx > p.max_blocks * B || q0 < 0 || q0 + n > p.total_q) {
     if (tid == 0 && qt == 0) record_error(ctx > p.max_blocks * B ? PKV_DEV_BAD_CONTEXT_LEN : PKV_DEV_BAD_QUERY_RANGE);
     return;
   }
   if (i0 >= n) return;
-  const int first_pos = ctx - n + i0;                             // position of the tile's first token
-  const int last_pos = ctx - n + min(i0 + BM, n) - 1;             // and of its last valid token
-  const int n_tiles = last_pos / BN + 1;
+  const int first_pos = ctx - n + i0;
+  const int last_pos = ctx - n + min(i0 + TC_BM, n) - 1;
+  const int n_tiles = last_pos / TC_BN + 1;
 
-  // Q tile -> shared memory (rows past the new tokens are zero)
-  for (int e = tid; e < BM * CPR; e += NWARP * 32) {
-    const int r = e / CPR, c = e % CPR;
-    const int i = i0 + r;
-    const __half* src = p.q + (static_cast<size_t>(q0 + min(i, n - 1)) * H + h) * D + c * 8;
-    cp_async16(smem_u32(sq) + swz<D>(r, c), src, i < n ? 16 : 0);
+  // tensor memory for S, P and O; barriers for the two MMA groups
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  if (tid == 0) {
+    mbar_init1(bar_s);
+    mbar_init1(bar_o);
+  }
+  // Q tile: thread t copies token row t (rows past the new tokens are zero)
+  {
+    const int i = i0 + tid;
+    const __half* src = p.q + (static_cast<size_t>(q0 + min(i, n - 1)) * H + h) * D;
+#pragma unroll
+    for (int c = 0; c < CPR; ++c) cp_async16(sq + sw128(tid, c, TC_BM), src + c * 8, i < n ? 16 : 0);
   }
   const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
   int bad = 0;
   auto load_tile = [&](int j, int stage) {
-    // two threads per key row, each half of the row's chunks
-    const int r = tid >> 1;
-    const int t = j * BN + r;
+    const int r = tid >> 1;                       // two threads per key row
+    const int t = j * TC_BN + r;
     const bool valid = t < ctx;
     int phys = 0;
     if (valid) {
@@ -151,155 +260,174 @@ __global__ void __launch_bounds__(NWARP * 32, 2) paged_prefill_kernel(const Pref
     const size_t row = ((static_cast<size_t>(phys) * H + h) << p.log2_block) + (t & (B - 1));
     const __half* ksrc = p.k + row * D;
     const __half* vsrc = p.v + row * D;
-    const uint32_t kdst = smem_u32(sk + stage * TILE), vdst = smem_u32(sv + stage * TILE);
+    const uint32_t kd = sk0 + stage * C::KV_BYTES, vd = sv0 + stage * C::KV_BYTES;
 #pragma unroll
     for (int c0 = 0; c0 < CPR / 2; ++c0) {
       const int c = (tid & 1) * (CPR / 2) + c0;
-      cp_async16(kdst + swz<D>(r, c), ksrc + c * 8, ok ? 16 : 0);
-      cp_async16(vdst + swz<D>(r, c), vsrc + c * 8, ok ? 16 : 0);
+      cp_async16(kd + sw128(r, c, TC_BN), ksrc + c * 8, ok ? 16 : 0);
+      cp_async16(vd + sw128(r, c, TC_BN), vsrc + c * 8, ok ? 16 : 0);
     }
   };
   load_tile(0, 0);
   cp_async_commit();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t t_s = tmem + C::S_COL, t_p = tmem + C::P_COL, t_o = tmem + C::O_COL;
 
-  // per-warp state: 16 rows (lane/4 and lane/4 + 8 of the warp's slice)
-  float o[D / 8][4];
-#pragma unroll
-  for (int d = 0; d < D / 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-  uint32_t qa[KSTEPS][4];
-  const int g = lane >> 2, tq = lane & 3;
-  const int row_lo = i0 + warp * 16 + g;                          // new-token index of this lane's rows
-  const int pos_lo = ctx - n + row_lo, pos_hi = pos_lo + 8;
-
-  for (int j = 0; j < n_tiles; ++j) {
-    if (j + 1 < n_tiles) load_tile(j + 1, (j + 1) & 1);
+  constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
+  constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
+  const int row_i = i0 + tid;
+  const int pos = ctx - n + row_i;                 // this thread's token position
+  float m_ref = -INFINITY, l = 0.f;
+  bool timed_out = false;
+  int s_issued = 0, o_issued = 0;                  // commits made on each barrier
+  for (int j = 0; j < n_tiles && !timed_out; ++j) {
+    const int stage = j & 1;
+    // the previous PV must be done: it reads P and the other stage's V
+    if (j > 0) {
+      const bool ok = mbar_wait(bar_o, (j - 1) & 1);
+      if (__syncthreads_or(!ok)) {                 // one decision for the whole CTA
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+    }
+    if (j + 1 < n_tiles) load_tile(j + 1, stage ^ 1);
     cp_async_commit();
     cp_async_wait<1>();
+    fence_proxy_async_smem();                      // cp.async writes -> tensor-core reads
     __syncthreads();
-    if (j == 0) {
-      // this warp's Q fragments, once
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t kb = sk0 + stage * C::KV_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        const int mi = lane >> 3, r = lane & 7;
-        ldsm_x4(smem_u32(sq) + swz<D>(warp * 16 + r + (mi & 1) * 8, kk * 2 + (mi >> 1)), qa[kk]);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
+        const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+        umma_ss(t_s, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(bar_s);
+    }
+    ++s_issued;
+    {
+      const bool ok = mbar_wait(bar_s, j & 1);
+      if (__syncthreads_or(!ok)) {
+        timed_out = true;
+        break;
       }
     }
-    const uint32_t kb = smem_u32(sk + (j & 1) * TILE), vb = smem_u32(sv + (j & 1) * TILE);
-
-    // S = Q K^T for 16 rows x 64 keys
-    float sc[BN / 8][4];
+    tc_fence_after();
+    // softmax of this thread's row of S
+    float sv[TC_BN];
+    {
+      float a[32], b2[32];
+      tmem_ld32(t_s + lane_off, a);
+      tmem_ld32(t_s + lane_off + 32, b2);
 #pragma unroll
-    for (int nt = 0; nt < BN / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-#pragma unroll
-      for (int pr = 0; pr < BN / 16; ++pr) {
-        uint32_t b[4];
-        const int mi = lane >> 3, r = lane & 7;
-        ldsm_x4(kb + swz<D>(pr * 16 + r + (mi >> 1) * 8, kk * 2 + (mi & 1)), b);
-        mma16816(sc[2 * pr], qa[kk], b[0], b[1]);
-        mma16816(sc[2 * pr + 1], qa[kk], b[2], b[3]);
+      for (int c = 0; c < 32; ++c) {
+        sv[c] = a[c];
+        sv[32 + c] = b2[c];
       }
     }
-    // scale, mask (causal and past the context), online softmax in base 2
-    const bool need_mask = (j + 1) * BN - 1 > first_pos;
-    float mx_lo = -INFINITY, mx_hi = -INFINITY;
+    const bool need_mask = (j + 1) * TC_BN - 1 > first_pos;
+    float mx = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < BN / 8; ++nt) {
+    for (int c = 0; c < TC_BN; ++c) {
+      float x = sv[c] * p.scale_log2;
+      if (need_mask && j * TC_BN + c > pos) x = -INFINITY;
+      sv[c] = x;
+      mx = fmaxf(mx, x);
+    }
+    const bool rescale = mx > m_ref + TC_RESCALE;  // also true for the first finite max
+    float alpha = 1.f;
+    if (rescale) {
+      alpha = exp2f(m_ref - mx);                   // 0 when m_ref = -inf
+      m_ref = mx;
+    }
+    const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+    float sum = 0.f;
+    uint32_t pk[32];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = j * BN + nt * 8 + tq * 2 + e;
-        float lo = sc[nt][e] * p.scale_log2, hi = sc[nt][2 + e] * p.scale_log2;
-        if (need_mask) {
-          if (t > pos_lo) lo = -INFINITY;
-          if (t > pos_hi) hi = -INFINITY;
-        }
-        sc[nt][e] = lo;
-        sc[nt][2 + e] = hi;
-        mx_lo = fmaxf(mx_lo, lo);
-        mx_hi = fmaxf(mx_hi, hi);
+    for (int c = 0; c < 32; ++c) {
+      const float e0 = exp2f(sv[2 * c] - ref), e1 = exp2f(sv[2 * c + 1] - ref);
+      sum += e0 + e1;
+      pk[c] = pack_half2(e0, e1);
+    }
+    l = l * alpha + sum;
+    tmem_st32(t_p + lane_off, pk);
+    // tcgen05.ld/st are warp-collective: if any row of the warp moved its max, the whole warp
+    // rewrites its O rows (alpha is 1 for the rows that did not move)
+    if (__any_sync(0xffffffffu, rescale && j > 0)) {
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(t_o + lane_off + c * 32, o);
+        uint32_t ob[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
+        tmem_st32(t_o + lane_off + c * 32, ob);
       }
     }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL, mx_hi, 2));
-    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-    // a row with every key masked so far keeps m = -inf; use 0 as its reference
-    const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo, ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-    const float al_lo = exp2f(m_lo - ref_lo), al_hi = exp2f(m_hi - ref_hi);
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-    float sum_lo = 0.f, sum_hi = 0.f;
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t vb = sv0 + stage * C::KV_BYTES;
 #pragma unroll
-    for (int nt = 0; nt < BN / 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        sc[nt][e] = exp2f(sc[nt][e] - ref_lo);
-        sc[nt][2 + e] = exp2f(sc[nt][2 + e] - ref_hi);
-        sum_lo += sc[nt][e];
-        sum_hi += sc[nt][2 + e];
+      for (int kk = 0; kk < TC_BN / 16; ++kk) {
+        const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
+        umma_ts(t_o, t_p + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
       }
+      umma_commit(bar_o);
     }
-    l_lo = l_lo * al_lo + sum_lo;
-    l_hi = l_hi * al_hi + sum_hi;
-#pragma unroll
-    for (int d = 0; d < D / 8; ++d) {
-      o[d][0] *= al_lo;
-      o[d][1] *= al_lo;
-      o[d][2] *= al_hi;
-      o[d][3] *= al_hi;
-    }
-    // O += P V: P's accumulators become the A fragments of 16-key steps
-#pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_half2(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = pack_half2(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = pack_half2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = pack_half2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b[4];
-        const int mi = lane >> 3, r = lane & 7;
-        ldsm_x4_trans(vb + swz<D>(kk * 16 + r + (mi & 1) * 8, dp * 2 + (mi >> 1)), b);
-        mma16816(o[2 * dp], pa, b[0], b[1]);
-        mma16816(o[2 * dp + 1], pa, b[2], b[3]);
-      }
-    }
-    __syncthreads();                               // the stage is refilled next iteration
+    ++o_issued;
   }
+  if (!timed_out) {
+    const bool ok = mbar_wait(bar_o, (n_tiles - 1) & 1);
+    timed_out = __syncthreads_or(!ok);
+    tc_fence_after();
+  }
+  if (timed_out) {
+    // let this CTA's tensor-core work in flight finish (bounded) before its memory is released
+    if (s_issued > 0) mbar_wait(bar_s, (s_issued - 1) & 1);
+    if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1);
+  }
+  cp_async_wait<0>();
   bad = __syncthreads_or(bad);
-  if (bad) {
+  if (timed_out) {
+    if (tid == 0) record_error(PKV_DEV_WAIT_TIMEOUT);
+  } else if (bad) {
     if (tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
-    return;
-  }
-
-  // normalise and store the warp's rows that are real new tokens
-  l_lo += __shfl_xor_sync(FULL, l_lo, 1);
-  l_lo += __shfl_xor_sync(FULL, l_lo, 2);
-  l_hi += __shfl_xor_sync(FULL, l_hi, 1);
-  l_hi += __shfl_xor_sync(FULL, l_hi, 2);
-  const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f, inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
-  const int row_hi = row_lo + 8;
+  } else {
+    // every lane loads (warp-collective); only rows that are real new tokens are stored
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __half* dst = p.out + (static_cast<size_t>(q0 + min(row_i, n - 1)) * H + h) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      float o[32];
+      tmem_ld32(t_o + lane_off + c * 32, o);
+      if (row_i >= n) continue;
 #pragma unroll
-  for (int d = 0; d < D / 8; ++d) {
-    const int col = d * 8 + tq * 2;
-    if (row_lo < n) {
-      __half2* dst = reinterpret_cast<__half2*>(p.out + (static_cast<size_t>(q0 + row_lo) * H + h) * D + col);
-      *dst = __floats2half2_rn(o[d][0] * inv_lo, o[d][1] * inv_lo);
-    }
-    if (row_hi < n) {
-      __half2* dst = reinterpret_cast<__half2*>(p.out + (static_cast<size_t>(q0 + row_hi) * H + h) * D + col);
-      *dst = __floats2half2_rn(o[d][2] * inv_hi, o[d][3] * inv_hi);
+      for (int e = 0; e < 32; e += 8) {
+        uint4 w;
+        w.x = pack_half2(o[e] * inv, o[e + 1] * inv);
+        w.y = pack_half2(o[e + 2] * inv, o[e + 3] * inv);
+        w.z = pack_half2(o[e + 4] * inv, o[e + 5] * inv);
+        w.w = pack_half2(o[e + 6] * inv, o[e + 7] * inv);
+        *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
+      }
     }
   }
-}
-
-template <int D>
-constexpr size_t prefill_smem() {
-  return static_cast<size_t>(BM) * D * 2 + 4 * static_cast<size_t>(BN) * D * 2;
+  // all tensor-memory reads are done (tcgen05.ld waits inline); release the columns
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+  }
 }
 
 template <int D>
@@ -311,14 +439,14 @@ int launch_prefill(const PrefillParams& p, int num_seqs, int max_query_len, cuda
   if (e == cudaSuccess) {
     std::lock_guard<std::mutex> g(mu);
     if (dev < 0 || dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(paged_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(prefill_smem<D>()));
+      e = cudaFuncSetAttribute(paged_prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               TcCfg<D>::SMEM);
       if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     }
   }
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill setup: %s", cudaGetErrorString(e));
-  dim3 grid((max_query_len + BM - 1) / BM, p.num_heads, num_seqs);
-  e = pkv::launch_pdl(paged_prefill_kernel<D>, grid, dim3(NWARP * 32), prefill_smem<D>(), st, p);
+  dim3 grid((max_query_len + TC_BM - 1) / TC_BM, p.num_heads, num_seqs);
+  e = pkv::launch_pdl(paged_prefill_tc_kernel<D>, grid, dim3(128), TcCfg<D>::SMEM, st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill launch: %s", cudaGetErrorString(e));
   return PKV_OK;
