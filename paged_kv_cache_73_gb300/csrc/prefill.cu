@@ -70,13 +70,11 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // ---- fifth-generation tensor cores (tcgen05): S, P and O live in tensor memory ---------------
 //
 // One CTA (4 warps, 128 threads) owns 128 new tokens of one (sequence, head); thread t owns
-// token row t, which is TMEM lane t.  Per key tile of 64 positions:
-//   1. one thread issues S = Q K^T (tcgen05.mma, M=128, N=64, fp16 in, fp32 in TMEM) and commits
-//      it to an mbarrier;
-//   2. every thread reads its row of S from TMEM (tcgen05.ld), masks it, updates its running
-//      max/sum and writes P = 2^(S - m) as fp16 back to TMEM (tcgen05.st);
-//   3. one thread issues O += P V (A = P from TMEM, B = V from shared memory, MN-major) into the
-//      TMEM accumulator and commits it.
+// token row t, which is TMEM lane t.  Per key tile of 64 positions one thread issues
+// S = Q K^T (tcgen05.mma, M=128, N=64, fp16 in, fp32 in TMEM); every thread reads its row of S
+// (tcgen05.ld), masks it, updates its running max/sum and writes P = 2^(S - m) as fp16 back to
+// TMEM (tcgen05.st); one thread issues O += P V (A = P from TMEM, B = V from shared memory,
+// MN-major) into the TMEM accumulator.  MMA groups complete on mbarriers.
 // The running max m of a row is only moved (and O rescaled) when a tile raises it by more than
 // 2^8, so P stays within fp16 range while most tiles skip the O read-modify-write.
 // Q, K and V tiles sit in shared memory in the canonical K-major / MN-major layouts with 128-byte
@@ -187,10 +185,24 @@ struct TcCfg {
   // sized as for D = 128 whatever D is: at most two CTAs per SM, so their 2 x 256 tensor-memory
   // columns always fit in the SM's 512
   static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 64;
-  static constexpr uint32_t TMEM_COLS = 256;    // S: 64, P: 32, O: D (<= 128)
-  static constexpr uint32_t S_COL = 0, P_COL = 64, O_COL = 128;
+  static constexpr uint32_t TMEM_COLS = 256;    // S ping: 64, S pong: 64 (P over its first 32), O: D
+  static constexpr uint32_t S_COL0 = 0, S_COL1 = 64, O_COL = 128;
 };
 
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Software pipeline per key tile j (thread 0 issues every MMA; all 128 threads do the softmax):
+//   wait S(j); wait PV(j-1); wait this thread's loads; barrier
+//   thread 0: S(j+1) = Q K(j+1)^T into the other S buffer   -- overlaps the softmax below
+//   all: start loading K(j+2) (K ring slot of j) and V(j+1) (V ring slot of j+1)
+//   all: softmax(j) from S(j); P(j) as fp16 over S(j)'s first 32 columns; rescale O if needed
+//   barrier; thread 0: O += P(j) V(j)
+// A K slot is reused once its S MMA has completed, a V slot and an S buffer once the PV MMA
+// that read them has completed, which the waits at the top of the next tile establish.
 template <int D>
 __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillParams p) {
   using C = TcCfg<D>;
@@ -201,8 +213,8 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
   unsigned char* smem = smem_raw + (base - raw);
   const uint32_t sq = base;
   const uint32_t sk0 = sq + C::Q_BYTES, sv0 = sk0 + 2 * C::KV_BYTES;
-  const uint32_t bar_s = sv0 + 2 * C::KV_BYTES, bar_o = bar_s + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_o + 8 - base));
+  const uint32_t bar_s0 = sv0 + 2 * C::KV_BYTES, bar_s1 = bar_s0 + 8, bar_o = bar_s0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_s0 + 24 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -223,7 +235,6 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
   const int last_pos = ctx - n + min(i0 + TC_BM, n) - 1;
   const int n_tiles = last_pos / TC_BN + 1;
 
-  // tensor memory for S, P and O; barriers for the two MMA groups
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(C::TMEM_COLS)
@@ -232,7 +243,8 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
     tc_fence_before();
   }
   if (tid == 0) {
-    mbar_init1(bar_s);
+    mbar_init1(bar_s0);
+    mbar_init1(bar_s1);
     mbar_init1(bar_o);
   }
   // Q tile: thread t copies token row t (rows past the new tokens are zero)
@@ -244,8 +256,10 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
   }
   const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
   int bad = 0;
-  auto load_tile = [&](int j, int stage) {
-    const int r = tid >> 1;                       // two threads per key row
+  // rows of key tile j into a K or V slot: two threads per key row, each half of its chunks;
+  // positions past the context are zero-filled and never read
+  auto load_rows = [&](const __half* pool, int j, uint32_t dst) {
+    const int r = tid >> 1;
     const int t = j * TC_BN + r;
     const bool valid = t < ctx;
     int phys = 0;
@@ -257,74 +271,72 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
       }
     }
     const bool ok = valid && !bad;
-    const size_t row = ((static_cast<size_t>(phys) * H + h) << p.log2_block) + (t & (B - 1));
-    const __half* ksrc = p.k + row * D;
-    const __half* vsrc = p.v + row * D;
-    const uint32_t kd = sk0 + stage * C::KV_BYTES, vd = sv0 + stage * C::KV_BYTES;
+    const __half* src = pool + (((static_cast<size_t>(phys) * H + h) << p.log2_block) + (t & (B - 1))) * D;
 #pragma unroll
     for (int c0 = 0; c0 < CPR / 2; ++c0) {
       const int c = (tid & 1) * (CPR / 2) + c0;
-      cp_async16(kd + sw128(r, c, TC_BN), ksrc + c * 8, ok ? 16 : 0);
-      cp_async16(vd + sw128(r, c, TC_BN), vsrc + c * 8, ok ? 16 : 0);
+      cp_async16(dst + sw128(r, c, TC_BN), src + c * 8, ok ? 16 : 0);
     }
   };
-  load_tile(0, 0);
+  // prologue: K(0), V(0), K(1)
+  load_rows(p.k, 0, sk0);
+  load_rows(p.v, 0, sv0);
+  if (n_tiles > 1) load_rows(p.k, 1, sk0 + C::KV_BYTES);
   cp_async_commit();
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t t_s = tmem + C::S_COL, t_p = tmem + C::P_COL, t_o = tmem + C::O_COL;
-
+  const uint32_t t_o = tmem + C::O_COL;
   constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
   constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
+
+  auto issue_s = [&](int j) {                      // thread 0: S(j) = Q K(j)^T
+    tc_fence_after();
+    const uint32_t kb = sk0 + (j & 1) * C::KV_BYTES;
+    const uint32_t ts = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
+      const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+      umma_ss(ts, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+    }
+    umma_commit((j & 1) ? bar_s1 : bar_s0);
+  };
+  if (tid == 0) issue_s(0);
+
   const int row_i = i0 + tid;
-  const int pos = ctx - n + row_i;                 // this thread's token position
+  const int pos = ctx - n + row_i;
   float m_ref = -INFINITY, l = 0.f;
   bool timed_out = false;
-  int s_issued = 0, o_issued = 0;                  // commits made on each barrier
-  for (int j = 0; j < n_tiles && !timed_out; ++j) {
-    const int stage = j & 1;
-    // the previous PV must be done: it reads P and the other stage's V
-    if (j > 0) {
-      const bool ok = mbar_wait(bar_o, (j - 1) & 1);
-      if (__syncthreads_or(!ok)) {                 // one decision for the whole CTA
-        timed_out = true;
-        break;
-      }
-      tc_fence_after();
-    }
-    if (j + 1 < n_tiles) load_tile(j + 1, stage ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    fence_proxy_async_smem();                      // cp.async writes -> tensor-core reads
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t kb = sk0 + stage * C::KV_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-        const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-        umma_ss(t_s, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
-      }
-      umma_commit(bar_s);
-    }
-    ++s_issued;
-    {
-      const bool ok = mbar_wait(bar_s, j & 1);
-      if (__syncthreads_or(!ok)) {
-        timed_out = true;
-        break;
-      }
+  int s_issued = 1, o_issued = 0;
+  for (int j = 0; j < n_tiles; ++j) {
+    const uint32_t ts = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
+    bool ok = mbar_wait((j & 1) ? bar_s1 : bar_s0, (j >> 1) & 1);
+    if (j > 0) ok = mbar_wait(bar_o, (j - 1) & 1) && ok;
+    cp_async_wait<0>();                            // K(j+1), V(j) issued last tile
+    fence_proxy_async_smem();
+    if (__syncthreads_or(!ok)) {                   // one decision for the whole CTA
+      timed_out = true;
+      break;
     }
     tc_fence_after();
-    // softmax of this thread's row of S
+    if (j + 1 < n_tiles) {
+      if (tid == 0) issue_s(j + 1);
+      ++s_issued;
+    }
+    if (j + 2 < n_tiles) load_rows(p.k, j + 2, sk0 + (j & 1) * C::KV_BYTES);
+    if (j + 1 < n_tiles) load_rows(p.v, j + 1, sv0 + ((j + 1) & 1) * C::KV_BYTES);
+    cp_async_commit();
+
+    // softmax of this thread's row of S(j)
     float sv[TC_BN];
     {
       float a[32], b2[32];
-      tmem_ld32(t_s + lane_off, a);
-      tmem_ld32(t_s + lane_off + 32, b2);
+      tmem_ld32(ts + lane_off, a);
+      tmem_ld32(ts + lane_off + 32, b2);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         sv[c] = a[c];
@@ -351,12 +363,12 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
     uint32_t pk[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
-      const float e0 = exp2f(sv[2 * c] - ref), e1 = exp2f(sv[2 * c + 1] - ref);
+      const float e0 = fast_exp2(sv[2 * c] - ref), e1 = fast_exp2(sv[2 * c + 1] - ref);
       sum += e0 + e1;
       pk[c] = pack_half2(e0, e1);
     }
     l = l * alpha + sum;
-    tmem_st32(t_p + lane_off, pk);
+    tmem_st32(ts + lane_off, pk);                  // P(j) over S(j)'s first 32 columns
     // tcgen05.ld/st are warp-collective: if any row of the warp moved its max, the whole warp
     // rewrites its O rows (alpha is 1 for the rows that did not move)
     if (__any_sync(0xffffffffu, rescale && j > 0)) {
@@ -375,11 +387,11 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t vb = sv0 + stage * C::KV_BYTES;
+      const uint32_t vb = sv0 + (j & 1) * C::KV_BYTES;
 #pragma unroll
       for (int kk = 0; kk < TC_BN / 16; ++kk) {
         const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
-        umma_ts(t_o, t_p + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_ts(t_o, ts + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
       }
       umma_commit(bar_o);
     }
@@ -392,7 +404,10 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
   }
   if (timed_out) {
     // let this CTA's tensor-core work in flight finish (bounded) before its memory is released
-    if (s_issued > 0) mbar_wait(bar_s, (s_issued - 1) & 1);
+    for (int k = 0; k < 2; ++k) {
+      const int cnt = (s_issued + 1 - k) / 2;      // commits on S buffer k
+      if (cnt > 0) mbar_wait(k ? bar_s1 : bar_s0, (cnt - 1) & 1);
+    }
     if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1);
   }
   cp_async_wait<0>();
