@@ -57,11 +57,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// Commits this thread's outstanding cp.async copies and waits until all of them have landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -143,9 +140,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void mbar_init1(uint32_t bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+__device__ __forceinline__ void mbar_init_count(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_parity(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -184,7 +184,7 @@ struct TcCfg {
   static constexpr int KV_BYTES = TC_BN * D * 2;
   // sized as for D = 128 whatever D is: at most two CTAs per SM, so their 2 x 256 tensor-memory
   // columns always fit in the SM's 512
-  static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 64;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 128;
   static constexpr uint32_t TMEM_COLS = 256;    // S ping: 64, S pong: 64 (P over its first 32), O: D
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 64, O_COL = 128;
 };
@@ -195,16 +195,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Software pipeline per key tile j (thread 0 issues every MMA; all 128 threads do the softmax):
-//   wait S(j); wait PV(j-1); wait this thread's loads; barrier
-//   thread 0: S(j+1) = Q K(j+1)^T into the other S buffer   -- overlaps the softmax below
-//   all: start loading K(j+2) (K ring slot of j) and V(j+1) (V ring slot of j+1)
-//   all: softmax(j) from S(j); P(j) as fp16 over S(j)'s first 32 columns; rescale O if needed
-//   barrier; thread 0: O += P(j) V(j)
-// A K slot is reused once its S MMA has completed, a V slot and an S buffer once the PV MMA
-// that read them has completed, which the waits at the top of the next tile establish.
+// Warp roles (7 warps):
+//   warps 0-3  softmax: thread t owns token row t = TMEM lane t.  For tile j it waits S(j), reads
+//              its row, masks it, updates its running max/sum, writes P(j) as fp16 over S(j)'s
+//              first 32 columns (rescaling its O row first when its max moved by > 2^8) and
+//              arrives on p_full.
+//   warp 4     MMA: one lane issues S(j) = Q K(j)^T into S buffer j%2 once tile j has landed and
+//              PV(j-2) (the last reader of that buffer) is done, then O += P(j-1) V(j-1) once
+//              P(j-1) is written.  S(j) thus runs on the tensor cores while the softmax warps work
+//              on tile j-1.
+//   warps 5, 6 loads: gather tile j's K (warp 5) or V (warp 6) rows through the table into slot
+//              j%2 (cp.async, 128-byte swizzle) once S(j-2) (for K) or PV(j-2) (for V) has
+//              released the slot, then signal k_full / v_full.
+// Hand-offs are mbarriers (per S buffer / stage, so no waiter can fall two phases behind); every
+// wait is bounded, and a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop, so
+// the others give up in turn and the CTA still reaches its final barrier.
+constexpr int TC_THREADS = 224;
+
 template <int D>
-__global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const PrefillParams p) {
   using C = TcCfg<D>;
   constexpr int CPR = D / 8;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -213,13 +222,21 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
   unsigned char* smem = smem_raw + (base - raw);
   const uint32_t sq = base;
   const uint32_t sk0 = sq + C::Q_BYTES, sv0 = sk0 + 2 * C::KV_BYTES;
-  const uint32_t bar_s0 = sv0 + 2 * C::KV_BYTES, bar_s1 = bar_s0 + 8, bar_o = bar_s0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_s0 + 24 - base));
+  // barriers: s_full[2], p_full[2], pv_done[2], k_full[2], v_full[2]
+  const uint32_t bars = sv0 + 2 * C::KV_BYTES;
+  auto s_full = [&](int b) { return bars + 8u * b; };
+  auto p_full = [&](int b) { return bars + 16u + 8u * b; };
+  auto pv_done = [&](int b) { return bars + 32u + 8u * b; };
+  auto k_full = [&](int b) { return bars + 48u + 8u * b; };
+  auto v_full = [&](int b) { return bars + 64u + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 80 - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 84 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
-  const int qt = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  // the last query tiles of a sequence see the most keys: launch them first
+  const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.num_heads;
   const int B = 1 << p.log2_block;
   const int ctx = p.lens[s];
@@ -243,181 +260,210 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
     tc_fence_before();
   }
   if (tid == 0) {
-    mbar_init1(bar_s0);
-    mbar_init1(bar_s1);
-    mbar_init1(bar_o);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init_count(s_full(b), 1);
+      mbar_init_count(p_full(b), 128);
+      mbar_init_count(pv_done(b), 1);
+      mbar_init_count(k_full(b), 32);
+      mbar_init_count(v_full(b), 32);
+    }
+    *abort_flag = 0;
   }
-  // Q tile: thread t copies token row t (rows past the new tokens are zero)
-  {
+  if (tid < TC_BM) {
+    // Q tile: softmax thread t copies token row t (rows past the new tokens are zero)
     const int i = i0 + tid;
     const __half* src = p.q + (static_cast<size_t>(q0 + min(i, n - 1)) * H + h) * D;
 #pragma unroll
     for (int c = 0; c < CPR; ++c) cp_async16(sq + sw128(tid, c, TC_BM), src + c * 8, i < n ? 16 : 0);
+    cp_async_wait_all();
+    fence_proxy_async_smem();
   }
-  const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
-  int bad = 0;
-  // rows of key tile j into a K or V slot: two threads per key row, each half of its chunks;
-  // positions past the context are zero-filled and never read
-  auto load_rows = [&](const __half* pool, int j, uint32_t dst) {
-    const int r = tid >> 1;
-    const int t = j * TC_BN + r;
-    const bool valid = t < ctx;
-    int phys = 0;
-    if (valid) {
-      phys = table[t >> p.log2_block];
-      if (phys < 0 || phys >= p.num_blocks) {
-        bad = 1;
-        phys = 0;
-      }
-    }
-    const bool ok = valid && !bad;
-    const __half* src = pool + (((static_cast<size_t>(phys) * H + h) << p.log2_block) + (t & (B - 1))) * D;
-#pragma unroll
-    for (int c0 = 0; c0 < CPR / 2; ++c0) {
-      const int c = (tid & 1) * (CPR / 2) + c0;
-      cp_async16(dst + sw128(r, c, TC_BN), src + c * 8, ok ? 16 : 0);
-    }
-  };
-  // prologue: K(0), V(0), K(1)
-  load_rows(p.k, 0, sk0);
-  load_rows(p.v, 0, sv0);
-  if (n_tiles > 1) load_rows(p.k, 1, sk0 + C::KV_BYTES);
-  cp_async_commit();
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t t_o = tmem + C::O_COL;
-  constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
-  constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
-
-  auto issue_s = [&](int j) {                      // thread 0: S(j) = Q K(j)^T
-    tc_fence_after();
-    const uint32_t kb = sk0 + (j & 1) * C::KV_BYTES;
-    const uint32_t ts = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-      const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-      umma_ss(ts, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
-    }
-    umma_commit((j & 1) ? bar_s1 : bar_s0);
+  auto s_col = [&](int j) { return tmem + ((j & 1) ? C::S_COL1 : C::S_COL0); };
+  auto give_up = [&]() {
+    if (!*abort_flag) record_error(PKV_DEV_WAIT_TIMEOUT);
+    *abort_flag = 1;
   };
-  if (tid == 0) issue_s(0);
+  int bad = 0;
+  bool failed = false;
+  float l = 0.f;
 
-  const int row_i = i0 + tid;
-  const int pos = ctx - n + row_i;
-  float m_ref = -INFINITY, l = 0.f;
-  bool timed_out = false;
-  int s_issued = 1, o_issued = 0;
-  for (int j = 0; j < n_tiles; ++j) {
-    const uint32_t ts = tmem + ((j & 1) ? C::S_COL1 : C::S_COL0);
-    bool ok = mbar_wait((j & 1) ? bar_s1 : bar_s0, (j >> 1) & 1);
-    if (j > 0) ok = mbar_wait(bar_o, (j - 1) & 1) && ok;
-    cp_async_wait<0>();                            // K(j+1), V(j) issued last tile
-    fence_proxy_async_smem();
-    if (__syncthreads_or(!ok)) {                   // one decision for the whole CTA
-      timed_out = true;
-      break;
+  if (warp >= 5) {
+    // ---------------- loads: warp 5 gathers K tiles, warp 6 V tiles ----------------
+    // A K slot is free once the S MMA that read it is done; a V slot once its PV MMA is done.
+    const bool is_k = warp == 5;
+    const __half* pool = is_k ? p.k : p.v;
+    const uint32_t slot0 = is_k ? sk0 : sv0;
+    const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      if (j >= 2 && !mbar_wait(is_k ? s_full(st) : pv_done(st), ((j - 2) >> 1) & 1)) {
+        failed = true;
+        break;
+      }
+      if (*abort_flag) break;
+      const uint32_t dst = slot0 + st * C::KV_BYTES;
+#pragma unroll
+      for (int rr = 0; rr < TC_BN / 32; ++rr) {
+        const int r = rr * 32 + lane;
+        const int t = j * TC_BN + r;
+        const bool valid = t < ctx;
+        int phys = valid ? table[t >> p.log2_block] : 0;
+        if (valid && (phys < 0 || phys >= p.num_blocks)) bad = 1;
+        const bool ok = valid && !bad;
+        if (!ok) phys = 0;
+        const __half* src = pool + (((static_cast<size_t>(phys) * H + h) << p.log2_block) + (t & (B - 1))) * D;
+#pragma unroll
+        for (int c = 0; c < CPR; ++c) cp_async16(dst + sw128(r, c, TC_BN), src + c * 8, ok ? 16 : 0);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();                    // cp.async writes -> tensor-core reads
+      mbar_arrive(is_k ? k_full(st) : v_full(st));
     }
-    tc_fence_after();
-    if (j + 1 < n_tiles) {
-      if (tid == 0) issue_s(j + 1);
-      ++s_issued;
+    if (failed) give_up();
+  } else if (warp == 4) {
+    // ---------------- MMA issue (one lane) ----------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
+      constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
+      int s_done = 0, pv_issued = 0;
+      auto issue_pv = [&](int j) -> bool {         // O += P(j) V(j) once P(j) and V(j) are there
+        if (!mbar_wait(p_full(j & 1), (j >> 1) & 1) || !mbar_wait(v_full(j & 1), (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t vb = sv0 + (j & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < TC_BN / 16; ++kk) {
+          const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
+          umma_ts(t_o, s_col(j) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(pv_done(j & 1));
+        ++pv_issued;
+        return true;
+      };
+      for (int j = 0; j < n_tiles && !failed; ++j) {
+        if (*abort_flag) break;
+        // K(j) landed, and PV(j-2), the last reader of S buffer j%2, is done
+        if (!mbar_wait(k_full(j & 1), (j >> 1) & 1) ||
+            (j >= 2 && !mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kb = sk0 + (j & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+          umma_ss(s_col(j), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full(j & 1));
+        s_done = j + 1;
+        if (j >= 1 && !issue_pv(j - 1)) {
+          failed = true;
+          break;
+        }
+      }
+      if (!failed && !*abort_flag && !issue_pv(n_tiles - 1)) failed = true;
+      if (failed || *abort_flag) {
+        give_up();
+        // let the tensor-core work this lane issued finish (bounded) before memory is released
+        if (s_done > 0) mbar_wait(s_full((s_done - 1) & 1), ((s_done - 1) >> 1) & 1);
+        if (pv_issued > 0) mbar_wait(pv_done((pv_issued - 1) & 1), ((pv_issued - 1) >> 1) & 1);
+      }
     }
-    if (j + 2 < n_tiles) load_rows(p.k, j + 2, sk0 + (j & 1) * C::KV_BYTES);
-    if (j + 1 < n_tiles) load_rows(p.v, j + 1, sv0 + ((j + 1) & 1) * C::KV_BYTES);
-    cp_async_commit();
-
-    // softmax of this thread's row of S(j)
-    float sv[TC_BN];
-    {
-      float a[32], b2[32];
-      tmem_ld32(ts + lane_off, a);
-      tmem_ld32(ts + lane_off + 32, b2);
+    __syncwarp();
+  } else {
+    // ---------------- softmax (warps 0-3) ----------------
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int row_i = i0 + tid;
+    const int pos = ctx - n + row_i;
+    float m_ref = -INFINITY;
+    for (int j = 0; j < n_tiles; ++j) {
+      // decisions stay warp-uniform: the tcgen05.ld/st below are warp-collective
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full(j & 1), (j >> 1) & 1))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t ts = s_col(j);
+      float sv[TC_BN];
+      {
+        float a[32], b2[32];
+        tmem_ld32(ts + lane_off, a);
+        tmem_ld32(ts + lane_off + 32, b2);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = a[c];
+          sv[32 + c] = b2[c];
+        }
+      }
+      const bool need_mask = (j + 1) * TC_BN - 1 > first_pos;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TC_BN; ++c) {
+        float x = sv[c] * p.scale_log2;
+        if (need_mask && j * TC_BN + c > pos) x = -INFINITY;
+        sv[c] = x;
+        mx = fmaxf(mx, x);
+      }
+      const bool rescale = mx > m_ref + TC_RESCALE;   // also true for the first finite max
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = exp2f(m_ref - mx);                     // 0 when m_ref = -inf
+        m_ref = mx;
+      }
+      const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+      float sum = 0.f;
+      uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        sv[c] = a[c];
-        sv[32 + c] = b2[c];
+        const float e0 = fast_exp2(sv[2 * c] - ref), e1 = fast_exp2(sv[2 * c + 1] - ref);
+        sum += e0 + e1;
+        pk[c] = pack_half2(e0, e1);
       }
-    }
-    const bool need_mask = (j + 1) * TC_BN - 1 > first_pos;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < TC_BN; ++c) {
-      float x = sv[c] * p.scale_log2;
-      if (need_mask && j * TC_BN + c > pos) x = -INFINITY;
-      sv[c] = x;
-      mx = fmaxf(mx, x);
-    }
-    const bool rescale = mx > m_ref + TC_RESCALE;  // also true for the first finite max
-    float alpha = 1.f;
-    if (rescale) {
-      alpha = exp2f(m_ref - mx);                   // 0 when m_ref = -inf
-      m_ref = mx;
-    }
-    const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-    float sum = 0.f;
-    uint32_t pk[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const float e0 = fast_exp2(sv[2 * c] - ref), e1 = fast_exp2(sv[2 * c + 1] - ref);
-      sum += e0 + e1;
-      pk[c] = pack_half2(e0, e1);
-    }
-    l = l * alpha + sum;
-    tmem_st32(ts + lane_off, pk);                  // P(j) over S(j)'s first 32 columns
-    // tcgen05.ld/st are warp-collective: if any row of the warp moved its max, the whole warp
-    // rewrites its O rows (alpha is 1 for the rows that did not move)
-    if (__any_sync(0xffffffffu, rescale && j > 0)) {
+      l = l * alpha + sum;
+      // tcgen05.ld/st are warp-collective: if any row of the warp moved its max after the first
+      // tile, the whole warp rescales its O rows (alpha is 1 for the rows that did not move), once
+      // PV(j-1) has finished accumulating into them
+      if (__any_sync(0xffffffffu, rescale && j > 0)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(t_o + lane_off + c * 32, o);
-        uint32_t ob[32];
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(t_o + lane_off + c * 32, o);
+          uint32_t ob[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
-        tmem_st32(t_o + lane_off + c * 32, ob);
+          for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
+          tmem_st32(t_o + lane_off + c * 32, ob);
+        }
       }
+      tmem_st32(ts + lane_off, pk);                    // P(j) over S(j)'s first 32 columns
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full(j & 1));
     }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
+    if (!failed && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+      failed = !__all_sync(0xffffffffu, mbar_wait(pv_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1));
       tc_fence_after();
-      const uint32_t vb = sv0 + (j & 1) * C::KV_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < TC_BN / 16; ++kk) {
-        const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
-        umma_ts(t_o, ts + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      umma_commit(bar_o);
     }
-    ++o_issued;
+    if (failed) give_up();
   }
-  if (!timed_out) {
-    const bool ok = mbar_wait(bar_o, (n_tiles - 1) & 1);
-    timed_out = __syncthreads_or(!ok);
-    tc_fence_after();
-  }
-  if (timed_out) {
-    // let this CTA's tensor-core work in flight finish (bounded) before its memory is released
-    for (int k = 0; k < 2; ++k) {
-      const int cnt = (s_issued + 1 - k) / 2;      // commits on S buffer k
-      if (cnt > 0) mbar_wait(k ? bar_s1 : bar_s0, (cnt - 1) & 1);
-    }
-    if (o_issued > 0) mbar_wait(bar_o, (o_issued - 1) & 1);
-  }
-  cp_async_wait<0>();
+
+  // ---------------- epilogue (all warps) ----------------
   bad = __syncthreads_or(bad);
-  if (timed_out) {
-    if (tid == 0) record_error(PKV_DEV_WAIT_TIMEOUT);
-  } else if (bad) {
-    if (tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
-  } else {
+  const bool aborted = *abort_flag != 0;
+  if (warp < 4 && !aborted && !bad) {
     // every lane loads (warp-collective); only rows that are real new tokens are stored
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int row_i = i0 + tid;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __half* dst = p.out + (static_cast<size_t>(q0 + min(row_i, n - 1)) * H + h) * D;
 #pragma unroll 1
@@ -436,6 +482,8 @@ __global__ void __launch_bounds__(128, 1) paged_prefill_tc_kernel(const PrefillP
       }
     }
   }
+  if (bad && tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
+  cp_async_wait_all();
   // all tensor-memory reads are done (tcgen05.ld waits inline); release the columns
   tc_fence_before();
   __syncthreads();
@@ -461,7 +509,7 @@ int launch_prefill(const PrefillParams& p, int num_seqs, int max_query_len, cuda
   }
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill setup: %s", cudaGetErrorString(e));
   dim3 grid((max_query_len + TC_BM - 1) / TC_BM, p.num_heads, num_seqs);
-  e = pkv::launch_pdl(paged_prefill_tc_kernel<D>, grid, dim3(128), TcCfg<D>::SMEM, st, p);
+  e = pkv::launch_pdl(paged_prefill_tc_kernel<D>, grid, dim3(TC_THREADS), TcCfg<D>::SMEM, st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill launch: %s", cudaGetErrorString(e));
   return PKV_OK;
