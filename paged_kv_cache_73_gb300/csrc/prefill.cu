@@ -67,8 +67,8 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // ---- fifth-generation tensor cores (tcgen05): S, P and O live in tensor memory ---------------
 //
 // One CTA (4 warps, 128 threads) owns 128 new tokens of one (sequence, head); thread t owns
-// token row t, which is TMEM lane t.  Per key tile of 64 positions one thread issues
-// S = Q K^T (tcgen05.mma, M=128, N=64, fp16 in, fp32 in TMEM); every thread reads its row of S
+// token row t, which is TMEM lane t.  Per key tile of 128 positions one thread issues
+// S = Q K^T (tcgen05.mma, M=128, N=128, fp16 in, fp32 in TMEM); every thread reads its row of S
 // (tcgen05.ld), masks it, updates its running max/sum and writes P = 2^(S - m) as fp16 back to
 // TMEM (tcgen05.st); one thread issues O += P V (A = P from TMEM, B = V from shared memory,
 // MN-major) into the TMEM accumulator.  MMA groups complete on mbarriers.
@@ -78,7 +78,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // swizzle: rows of 64 elements (128 B), 16-byte chunks XOR-ed with the row's low three bits,
 // 8-row groups 1024 B apart, head-dimension halves in separate regions.
 constexpr int TC_BM = 128;  // new tokens per CTA (MMA M)
-constexpr int TC_BN = 64;   // key positions per tile (S MMA N, PV MMA K)
+constexpr int TC_BN = 128;  // key positions per tile (S MMA N, PV MMA K)
 constexpr float TC_RESCALE = 8.f;
 
 __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -138,6 +138,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_init_count(uint32_t bar, uint32_t count) {
@@ -184,9 +192,9 @@ struct TcCfg {
   static constexpr int KV_BYTES = TC_BN * D * 2;
   // sized as for D = 128 whatever D is: at most two CTAs per SM, so their 2 x 256 tensor-memory
   // columns always fit in the SM's 512
-  static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 128;
-  static constexpr uint32_t TMEM_COLS = 256;    // S ping: 64, S pong: 64 (P over its first 32), O: D
-  static constexpr uint32_t S_COL0 = 0, S_COL1 = 64, O_COL = 128;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 2 * TC_BN * 128 * 2 + 128;
+  static constexpr uint32_t TMEM_COLS = 256;    // S: 128 (P as fp16 over its first 64), O: D
+  static constexpr uint32_t S_COL = 0, O_COL = 128;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -195,21 +203,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Warp roles (7 warps):
-//   warps 0-3  softmax: thread t owns token row t = TMEM lane t.  For tile j it waits S(j), reads
-//              its row, masks it, updates its running max/sum, writes P(j) as fp16 over S(j)'s
-//              first 32 columns (rescaling its O row first when its max moved by > 2^8) and
-//              arrives on p_full.
-//   warp 4     MMA: one lane issues S(j) = Q K(j)^T into S buffer j%2 once tile j has landed and
-//              PV(j-2) (the last reader of that buffer) is done, then O += P(j-1) V(j-1) once
-//              P(j-1) is written.  S(j) thus runs on the tensor cores while the softmax warps work
-//              on tile j-1.
-//   warps 5, 6 loads: gather tile j's K (warp 5) or V (warp 6) rows through the table into slot
-//              j%2 (cp.async, 128-byte swizzle) once S(j-2) (for K) or PV(j-2) (for V) has
-//              released the slot, then signal k_full / v_full.
-// Hand-offs are mbarriers (per S buffer / stage, so no waiter can fall two phases behind); every
-// wait is bounded, and a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop, so
-// the others give up in turn and the CTA still reaches its final barrier.
+// Warp roles (7 warps); tile = 128 key positions, one buffer each for S (P over it), K and V:
+//   warps 0-3  softmax: thread t owns token row t = TMEM lane t.  For tile j it waits S(j), finds
+//              its row maximum (first pass over S in tensor memory), moves its running max (and
+//              rescales its O row) only when the tile raises it by more than 2^8, then writes
+//              P = 2^(S - m) as fp16 over S's first 64 columns (second pass) and arrives on p_full.
+//   warp 4     MMA: one lane issues S(j) = Q K(j)^T once K(j) has landed and PV(j-1), the last
+//              reader of the S buffer, is done; then O += P(j) V(j) once P(j) and V(j) are there.
+//              Completion of S(j) also implies that PV(j-1) has finished writing O.
+//   warps 5, 6 loads: gather tile j's K (warp 5) or V (warp 6) rows through the table into their
+//              buffer (cp.async, 128-byte swizzle) once S(j-1) (for K) or PV(j-1) (for V) has
+//              finished reading it, then signal k_full / v_full.
+// Two CTAs per SM interleave these chains on the tensor cores.  Every wait is bounded; a role
+// that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop, the others give up in turn,
+// and the CTA still reaches its final barrier.
 constexpr int TC_THREADS = 224;
 
 template <int D>
@@ -221,16 +228,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
   const uint32_t sq = base;
-  const uint32_t sk0 = sq + C::Q_BYTES, sv0 = sk0 + 2 * C::KV_BYTES;
-  // barriers: s_full[2], p_full[2], pv_done[2], k_full[2], v_full[2]
-  const uint32_t bars = sv0 + 2 * C::KV_BYTES;
-  auto s_full = [&](int b) { return bars + 8u * b; };
-  auto p_full = [&](int b) { return bars + 16u + 8u * b; };
-  auto pv_done = [&](int b) { return bars + 32u + 8u * b; };
-  auto k_full = [&](int b) { return bars + 48u + 8u * b; };
-  auto v_full = [&](int b) { return bars + 64u + 8u * b; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 80 - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 84 - base));
+  const uint32_t sk = sq + C::Q_BYTES, sv = sk + C::KV_BYTES;
+  const uint32_t bars = sv + C::KV_BYTES;
+  const uint32_t s_full = bars, p_full = bars + 8, pv_done = bars + 16, k_full = bars + 24, v_full = bars + 32;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 40 - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 44 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -260,13 +262,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
     tc_fence_before();
   }
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init_count(s_full(b), 1);
-      mbar_init_count(p_full(b), 128);
-      mbar_init_count(pv_done(b), 1);
-      mbar_init_count(k_full(b), 32);
-      mbar_init_count(v_full(b), 32);
-    }
+    mbar_init_count(s_full, 1);
+    mbar_init_count(p_full, 128);
+    mbar_init_count(pv_done, 1);
+    mbar_init_count(k_full, 32);
+    mbar_init_count(v_full, 32);
     *abort_flag = 0;
   }
   if (tid < TC_BM) {
@@ -281,8 +281,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_o = tmem + C::O_COL;
-  auto s_col = [&](int j) { return tmem + ((j & 1) ? C::S_COL1 : C::S_COL0); };
+  const uint32_t t_s = tmem + C::S_COL, t_o = tmem + C::O_COL;
   auto give_up = [&]() {
     if (!*abort_flag) record_error(PKV_DEV_WAIT_TIMEOUT);
     *abort_flag = 1;
@@ -293,19 +292,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
 
   if (warp >= 5) {
     // ---------------- loads: warp 5 gathers K tiles, warp 6 V tiles ----------------
-    // A K slot is free once the S MMA that read it is done; a V slot once its PV MMA is done.
     const bool is_k = warp == 5;
     const __half* pool = is_k ? p.k : p.v;
-    const uint32_t slot0 = is_k ? sk0 : sv0;
+    const uint32_t dst = is_k ? sk : sv;
     const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      if (j >= 2 && !mbar_wait(is_k ? s_full(st) : pv_done(st), ((j - 2) >> 1) & 1)) {
+      // the buffer is free once the MMA that read tile j-1 from it is done
+      if (j >= 1 && !mbar_wait(is_k ? s_full : pv_done, (j - 1) & 1)) {
         failed = true;
         break;
       }
       if (*abort_flag) break;
-      const uint32_t dst = slot0 + st * C::KV_BYTES;
 #pragma unroll
       for (int rr = 0; rr < TC_BN / 32; ++rr) {
         const int r = rr * 32 + lane;
@@ -321,7 +318,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
       }
       cp_async_wait_all();
       fence_proxy_async_smem();                    // cp.async writes -> tensor-core reads
-      mbar_arrive(is_k ? k_full(st) : v_full(st));
+      mbar_arrive(is_k ? k_full : v_full);
     }
     if (failed) give_up();
   } else if (warp == 4) {
@@ -329,49 +326,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
       constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
-      int s_done = 0, pv_issued = 0;
-      auto issue_pv = [&](int j) -> bool {         // O += P(j) V(j) once P(j) and V(j) are there
-        if (!mbar_wait(p_full(j & 1), (j >> 1) & 1) || !mbar_wait(v_full(j & 1), (j >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t vb = sv0 + (j & 1) * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < TC_BN / 16; ++kk) {
-          const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
-          umma_ts(t_o, s_col(j) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done(j & 1));
-        ++pv_issued;
-        return true;
-      };
-      for (int j = 0; j < n_tiles && !failed; ++j) {
+      int s_issued = 0, pv_issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
         if (*abort_flag) break;
-        // K(j) landed, and PV(j-2), the last reader of S buffer j%2, is done
-        if (!mbar_wait(k_full(j & 1), (j >> 1) & 1) ||
-            (j >= 2 && !mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))) {
+        // K(j) landed, and PV(j-1), the last reader of the S buffer, is done
+        if (!mbar_wait(k_full, j & 1) || (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1))) {
           failed = true;
           break;
         }
         tc_fence_after();
-        const uint32_t kb = sk0 + (j & 1) * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-          umma_ss(s_col(j), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint64_t b = umma_smem_desc(sk + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+          umma_ss(t_s, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_full(j & 1));
-        s_done = j + 1;
-        if (j >= 1 && !issue_pv(j - 1)) {
+        umma_commit(s_full);
+        ++s_issued;
+        // O += P(j) V(j)
+        if (!mbar_wait(p_full, j & 1) || !mbar_wait(v_full, j & 1)) {
           failed = true;
           break;
         }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TC_BN / 16; ++kk) {
+          const uint64_t b = umma_smem_desc(sv + kk * 16 * 128, TC_BN * 128, 1024);
+          umma_ts(t_o, t_s + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(pv_done);
+        ++pv_issued;
       }
-      if (!failed && !*abort_flag && !issue_pv(n_tiles - 1)) failed = true;
       if (failed || *abort_flag) {
         give_up();
         // let the tensor-core work this lane issued finish (bounded) before memory is released
-        if (s_done > 0) mbar_wait(s_full((s_done - 1) & 1), ((s_done - 1) >> 1) & 1);
-        if (pv_issued > 0) mbar_wait(pv_done((pv_issued - 1) & 1), ((pv_issued - 1) >> 1) & 1);
+        if (s_issued > 0) mbar_wait(s_full, (s_issued - 1) & 1);
+        if (pv_issued > 0) mbar_wait(pv_done, (pv_issued - 1) & 1);
       }
     }
     __syncwarp();
@@ -384,31 +374,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
     for (int j = 0; j < n_tiles; ++j) {
       // decisions stay warp-uniform: the tcgen05.ld/st below are warp-collective
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full(j & 1), (j >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1))) {
         failed = true;
         break;
       }
-      tc_fence_after();
-      const uint32_t ts = s_col(j);
-      float sv[TC_BN];
-      {
-        float a[32], b2[32];
-        tmem_ld32(ts + lane_off, a);
-        tmem_ld32(ts + lane_off + 32, b2);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sv[c] = a[c];
-          sv[32 + c] = b2[c];
-        }
-      }
+      tc_fence_after();                            // S(j) complete, and with it PV(j-1)
       const bool need_mask = (j + 1) * TC_BN - 1 > first_pos;
+      const int key0 = j * TC_BN;
+      // pass 1: the row maximum of the scaled, masked scores
       float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < TC_BN / 32; ++c) {
+        float x[32];
+        tmem_ld32(t_s + lane_off + c * 32, x);
 #pragma unroll
-      for (int c = 0; c < TC_BN; ++c) {
-        float x = sv[c] * p.scale_log2;
-        if (need_mask && j * TC_BN + c > pos) x = -INFINITY;
-        sv[c] = x;
-        mx = fmaxf(mx, x);
+        for (int e = 0; e < 32; ++e) {
+          const bool dead = need_mask && key0 + c * 32 + e > pos;
+          mx = fmaxf(mx, dead ? -INFINITY : x[e] * p.scale_log2);
+        }
       }
       const bool rescale = mx > m_ref + TC_RESCALE;   // also true for the first finite max
       float alpha = 1.f;
@@ -417,24 +400,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
         m_ref = mx;
       }
       const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum = 0.f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float e0 = fast_exp2(sv[2 * c] - ref), e1 = fast_exp2(sv[2 * c + 1] - ref);
-        sum += e0 + e1;
-        pk[c] = pack_half2(e0, e1);
-      }
-      l = l * alpha + sum;
-      // tcgen05.ld/st are warp-collective: if any row of the warp moved its max after the first
-      // tile, the whole warp rescales its O rows (alpha is 1 for the rows that did not move), once
-      // PV(j-1) has finished accumulating into them
+      // if any row of the warp moved its max after the first tile, the whole warp rescales its O
+      // rows (alpha is 1 for the rows that did not move)
       if (__any_sync(0xffffffffu, rescale && j > 0)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1))) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -445,13 +413,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
           tmem_st32(t_o + lane_off + c * 32, ob);
         }
       }
-      tmem_st32(ts + lane_off, pk);                    // P(j) over S(j)'s first 32 columns
+      // pass 2: P = 2^(S - m) as fp16, 32 scores -> 16 columns, written over scores already read
+      float sum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < TC_BN / 32; ++c) {
+        float x[32];
+        tmem_ld32(t_s + lane_off + c * 32, x);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k0 = key0 + c * 32 + 2 * e;
+          const float s0 = (need_mask && k0 > pos) ? -INFINITY : x[2 * e] * p.scale_log2;
+          const float s1 = (need_mask && k0 + 1 > pos) ? -INFINITY : x[2 * e + 1] * p.scale_log2;
+          const float e0 = fast_exp2(s0 - ref), e1 = fast_exp2(s1 - ref);
+          sum += e0 + e1;
+          pk[e] = pack_half2(e0, e1);
+        }
+        tmem_st16(t_s + lane_off + c * 16, pk);
+      }
+      l = l * alpha + sum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full(j & 1));
+      mbar_arrive(p_full);
     }
     if (!failed && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      failed = !__all_sync(0xffffffffu, mbar_wait(pv_done((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1));
+      failed = !__all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1));
       tc_fence_after();
     }
     if (failed) give_up();
