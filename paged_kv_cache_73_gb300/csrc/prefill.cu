@@ -66,9 +66,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 // ---- fifth-generation tensor cores (tcgen05): S, P and O live in tensor memory ---------------
 //
-// One CTA (4 warps, 128 threads) owns 128 new tokens of one (sequence, head); thread t owns
-// token row t, which is TMEM lane t.  Per key tile of 128 positions one thread issues
-// S = Q K^T (tcgen05.mma, M=128, N=128, fp16 in, fp32 in TMEM); every thread reads its row of S
+// A softmax thread owns one new-token row, which is one TMEM lane of its query tile.  Per key
+// tile of 128 positions one thread issues S = Q K^T (tcgen05.mma, M=128, N=128, fp16 in, fp32 in
+// TMEM); every softmax thread reads its row of S
 // (tcgen05.ld), masks it, updates its running max/sum and writes P = 2^(S - m) as fp16 back to
 // TMEM (tcgen05.st); one thread issues O += P V (A = P from TMEM, B = V from shared memory,
 // MN-major) into the TMEM accumulator.  MMA groups complete on mbarriers.
@@ -77,7 +77,7 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // Q, K and V tiles sit in shared memory in the canonical K-major / MN-major layouts with 128-byte
 // swizzle: rows of 64 elements (128 B), 16-byte chunks XOR-ed with the row's low three bits,
 // 8-row groups 1024 B apart, head-dimension halves in separate regions.
-constexpr int TC_BM = 128;  // new tokens per CTA (MMA M)
+constexpr int TC_BM = 128;  // new tokens per query tile (MMA M)
 constexpr int TC_BN = 128;  // key positions per tile (S MMA N, PV MMA K)
 constexpr float TC_RESCALE = 8.f;
 
@@ -188,13 +188,13 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk, int rows) {
 
 template <int D>
 struct TcCfg {
-  static constexpr int Q_BYTES = TC_BM * D * 2;
+  static constexpr int Q_BYTES = TC_BM * D * 2;          // one 128-token query tile
   static constexpr int KV_BYTES = TC_BN * D * 2;
-  // sized as for D = 128 whatever D is: at most two CTAs per SM, so their 2 x 256 tensor-memory
-  // columns always fit in the SM's 512
-  static constexpr int SMEM = 1024 /*alignment slack*/ + TC_BM * 128 * 2 + 2 * TC_BN * 128 * 2 + 128;
-  static constexpr uint32_t TMEM_COLS = 256;    // S: 128 (P as fp16 over its first 64), O: D
-  static constexpr uint32_t S_COL = 0, O_COL = 128;
+  // two query tiles + one K and one V buffer; sized as for D = 128 whatever D is so that one CTA
+  // (holding all 512 tensor-memory columns) runs per SM
+  static constexpr int SMEM = 1024 /*alignment slack*/ + 2 * TC_BM * 128 * 2 + 2 * TC_BN * 128 * 2 + 256;
+  static constexpr uint32_t TMEM_COLS = 512;             // per query tile: S 128 (P over it), O 128
+  static constexpr uint32_t TILE_COLS = 256, S_COL = 0, O_COL = 128;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -203,21 +203,26 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Warp roles (7 warps); tile = 128 key positions, one buffer each for S (P over it), K and V:
-//   warps 0-3  softmax: thread t owns token row t = TMEM lane t.  For tile j it waits S(j), finds
-//              its row maximum (first pass over S in tensor memory), moves its running max (and
-//              rescales its O row) only when the tile raises it by more than 2^8, then writes
-//              P = 2^(S - m) as fp16 over S's first 64 columns (second pass) and arrives on p_full.
-//   warp 4     MMA: one lane issues S(j) = Q K(j)^T once K(j) has landed and PV(j-1), the last
-//              reader of the S buffer, is done; then O += P(j) V(j) once P(j) and V(j) are there.
-//              Completion of S(j) also implies that PV(j-1) has finished writing O.
-//   warps 5, 6 loads: gather tile j's K (warp 5) or V (warp 6) rows through the table into their
-//              buffer (cp.async, 128-byte swizzle) once S(j-1) (for K) or PV(j-1) (for V) has
-//              finished reading it, then signal k_full / v_full.
-// Two CTAs per SM interleave these chains on the tensor cores.  Every wait is bounded; a role
-// that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop, the others give up in turn,
-// and the CTA still reaches its final barrier.
-constexpr int TC_THREADS = 224;
+// One CTA owns 256 new tokens of one (sequence, head) as two 128-token query tiles that share
+// every K/V tile it loads (half the gather traffic per flop of one tile per CTA).  Key tiles are
+// 128 positions; one buffer each for K and V, and per query tile one S buffer (P over it) and one
+// O accumulator in tensor memory.  Warp roles (11 warps):
+//   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread t of the group owns token row t = TMEM
+//              lane t of its tile's columns.  For key tile j it waits S(j), finds its row maximum
+//              (first pass over S), moves its running max (rescaling its O row) only when the
+//              tile raises it by more than 2^8, writes P = 2^(S - m) as fp16 over S's first 64
+//              columns (second pass) and arrives on its p_full.
+//   warp 8     MMA: one lane issues, per key tile j, S0(j) and S1(j) once K(j) has landed and the
+//              previous PV of that tile (the last reader of its S buffer) is done, then
+//              O0 += P0(j) V(j) and O1 += P1(j) V(j) as P0(j), P1(j) and V(j) arrive.  The
+//              completion of S(j) also implies that the tile's PV(j-1) has finished writing O.
+//   warps 9, 10 loads: gather key tile j's K (warp 9) or V (warp 10) rows through the table into
+//              their buffer (cp.async, 128-byte swizzle) once the MMAs of tile j-1 that read it
+//              are done, then signal k_full / v_full.
+// Every wait is bounded; a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop,
+// the others give up in turn, and the CTA still reaches its final barrier.
+constexpr int TC_QTILES = 2;
+constexpr int TC_THREADS = 352;
 
 template <int D>
 __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const PrefillParams p) {
@@ -227,12 +232,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
-  const uint32_t sq = base;
-  const uint32_t sk = sq + C::Q_BYTES, sv = sk + C::KV_BYTES;
+  const uint32_t sq = base;                                   // [2][128 rows][D], per-tile regions
+  const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + C::KV_BYTES;
   const uint32_t bars = sv + C::KV_BYTES;
-  const uint32_t s_full = bars, p_full = bars + 8, pv_done = bars + 16, k_full = bars + 24, v_full = bars + 32;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 40 - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 44 - base));
+  // per query tile g: s_full(g), p_full(g), pv_done(g); shared: k_full, v_full
+  auto s_full = [&](int g) { return bars + 8u * g; };
+  auto p_full = [&](int g) { return bars + 16u + 8u * g; };
+  auto pv_done = [&](int g) { return bars + 32u + 8u * g; };
+  const uint32_t k_full = bars + 48, v_full = bars + 56;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 64 - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 68 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -244,14 +253,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   const int ctx = p.lens[s];
   const int q0 = p.qstart[s];
   const int n = p.qstart[s + 1] - q0;
-  const int i0 = qt * TC_BM;
+  const int i0 = qt * TC_QTILES * TC_BM;
   if (n < 0 || n > ctx || ctx > p.max_blocks * B || q0 < 0 || q0 + n > p.total_q) {
     if (tid == 0 && qt == 0) record_error(ctx > p.max_blocks * B ? PKV_DEV_BAD_CONTEXT_LEN : PKV_DEV_BAD_QUERY_RANGE);
     return;
   }
   if (i0 >= n) return;
+  const int ntile_q = i0 + TC_BM < n ? 2 : 1;                 // query tiles with real tokens
   const int first_pos = ctx - n + i0;
-  const int last_pos = ctx - n + min(i0 + TC_BM, n) - 1;
+  const int last_pos = ctx - n + min(i0 + TC_QTILES * TC_BM, n) - 1;
   const int n_tiles = last_pos / TC_BN + 1;
 
   if (warp == 0) {
@@ -262,26 +272,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
     tc_fence_before();
   }
   if (tid == 0) {
-    mbar_init_count(s_full, 1);
-    mbar_init_count(p_full, 128);
-    mbar_init_count(pv_done, 1);
+    for (int g = 0; g < TC_QTILES; ++g) {
+      mbar_init_count(s_full(g), 1);
+      mbar_init_count(p_full(g), 128);
+      mbar_init_count(pv_done(g), 1);
+    }
     mbar_init_count(k_full, 32);
     mbar_init_count(v_full, 32);
     *abort_flag = 0;
   }
-  if (tid < TC_BM) {
-    // Q tile: softmax thread t copies token row t (rows past the new tokens are zero)
+  if (tid < TC_QTILES * TC_BM) {
+    // Q tiles: softmax thread t copies token row t (rows past the new tokens are zero)
+    const int g = tid >> 7, r = tid & 127;
     const int i = i0 + tid;
     const __half* src = p.q + (static_cast<size_t>(q0 + min(i, n - 1)) * H + h) * D;
+    const uint32_t dst = sq + g * C::Q_BYTES;
 #pragma unroll
-    for (int c = 0; c < CPR; ++c) cp_async16(sq + sw128(tid, c, TC_BM), src + c * 8, i < n ? 16 : 0);
+    for (int c = 0; c < CPR; ++c) cp_async16(dst + sw128(r, c, TC_BM), src + c * 8, i < n ? 16 : 0);
     cp_async_wait_all();
     fence_proxy_async_smem();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem + C::S_COL, t_o = tmem + C::O_COL;
+  auto t_s = [&](int g) { return tmem + g * C::TILE_COLS + C::S_COL; };
+  auto t_o = [&](int g) { return tmem + g * C::TILE_COLS + C::O_COL; };
   auto give_up = [&]() {
     if (!*abort_flag) record_error(PKV_DEV_WAIT_TIMEOUT);
     *abort_flag = 1;
@@ -290,15 +305,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   bool failed = false;
   float l = 0.f;
 
-  if (warp >= 5) {
-    // ---------------- loads: warp 5 gathers K tiles, warp 6 V tiles ----------------
-    const bool is_k = warp == 5;
+  if (warp >= 9) {
+    // ---------------- loads: warp 9 gathers K tiles, warp 10 V tiles ----------------
+    const bool is_k = warp == 9;
     const __half* pool = is_k ? p.k : p.v;
     const uint32_t dst = is_k ? sk : sv;
+    // the buffer is free once the last MMA that read tile j-1 from it is done: the S (for K) or
+    // PV (for V) of the last query tile with tokens, which completes after the other tile's
+    const uint32_t freed = is_k ? s_full(ntile_q - 1) : pv_done(ntile_q - 1);
     const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
     for (int j = 0; j < n_tiles; ++j) {
-      // the buffer is free once the MMA that read tile j-1 from it is done
-      if (j >= 1 && !mbar_wait(is_k ? s_full : pv_done, (j - 1) & 1)) {
+      if (j >= 1 && !mbar_wait(freed, (j - 1) & 1)) {
         failed = true;
         break;
       }
@@ -321,72 +338,91 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
       mbar_arrive(is_k ? k_full : v_full);
     }
     if (failed) give_up();
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ---------------- MMA issue (one lane) ----------------
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
       constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
-      int s_issued = 0, pv_issued = 0;
+      int s_issued = 0, pv_issued = 0;             // per query tile, the same for both
       for (int j = 0; j < n_tiles; ++j) {
         if (*abort_flag) break;
-        // K(j) landed, and PV(j-1), the last reader of the S buffer, is done
-        if (!mbar_wait(k_full, j & 1) || (j >= 1 && !mbar_wait(pv_done, (j - 1) & 1))) {
+        if (!mbar_wait(k_full, j & 1)) {
           failed = true;
           break;
         }
-        tc_fence_after();
+        for (int g = 0; g < ntile_q; ++g) {
+          // PV_g(j-1), the last reader of S buffer g, is done
+          if (j >= 1 && !mbar_wait(pv_done(g), (j - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qb = sq + g * C::Q_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = umma_smem_desc(sq + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = umma_smem_desc(sk + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-          umma_ss(t_s, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = umma_smem_desc(qb + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = umma_smem_desc(sk + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+            umma_ss(t_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(g));
         }
-        umma_commit(s_full);
+        if (failed) break;
         ++s_issued;
-        // O += P(j) V(j)
-        if (!mbar_wait(p_full, j & 1) || !mbar_wait(v_full, j & 1)) {
+        if (!mbar_wait(v_full, j & 1)) {
           failed = true;
           break;
         }
-        tc_fence_after();
+        for (int g = 0; g < ntile_q; ++g) {
+          if (!mbar_wait(p_full(g), j & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < TC_BN / 16; ++kk) {
-          const uint64_t b = umma_smem_desc(sv + kk * 16 * 128, TC_BN * 128, 1024);
-          umma_ts(t_o, t_s + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < TC_BN / 16; ++kk) {
+            const uint64_t b = umma_smem_desc(sv + kk * 16 * 128, TC_BN * 128, 1024);
+            umma_ts(t_o(g), t_s(g) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(pv_done(g));
         }
-        umma_commit(pv_done);
+        if (failed) break;
         ++pv_issued;
       }
       if (failed || *abort_flag) {
         give_up();
         // let the tensor-core work this lane issued finish (bounded) before memory is released
-        if (s_issued > 0) mbar_wait(s_full, (s_issued - 1) & 1);
-        if (pv_issued > 0) mbar_wait(pv_done, (pv_issued - 1) & 1);
+        for (int g = 0; g < ntile_q; ++g) {
+          if (s_issued > 0) mbar_wait(s_full(g), (s_issued - 1) & 1);
+          if (pv_issued > 0) mbar_wait(pv_done(g), (pv_issued - 1) & 1);
+        }
       }
     }
     __syncwarp();
-  } else {
-    // ---------------- softmax (warps 0-3) ----------------
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int row_i = i0 + tid;
+  } else if (warp < 4 * ntile_q) {
+    // ---------------- softmax (warps 0-3: query tile 0, warps 4-7: query tile 1) ----------------
+    const int g = warp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = t_s(g), to = t_o(g);
+    const int row_i = i0 + tid;                        // tid = g * 128 + row within the tile
     const int pos = ctx - n + row_i;
+    const int tile_first = first_pos + g * TC_BM;      // position of the tile's first token
     float m_ref = -INFINITY;
     for (int j = 0; j < n_tiles; ++j) {
       // decisions stay warp-uniform: the tcgen05.ld/st below are warp-collective
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full(g), j & 1))) {
         failed = true;
         break;
       }
-      tc_fence_after();                            // S(j) complete, and with it PV(j-1)
-      const bool need_mask = (j + 1) * TC_BN - 1 > first_pos;
+      tc_fence_after();                                // S(j) complete, and with it PV(j-1)
+      const bool need_mask = (j + 1) * TC_BN - 1 > tile_first;
       const int key0 = j * TC_BN;
       // pass 1: the row maximum of the scaled, masked scores
       float mx = -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < TC_BN / 32; ++c) {
         float x[32];
-        tmem_ld32(t_s + lane_off + c * 32, x);
+        tmem_ld32(ts + lane_off + c * 32, x);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const bool dead = need_mask && key0 + c * 32 + e > pos;
@@ -406,11 +442,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
-          tmem_ld32(t_o + lane_off + c * 32, o);
+          tmem_ld32(to + lane_off + c * 32, o);
           uint32_t ob[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) ob[e] = __float_as_uint(o[e] * alpha);
-          tmem_st32(t_o + lane_off + c * 32, ob);
+          tmem_st32(to + lane_off + c * 32, ob);
         }
       }
       // pass 2: P = 2^(S - m) as fp16, 32 scores -> 16 columns, written over scores already read
@@ -418,7 +454,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
 #pragma unroll 1
       for (int c = 0; c < TC_BN / 32; ++c) {
         float x[32];
-        tmem_ld32(t_s + lane_off + c * 32, x);
+        tmem_ld32(ts + lane_off + c * 32, x);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -429,15 +465,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
           sum += e0 + e1;
           pk[e] = pack_half2(e0, e1);
         }
-        tmem_st16(t_s + lane_off + c * 16, pk);
+        tmem_st16(ts + lane_off + c * 16, pk);
       }
       l = l * alpha + sum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full(g));
     }
     if (!failed && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      failed = !__all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1));
+      failed = !__all_sync(0xffffffffu, mbar_wait(pv_done(g), (n_tiles - 1) & 1));
       tc_fence_after();
     }
     if (failed) give_up();
@@ -446,16 +482,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   // ---------------- epilogue (all warps) ----------------
   bad = __syncthreads_or(bad);
   const bool aborted = *abort_flag != 0;
-  if (warp < 4 && !aborted && !bad) {
+  if (warp < 4 * ntile_q && !aborted && !bad) {
     // every lane loads (warp-collective); only rows that are real new tokens are stored
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = warp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int row_i = i0 + tid;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     __half* dst = p.out + (static_cast<size_t>(q0 + min(row_i, n - 1)) * H + h) * D;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       float o[32];
-      tmem_ld32(t_o + lane_off + c * 32, o);
+      tmem_ld32(t_o(g) + lane_off + c * 32, o);
       if (row_i >= n) continue;
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
@@ -494,7 +531,7 @@ int launch_prefill(const PrefillParams& p, int num_seqs, int max_query_len, cuda
     }
   }
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill setup: %s", cudaGetErrorString(e));
-  dim3 grid((max_query_len + TC_BM - 1) / TC_BM, p.num_heads, num_seqs);
+  dim3 grid((max_query_len + TC_QTILES * TC_BM - 1) / (TC_QTILES * TC_BM), p.num_heads, num_seqs);
   e = pkv::launch_pdl(paged_prefill_tc_kernel<D>, grid, dim3(TC_THREADS), TcCfg<D>::SMEM, st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill launch: %s", cudaGetErrorString(e));
