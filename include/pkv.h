@@ -142,8 +142,8 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
  *   max_query_len host: the largest n_s (sizes the grid; larger n_s are not
  *                 fully processed)
  *   pools, tables, context_lens as for pkv_paged_attention_decode.
- * A sequence with n_s = 0 is skipped; n_s > ctx_s or rows outside q record
- * PKV_DEV_BAD_QUERY_RANGE.  No workspace.
+ * scale must be positive.  A sequence with n_s = 0 is skipped; n_s > ctx_s or
+ * rows outside q record PKV_DEV_BAD_QUERY_RANGE.  No workspace.
  * ------------------------------------------------------------------------- */
 int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                                 const int32_t* block_tables, const int32_t* context_lens,

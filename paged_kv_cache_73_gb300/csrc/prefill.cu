@@ -128,6 +128,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// The same load without its wait: the values are valid only after tmem_ld_wait().
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float (&v)[32]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -136,14 +150,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -192,7 +198,7 @@ struct TcCfg {
   static constexpr int KV_BYTES = TC_BN * D * 2;
   // two query tiles + one K and one V buffer; sized as for D = 128 whatever D is so that one CTA
   // (holding all 512 tensor-memory columns) runs per SM
-  static constexpr int SMEM = 1024 /*alignment slack*/ + 2 * TC_BM * 128 * 2 + 2 * TC_BN * 128 * 2 + 256;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + 2 * TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 256;
   static constexpr uint32_t TMEM_COLS = 512;             // per query tile: S 128 (P over it), O 128
   static constexpr uint32_t TILE_COLS = 256, S_COL = 0, O_COL = 128;
 };
@@ -205,8 +211,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // One CTA owns 256 new tokens of one (sequence, head) as two 128-token query tiles that share
 // every K/V tile it loads (half the gather traffic per flop of one tile per CTA).  Key tiles are
-// 128 positions; one buffer each for K and V, and per query tile one S buffer (P over it) and one
-// O accumulator in tensor memory.  Warp roles (11 warps):
+// 128 positions; two slots each for K and V (tile j in slot j%2, loaded while tile j-1 is in
+// use), and per query tile one S buffer (P over it) and one O accumulator in tensor memory.  Warp roles (11 warps):
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread t of the group owns token row t = TMEM
 //              lane t of its tile's columns.  For key tile j it waits S(j), finds its row maximum
 //              (first pass over S), moves its running max (rescaling its O row) only when the
@@ -217,8 +223,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
 //              O0 += P0(j) V(j) and O1 += P1(j) V(j) as P0(j), P1(j) and V(j) arrive.  The
 //              completion of S(j) also implies that the tile's PV(j-1) has finished writing O.
 //   warps 9, 10 loads: gather key tile j's K (warp 9) or V (warp 10) rows through the table into
-//              their buffer (cp.async, 128-byte swizzle) once the MMAs of tile j-1 that read it
-//              are done, then signal k_full / v_full.
+//              slot j%2 (cp.async, 128-byte swizzle) once the MMAs of tile j-2 that read the slot
+//              are done (k_free / v_free, committed by the MMA lane), then signal k_full / v_full.
+//              Per-slot barriers keep every waiter within one phase of the barrier.
 // Every wait is bounded; a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop,
 // the others give up in turn, and the CTA still reaches its final barrier.
 constexpr int TC_QTILES = 2;
@@ -233,15 +240,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
   const uint32_t sq = base;                                   // [2][128 rows][D], per-tile regions
-  const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + C::KV_BYTES;
-  const uint32_t bars = sv + C::KV_BYTES;
-  // per query tile g: s_full(g), p_full(g), pv_done(g); shared: k_full, v_full
+  const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + 2 * C::KV_BYTES;   // two slots each
+  const uint32_t bars = sv + 2 * C::KV_BYTES;
+  // per query tile g: s_full(g), p_full(g), pv_done(g); per K/V slot b: k_full, v_full (data
+  // landed) and k_free, v_free (the MMAs that read the slot are done)
   auto s_full = [&](int g) { return bars + 8u * g; };
   auto p_full = [&](int g) { return bars + 16u + 8u * g; };
   auto pv_done = [&](int g) { return bars + 32u + 8u * g; };
-  const uint32_t k_full = bars + 48, v_full = bars + 56;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 64 - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 68 - base));
+  auto k_full = [&](int b) { return bars + 48u + 8u * b; };
+  auto v_full = [&](int b) { return bars + 64u + 8u * b; };
+  auto k_free = [&](int b) { return bars + 80u + 8u * b; };
+  auto v_free = [&](int b) { return bars + 96u + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 112 - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 116 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -277,8 +288,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
       mbar_init_count(p_full(g), 128);
       mbar_init_count(pv_done(g), 1);
     }
-    mbar_init_count(k_full, 32);
-    mbar_init_count(v_full, 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init_count(k_full(b), 32);
+      mbar_init_count(v_full(b), 32);
+      mbar_init_count(k_free(b), 1);
+      mbar_init_count(v_free(b), 1);
+    }
     *abort_flag = 0;
   }
   if (tid < TC_QTILES * TC_BM) {
@@ -309,13 +324,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
     // ---------------- loads: warp 9 gathers K tiles, warp 10 V tiles ----------------
     const bool is_k = warp == 9;
     const __half* pool = is_k ? p.k : p.v;
-    const uint32_t dst = is_k ? sk : sv;
-    // the buffer is free once the last MMA that read tile j-1 from it is done: the S (for K) or
-    // PV (for V) of the last query tile with tokens, which completes after the other tile's
-    const uint32_t freed = is_k ? s_full(ntile_q - 1) : pv_done(ntile_q - 1);
     const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
     for (int j = 0; j < n_tiles; ++j) {
-      if (j >= 1 && !mbar_wait(freed, (j - 1) & 1)) {
+      const int st = j & 1;
+      const uint32_t dst = (is_k ? sk : sv) + st * C::KV_BYTES;
+      // slot j%2 is free once the MMAs of tile j-2 that read it are done
+      if (j >= 2 && !mbar_wait(is_k ? k_free(st) : v_free(st), ((j - 2) >> 1) & 1)) {
         failed = true;
         break;
       }
@@ -335,65 +349,87 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
       }
       cp_async_wait_all();
       fence_proxy_async_smem();                    // cp.async writes -> tensor-core reads
-      mbar_arrive(is_k ? k_full : v_full);
+      mbar_arrive(is_k ? k_full(st) : v_full(st));
     }
     if (failed) give_up();
   } else if (warp == 8) {
     // ---------------- MMA issue (one lane) ----------------
+    // Ping-pong order per key tile j: S0(j), PV1(j-1), S1(j), PV0(j).  While softmax 0 works on
+    // S0(j) the tensor cores run PV1(j-1) and S1(j), and while softmax 1 works on S1(j) they run
+    // PV0(j) and S0(j+1); with one query tile the order is S0(j), PV0(j).
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
       constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
-      int s_issued = 0, pv_issued = 0;             // per query tile, the same for both
-      for (int j = 0; j < n_tiles; ++j) {
+      int s_issued[TC_QTILES] = {0, 0}, pv_issued[TC_QTILES] = {0, 0};
+      // S_g(j) = Q_g K(j)^T, once PV_g(j-1), the last reader of S buffer g, is done
+      auto issue_s = [&](int g, int j) -> bool {
+        if (j >= 1 && !mbar_wait(pv_done(g), (j - 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t qb = sq + g * C::Q_BYTES;
+        const uint32_t kb = sk + (j & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = umma_smem_desc(qb + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+          umma_ss(t_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full(g));
+        ++s_issued[g];
+        return true;
+      };
+      // O_g += P_g(j) V(j), once softmax g has written P_g(j) (V(j) has landed: checked by the caller)
+      auto issue_pv = [&](int g, int j) -> bool {
+        if (!mbar_wait(p_full(g), j & 1)) return false;
+        tc_fence_after();
+        const uint32_t vb = sv + (j & 1) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < TC_BN / 16; ++kk) {
+          const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
+          umma_ts(t_o(g), t_s(g) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(pv_done(g));
+        ++pv_issued[g];
+        return true;
+      };
+      const bool two = ntile_q == 2;
+      for (int j = 0; j < n_tiles && !failed; ++j) {
         if (*abort_flag) break;
-        if (!mbar_wait(k_full, j & 1)) {
+        if (!mbar_wait(k_full(j & 1), (j >> 1) & 1) || !issue_s(0, j)) {
           failed = true;
           break;
         }
-        for (int g = 0; g < ntile_q; ++g) {
-          // PV_g(j-1), the last reader of S buffer g, is done
-          if (j >= 1 && !mbar_wait(pv_done(g), (j - 1) & 1)) {
+        if (two) {
+          if (j >= 1) {
+            if (!issue_pv(1, j - 1)) {              // V(j-1) landed before PV0(j-1) was issued
+              failed = true;
+              break;
+            }
+            umma_commit(v_free((j - 1) & 1));       // both PVs of tile j-1 issued
+          }
+          if (!issue_s(1, j)) {
             failed = true;
             break;
           }
-          tc_fence_after();
-          const uint32_t qb = sq + g * C::Q_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = umma_smem_desc(qb + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = umma_smem_desc(sk + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-            umma_ss(t_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full(g));
         }
-        if (failed) break;
-        ++s_issued;
-        if (!mbar_wait(v_full, j & 1)) {
+        umma_commit(k_free(j & 1));                // every S of tile j issued
+        if (!mbar_wait(v_full(j & 1), (j >> 1) & 1) || !issue_pv(0, j)) {
           failed = true;
           break;
         }
-        for (int g = 0; g < ntile_q; ++g) {
-          if (!mbar_wait(p_full(g), j & 1)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < TC_BN / 16; ++kk) {
-            const uint64_t b = umma_smem_desc(sv + kk * 16 * 128, TC_BN * 128, 1024);
-            umma_ts(t_o(g), t_s(g) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(pv_done(g));
-        }
-        if (failed) break;
-        ++pv_issued;
+        if (!two) umma_commit(v_free(j & 1));
+      }
+      if (!failed && !*abort_flag && two) {
+        if (issue_pv(1, n_tiles - 1))
+          umma_commit(v_free((n_tiles - 1) & 1));
+        else
+          failed = true;
       }
       if (failed || *abort_flag) {
         give_up();
         // let the tensor-core work this lane issued finish (bounded) before memory is released
         for (int g = 0; g < ntile_q; ++g) {
-          if (s_issued > 0) mbar_wait(s_full(g), (s_issued - 1) & 1);
-          if (pv_issued > 0) mbar_wait(pv_done(g), (pv_issued - 1) & 1);
+          if (s_issued[g] > 0) mbar_wait(s_full(g), (s_issued[g] - 1) & 1);
+          if (pv_issued[g] > 0) mbar_wait(pv_done(g), (pv_issued[g] - 1) & 1);
         }
       }
     }
@@ -417,18 +453,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
       tc_fence_after();                                // S(j) complete, and with it PV(j-1)
       const bool need_mask = (j + 1) * TC_BN - 1 > tile_first;
       const int key0 = j * TC_BN;
-      // pass 1: the row maximum of the scaled, masked scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < TC_BN / 32; ++c) {
-        float x[32];
-        tmem_ld32(ts + lane_off + c * 32, x);
+      // this thread's row of S in registers: four 32-column loads, one wait
+      float sv[TC_BN];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const bool dead = need_mask && key0 + c * 32 + e > pos;
-          mx = fmaxf(mx, dead ? -INFINITY : x[e] * p.scale_log2);
-        }
+      for (int c = 0; c < TC_BN / 32; ++c)
+        tmem_ld32_nowait(ts + lane_off + c * 32, *reinterpret_cast<float(*)[32]>(sv + c * 32));
+      tmem_ld_wait();
+      if (need_mask) {                                 // the diagonal tiles: keys after the token
+#pragma unroll
+        for (int c = 0; c < TC_BN; ++c)
+          if (key0 + c > pos) sv[c] = -INFINITY;
       }
+      // scale > 0, so the maximum of the scaled scores is the scaled maximum
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < TC_BN; ++c) mx = fmaxf(mx, sv[c]);
+      mx *= p.scale_log2;
       const bool rescale = mx > m_ref + TC_RESCALE;   // also true for the first finite max
       float alpha = 1.f;
       if (rescale) {
@@ -449,23 +489,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
           tmem_st32(to + lane_off + c * 32, ob);
         }
       }
-      // pass 2: P = 2^(S - m) as fp16, 32 scores -> 16 columns, written over scores already read
+      // P = 2^(scale*S - m) as fp16, one FMA and one ex2 per score; 128 scores -> 64 columns
+      // written over the scores already read
       float sum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < TC_BN / 32; ++c) {
-        float x[32];
-        tmem_ld32(ts + lane_off + c * 32, x);
-        uint32_t pk[16];
+      const float nref = -ref;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int k0 = key0 + c * 32 + 2 * e;
-          const float s0 = (need_mask && k0 > pos) ? -INFINITY : x[2 * e] * p.scale_log2;
-          const float s1 = (need_mask && k0 + 1 > pos) ? -INFINITY : x[2 * e + 1] * p.scale_log2;
-          const float e0 = fast_exp2(s0 - ref), e1 = fast_exp2(s1 - ref);
+      for (int c = 0; c < TC_BN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float e0 = fast_exp2(fmaf(sv[c * 64 + 2 * e], p.scale_log2, nref));
+          const float e1 = fast_exp2(fmaf(sv[c * 64 + 2 * e + 1], p.scale_log2, nref));
           sum += e0 + e1;
           pk[e] = pack_half2(e0, e1);
         }
-        tmem_st16(ts + lane_off + c * 16, pk);
+        tmem_st32(ts + lane_off + c * 32, pk);
       }
       l = l * alpha + sum;
       tmem_st_wait();
@@ -586,7 +624,8 @@ int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, cons
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: null pointer");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: q, caches and out must be 16-byte aligned");
-  if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: scale not finite");
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: scale must be finite and positive");
   PrefillParams p{};
   p.q = reinterpret_cast<const __half*>(q);
   p.k = reinterpret_cast<const __half*>(k_cache);
