@@ -13,10 +13,11 @@
 // (tcgen05.mma, fp16 inputs, fp32 accumulation in tensor memory); see the
 // kernel's comment below.  Key tiles of 64 positions are gathered block by
 // block through the table with 16-byte cp.async copies into the 128-byte
-// swizzled layout the tensor cores read, double-buffered.  P is rounded to
+// swizzled layout the tensor cores read, through a four-slot ring.  P is rounded to
 // fp16 for the second product, as flash attention does.  Key rows past the
 // context are zero-filled (never read), so stale NaN/Inf in unfilled slots
 // cannot reach a product.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched through the runtime
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -34,6 +35,10 @@ __device__ __forceinline__ void record_error(int code) { atomicCAS(&g_dev_error_
 
 
 struct PrefillParams {
+  // K and V pools as 3-D tensors (D, H*B, num_blocks), boxes of 64 x B x 1 with 128-byte swizzle
+  // (encoded only when use_tma is set)
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
   const __half* q;
   const __half* k;
   const __half* v;
@@ -46,6 +51,7 @@ struct PrefillParams {
   int max_blocks;
   int log2_block;
   int total_q;
+  int use_tma;
   float scale_log2;
 };
 
@@ -67,18 +73,18 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 // ---- fifth-generation tensor cores (tcgen05): S, P and O live in tensor memory ---------------
 //
 // A softmax thread owns one new-token row, which is one TMEM lane of its query tile.  Per key
-// tile of 128 positions one thread issues S = Q K^T (tcgen05.mma, M=128, N=128, fp16 in, fp32 in
+// tile of 64 positions one thread issues S = Q K^T (tcgen05.mma, M=128, N=64, fp16 in, fp32 in
 // TMEM); every softmax thread reads its row of S
-// (tcgen05.ld), masks it, updates its running max/sum and writes P = 2^(S - m) as fp16 back to
-// TMEM (tcgen05.st); one thread issues O += P V (A = P from TMEM, B = V from shared memory,
-// MN-major) into the TMEM accumulator.  MMA groups complete on mbarriers.
+// (tcgen05.ld), masks it, updates its running max/sum and writes P = 2^(S - m) as fp16 to its
+// own TMEM columns (tcgen05.st); one thread issues O += P V (A = P from TMEM, B = V from shared
+// memory, MN-major) into the TMEM accumulator.  MMA groups complete on mbarriers.
 // The running max m of a row is only moved (and O rescaled) when a tile raises it by more than
 // 2^8, so P stays within fp16 range while most tiles skip the O read-modify-write.
 // Q, K and V tiles sit in shared memory in the canonical K-major / MN-major layouts with 128-byte
 // swizzle: rows of 64 elements (128 B), 16-byte chunks XOR-ed with the row's low three bits,
 // 8-row groups 1024 B apart, head-dimension halves in separate regions.
 constexpr int TC_BM = 128;  // new tokens per query tile (MMA M)
-constexpr int TC_BN = 128;  // key positions per tile (S MMA N, PV MMA K)
+constexpr int TC_BN = 64;   // key positions per tile (S MMA N, PV MMA K)
 constexpr float TC_RESCALE = 8.f;
 
 __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -161,6 +167,20 @@ __device__ __forceinline__ void mbar_init_count(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Adds `bytes` to the transaction count the barrier's current phase waits for (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// TMA tile load of the box at (x, y, z) of a 3-D tensor map into shared memory; completion is
+// counted in bytes on `bar`.  Coordinates outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait_parity(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -195,12 +215,15 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk, int rows) {
 template <int D>
 struct TcCfg {
   static constexpr int Q_BYTES = TC_BM * D * 2;          // one 128-token query tile
-  static constexpr int KV_BYTES = TC_BN * D * 2;
-  // two query tiles + one K and one V buffer; sized as for D = 128 whatever D is so that one CTA
+  static constexpr int KV_BYTES = TC_BN * D * 2;         // one 64-position key or value tile
+  static constexpr int STAGES = 4;                       // ring slots each for K and for V
+  // two query tiles + the K and V rings; sized as for D = 128 whatever D is so that one CTA
   // (holding all 512 tensor-memory columns) runs per SM
-  static constexpr int SMEM = 1024 /*alignment slack*/ + 2 * TC_BM * 128 * 2 + 4 * TC_BN * 128 * 2 + 256;
-  static constexpr uint32_t TMEM_COLS = 512;             // per query tile: S 128 (P over it), O 128
-  static constexpr uint32_t TILE_COLS = 256, S_COL = 0, O_COL = 128;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + 2 * TC_BM * 128 * 2 + 2 * STAGES * TC_BN * 128 * 2 + 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // tensor-memory columns of query tile g: O at 128 g (D used), S at 256 + 64 g, P (fp16 pairs)
+  // at 384 + 32 g
+  static constexpr uint32_t O_COL = 0, S_COL = 256, P_COL = 384;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -210,49 +233,54 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // One CTA owns 256 new tokens of one (sequence, head) as two 128-token query tiles that share
-// every K/V tile it loads (half the gather traffic per flop of one tile per CTA).  Key tiles are
-// 128 positions; two slots each for K and V (tile j in slot j%2, loaded while tile j-1 is in
-// use), and per query tile one S buffer (P over it) and one O accumulator in tensor memory.  Warp roles (11 warps):
+// every K/V tile it loads.  Key tiles are 64 positions.  Per query tile g tensor memory holds
+// S_g, a separate P_g and the O_g accumulator, so S_g(j+1) is computed while softmax g is still
+// turning S_g(j) into P_g(j).  Warp roles (12 warps):
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread t of the group owns token row t = TMEM
-//              lane t of its tile's columns.  For key tile j it waits S(j), finds its row maximum
-//              (first pass over S), moves its running max (rescaling its O row) only when the
-//              tile raises it by more than 2^8, writes P = 2^(S - m) as fp16 over S's first 64
-//              columns (second pass) and arrives on its p_full.
-//   warp 8     MMA: one lane issues, per key tile j, S0(j) and S1(j) once K(j) has landed and the
-//              previous PV of that tile (the last reader of its S buffer) is done, then
-//              O0 += P0(j) V(j) and O1 += P1(j) V(j) as P0(j), P1(j) and V(j) arrive.  The
-//              completion of S(j) also implies that the tile's PV(j-1) has finished writing O.
-//   warps 9, 10 loads: gather key tile j's K (warp 9) or V (warp 10) rows through the table into
-//              slot j%2 (cp.async, 128-byte swizzle) once the MMAs of tile j-2 that read the slot
-//              are done (k_free / v_free, committed by the MMA lane), then signal k_full / v_full.
-//              Per-slot barriers keep every waiter within one phase of the barrier.
+//              lane t.  For key tile j it waits S_g(j), copies its row to registers and releases
+//              the S buffer (s_free), masks and takes the row maximum, moves its running max
+//              (rescaling its O row) only when the tile raises it by more than 2^8, waits for
+//              PV_g(j-1) (the last reader of P_g and writer of O_g), writes P = 2^(S - m) as fp16
+//              and arrives on p_full.
+//   warp 8     one lane issues S_0(j) and S_1(j) once K(j) has landed and softmax g has released
+//              S_g(j-1).
+//   warp 11    one lane issues O_g += P_g(j) V(j) once V(j) and P_g(j) are there.  Two issuing
+//              threads keep the tensor cores fed while either one waits on a barrier.
+//   warps 9, 10 loads: gather key tile j's K (warp 9) or V (warp 10) through the table into ring
+//              slot j%4 once the MMAs of tile j-4 that read the slot are done (k_free / v_free).
+//              Whole blocks come by TMA (one box per block and head-dimension half, landing in
+//              the 128-byte swizzle); the rest by cp.async.  k_full / v_full complete when every
+//              lane has arrived and the TMA bytes have landed.
+// Per-slot and per-tile barriers keep every waiter within one phase of the barrier it waits on.
 // Every wait is bounded; a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop,
 // the others give up in turn, and the CTA still reaches its final barrier.
 constexpr int TC_QTILES = 2;
-constexpr int TC_THREADS = 352;
+constexpr int TC_THREADS = 384;
 
 template <int D>
-__global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using C = TcCfg<D>;
-  constexpr int CPR = D / 8;
+  constexpr int CPR = D / 8;                                  // 16-byte chunks per row
+  constexpr int NS = C::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
   const uint32_t sq = base;                                   // [2][128 rows][D], per-tile regions
-  const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + 2 * C::KV_BYTES;   // two slots each
-  const uint32_t bars = sv + 2 * C::KV_BYTES;
-  // per query tile g: s_full(g), p_full(g), pv_done(g); per K/V slot b: k_full, v_full (data
-  // landed) and k_free, v_free (the MMAs that read the slot are done)
+  const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + NS * C::KV_BYTES;
+  const uint32_t bars = sv + NS * C::KV_BYTES;
+  // per query tile g: s_full (S_g landed), s_free (S_g read out), p_full (P_g written), pv_done;
+  // per ring slot b: k_full / v_full (data landed), k_free / v_free (the MMAs reading it are done)
   auto s_full = [&](int g) { return bars + 8u * g; };
-  auto p_full = [&](int g) { return bars + 16u + 8u * g; };
-  auto pv_done = [&](int g) { return bars + 32u + 8u * g; };
-  auto k_full = [&](int b) { return bars + 48u + 8u * b; };
-  auto v_full = [&](int b) { return bars + 64u + 8u * b; };
-  auto k_free = [&](int b) { return bars + 80u + 8u * b; };
-  auto v_free = [&](int b) { return bars + 96u + 8u * b; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 112 - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 116 - base));
+  auto s_free = [&](int g) { return bars + 16u + 8u * g; };
+  auto p_full = [&](int g) { return bars + 32u + 8u * g; };
+  auto pv_done = [&](int g) { return bars + 48u + 8u * g; };
+  auto k_full = [&](int b) { return bars + 64u + 8u * b; };
+  auto v_full = [&](int b) { return bars + 96u + 8u * b; };
+  auto k_free = [&](int b) { return bars + 128u + 8u * b; };
+  auto v_free = [&](int b) { return bars + 160u + 8u * b; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 192 - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 196 - base));
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -260,7 +288,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.num_heads;
-  const int B = 1 << p.log2_block;
+  const int lb = p.log2_block;
+  const int B = 1 << lb;
   const int ctx = p.lens[s];
   const int q0 = p.qstart[s];
   const int n = p.qstart[s + 1] - q0;
@@ -285,10 +314,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   if (tid == 0) {
     for (int g = 0; g < TC_QTILES; ++g) {
       mbar_init_count(s_full(g), 1);
+      mbar_init_count(s_free(g), 128);
       mbar_init_count(p_full(g), 128);
       mbar_init_count(pv_done(g), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NS; ++b) {
       mbar_init_count(k_full(b), 32);
       mbar_init_count(v_full(b), 32);
       mbar_init_count(k_free(b), 1);
@@ -310,8 +340,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto t_s = [&](int g) { return tmem + g * C::TILE_COLS + C::S_COL; };
-  auto t_o = [&](int g) { return tmem + g * C::TILE_COLS + C::O_COL; };
+  auto t_s = [&](int g) { return tmem + C::S_COL + 64u * g; };
+  auto t_p = [&](int g) { return tmem + C::P_COL + 32u * g; };
+  auto t_o = [&](int g) { return tmem + C::O_COL + 128u * g; };
   auto give_up = [&]() {
     if (!*abort_flag) record_error(PKV_DEV_WAIT_TIMEOUT);
     *abort_flag = 1;
@@ -320,117 +351,141 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
   bool failed = false;
   float l = 0.f;
 
-  if (warp >= 9) {
+  if (warp == 9 || warp == 10) {
     // ---------------- loads: warp 9 gathers K tiles, warp 10 V tiles ----------------
     const bool is_k = warp == 9;
     const __half* pool = is_k ? p.k : p.v;
+    const CUtensorMap* map = is_k ? &p.tmap_k : &p.tmap_v;
     const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
+    constexpr int ROWS = 32 / CPR;                            // rows per warp-wide cp.async
+    const int c = lane % CPR, rsub = lane / CPR;              // this lane's chunk and row offset
+    const int nb = TC_BN >> lb;                               // blocks per tile (2..16)
+    const uint32_t all_blocks = (nb == 32 ? 0xffffffffu : (1u << nb) - 1u);
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      const uint32_t dst = (is_k ? sk : sv) + st * C::KV_BYTES;
-      // slot j%2 is free once the MMAs of tile j-2 that read it are done
-      if (j >= 2 && !mbar_wait(is_k ? k_free(st) : v_free(st), ((j - 2) >> 1) & 1)) {
+      const int st = j % NS;
+      // slot j%4 is free once the MMAs of tile j-4 that read it are done
+      if (j >= NS && !mbar_wait(is_k ? k_free(st) : v_free(st), (j / NS - 1) & 1)) {
         failed = true;
         break;
       }
       if (*abort_flag) break;
-#pragma unroll
-      for (int rr = 0; rr < TC_BN / 32; ++rr) {
-        const int r = rr * 32 + lane;
-        const int t = j * TC_BN + r;
-        const bool valid = t < ctx;
-        int phys = valid ? table[t >> p.log2_block] : 0;
-        if (valid && (phys < 0 || phys >= p.num_blocks)) bad = 1;
-        const bool ok = valid && !bad;
-        if (!ok) phys = 0;
-        const __half* src = pool + (((static_cast<size_t>(phys) * H + h) << p.log2_block) + (t & (B - 1))) * D;
-#pragma unroll
-        for (int c = 0; c < CPR; ++c) cp_async16(dst + sw128(r, c, TC_BN), src + c * 8, ok ? 16 : 0);
+      const uint32_t full = is_k ? k_full(st) : v_full(st);
+      const uint32_t dst = (is_k ? sk : sv) + st * C::KV_BYTES;
+      // lane b < nb maps the tile's b-th block: phys = -1 past the context or for a bad entry
+      const int t0 = j * TC_BN + (lane << lb);
+      int phys = -1;
+      if (lane < nb && t0 < ctx) {
+        phys = table[t0 >> lb];
+        if (phys < 0 || phys >= p.num_blocks) {
+          bad = 1;
+          phys = -1;
+        }
       }
-      cp_async_wait_all();
-      fence_proxy_async_smem();                    // cp.async writes -> tensor-core reads
-      mbar_arrive(is_k ? k_full(st) : v_full(st));
+      // whole blocks inside the context arrive by TMA (B >= 8, so each lands on a 1024-byte
+      // boundary of the swizzled tile); the block holding the context's end, blocks past it and
+      // bad entries are copied (or zero-filled) by cp.async
+      const uint32_t tma_mask = __ballot_sync(0xffffffffu, p.use_tma && lane < nb && phys >= 0 && t0 + B <= ctx);
+      if (lane == 0 && tma_mask) mbar_expect_tx(full, static_cast<uint32_t>(__popc(tma_mask)) * B * D * 2);
+      for (int b = 0; b < nb; ++b) {
+        const int pb = __shfl_sync(0xffffffffu, phys, b);
+        if (lane == 0 && ((tma_mask >> b) & 1u)) {
+#pragma unroll
+          for (int half = 0; half < D / 64; ++half)
+            tma_load_3d(dst + half * (TC_BN * 128) + b * B * 128, map, half * 64, h * B, pb, full);
+        }
+      }
+      if (tma_mask != all_blocks) {
+        for (int r0 = 0; r0 < TC_BN; r0 += ROWS) {
+          const int b = r0 >> lb;                             // ROWS <= 4 <= B: one block per pass
+          const int pb = __shfl_sync(0xffffffffu, phys, b);
+          if ((tma_mask >> b) & 1u) continue;
+          const int r = r0 + rsub;
+          const int t = j * TC_BN + r;
+          const bool ok = t < ctx && pb >= 0;
+          const __half* src =
+              pool + (((static_cast<size_t>(ok ? pb : 0) * H + h) << lb) + (t & (B - 1))) * D + c * 8;
+          cp_async16(dst + sw128(r, c, TC_BN), src, ok ? 16 : 0);
+        }
+        cp_async_wait_all();
+        fence_proxy_async_smem();                             // cp.async writes -> tensor-core reads
+      }
+      mbar_arrive(full);
     }
     if (failed) give_up();
   } else if (warp == 8) {
-    // ---------------- MMA issue (one lane) ----------------
-    // Ping-pong order per key tile j: S0(j), PV1(j-1), S1(j), PV0(j).  While softmax 0 works on
-    // S0(j) the tensor cores run PV1(j-1) and S1(j), and while softmax 1 works on S1(j) they run
-    // PV0(j) and S0(j+1); with one query tile the order is S0(j), PV0(j).
+    // ---------------- S = Q K^T issue (one lane) ----------------
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
-      constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
-      int s_issued[TC_QTILES] = {0, 0}, pv_issued[TC_QTILES] = {0, 0};
-      // S_g(j) = Q_g K(j)^T, once PV_g(j-1), the last reader of S buffer g, is done
-      auto issue_s = [&](int g, int j) -> bool {
-        if (j >= 1 && !mbar_wait(pv_done(g), (j - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t qb = sq + g * C::Q_BYTES;
-        const uint32_t kb = sk + (j & 1) * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = umma_smem_desc(qb + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-          umma_ss(t_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full(g));
-        ++s_issued[g];
-        return true;
-      };
-      // O_g += P_g(j) V(j), once softmax g has written P_g(j) (V(j) has landed: checked by the caller)
-      auto issue_pv = [&](int g, int j) -> bool {
-        if (!mbar_wait(p_full(g), j & 1)) return false;
-        tc_fence_after();
-        const uint32_t vb = sv + (j & 1) * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < TC_BN / 16; ++kk) {
-          const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
-          umma_ts(t_o(g), t_s(g) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done(g));
-        ++pv_issued[g];
-        return true;
-      };
-      const bool two = ntile_q == 2;
+      int issued[TC_QTILES] = {0, 0};
       for (int j = 0; j < n_tiles && !failed; ++j) {
         if (*abort_flag) break;
-        if (!mbar_wait(k_full(j & 1), (j >> 1) & 1) || !issue_s(0, j)) {
+        if (!mbar_wait(k_full(j % NS), (j / NS) & 1)) {
           failed = true;
           break;
         }
-        if (two) {
-          if (j >= 1) {
-            if (!issue_pv(1, j - 1)) {              // V(j-1) landed before PV0(j-1) was issued
-              failed = true;
-              break;
-            }
-            umma_commit(v_free((j - 1) & 1));       // both PVs of tile j-1 issued
-          }
-          if (!issue_s(1, j)) {
+        const uint32_t kb = sk + (j % NS) * C::KV_BYTES;
+        for (int g = 0; g < ntile_q; ++g) {
+          // softmax g has read S_g(j-1) out of the buffer
+          if (j >= 1 && !mbar_wait(s_free(g), (j - 1) & 1)) {
             failed = true;
             break;
           }
+          tc_fence_after();
+          const uint32_t qb = sq + g * C::Q_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = umma_smem_desc(qb + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
+            umma_ss(t_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(g));
+          ++issued[g];
         }
-        umma_commit(k_free(j & 1));                // every S of tile j issued
-        if (!mbar_wait(v_full(j & 1), (j >> 1) & 1) || !issue_pv(0, j)) {
-          failed = true;
-          break;
-        }
-        if (!two) umma_commit(v_free(j & 1));
-      }
-      if (!failed && !*abort_flag && two) {
-        if (issue_pv(1, n_tiles - 1))
-          umma_commit(v_free((n_tiles - 1) & 1));
-        else
-          failed = true;
+        if (failed) break;
+        umma_commit(k_free(j % NS));               // every S of tile j issued
       }
       if (failed || *abort_flag) {
         give_up();
         // let the tensor-core work this lane issued finish (bounded) before memory is released
-        for (int g = 0; g < ntile_q; ++g) {
-          if (s_issued[g] > 0) mbar_wait(s_full(g), (s_issued[g] - 1) & 1);
-          if (pv_issued[g] > 0) mbar_wait(pv_done(g), (pv_issued[g] - 1) & 1);
+        for (int g = 0; g < ntile_q; ++g)
+          if (issued[g] > 0) mbar_wait(s_full(g), (issued[g] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ---------------- O += P V issue (one lane) ----------------
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
+      int issued[TC_QTILES] = {0, 0};
+      for (int j = 0; j < n_tiles && !failed; ++j) {
+        if (*abort_flag) break;
+        if (!mbar_wait(v_full(j % NS), (j / NS) & 1)) {
+          failed = true;
+          break;
         }
+        const uint32_t vb = sv + (j % NS) * C::KV_BYTES;
+        for (int g = 0; g < ntile_q; ++g) {
+          // softmax g has written P_g(j) (and finished any rescale of O_g)
+          if (!mbar_wait(p_full(g), j & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < TC_BN / 16; ++kk) {
+            const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
+            umma_ts(t_o(g), t_p(g) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(pv_done(g));
+          ++issued[g];
+        }
+        if (failed) break;
+        umma_commit(v_free(j % NS));               // every PV of tile j issued
+      }
+      if (failed || *abort_flag) {
+        give_up();
+        for (int g = 0; g < ntile_q; ++g)
+          if (issued[g] > 0) mbar_wait(pv_done(g), (issued[g] - 1) & 1);
       }
     }
     __syncwarp();
@@ -438,7 +493,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
     // ---------------- softmax (warps 0-3: query tile 0, warps 4-7: query tile 1) ----------------
     const int g = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t ts = t_s(g), to = t_o(g);
+    const uint32_t ts = t_s(g), tp = t_p(g), to = t_o(g);
     const int row_i = i0 + tid;                        // tid = g * 128 + row within the tile
     const int pos = ctx - n + row_i;
     const int tile_first = first_pos + g * TC_BM;      // position of the tile's first token
@@ -450,24 +505,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
         failed = true;
         break;
       }
-      tc_fence_after();                                // S(j) complete, and with it PV(j-1)
-      const bool need_mask = (j + 1) * TC_BN - 1 > tile_first;
-      const int key0 = j * TC_BN;
-      // this thread's row of S in registers: four 32-column loads, one wait
+      tc_fence_after();
       float sv[TC_BN];
-#pragma unroll
-      for (int c = 0; c < TC_BN / 32; ++c)
-        tmem_ld32_nowait(ts + lane_off + c * 32, *reinterpret_cast<float(*)[32]>(sv + c * 32));
+      tmem_ld32_nowait(ts + lane_off, *reinterpret_cast<float(*)[32]>(sv));
+      tmem_ld32_nowait(ts + lane_off + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
       tmem_ld_wait();
-      if (need_mask) {                                 // the diagonal tiles: keys after the token
+      tc_fence_before();
+      mbar_arrive(s_free(g));                          // S_g may now be overwritten by S_g(j+1)
+      const int key0 = j * TC_BN;
+      if (key0 + TC_BN - 1 > tile_first) {             // the diagonal tiles: keys after the token
 #pragma unroll
         for (int c = 0; c < TC_BN; ++c)
           if (key0 + c > pos) sv[c] = -INFINITY;
       }
-      // scale > 0, so the maximum of the scaled scores is the scaled maximum
-      float mx = sv[0];
+      // row maximum in eight independent chains; scale > 0, so the maximum of the scaled scores
+      // is the scaled maximum
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < TC_BN; ++c) mx = fmaxf(mx, sv[c]);
+      for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+#pragma unroll
+      for (int c = 8; c < TC_BN; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], sv[c + i]);
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       mx *= p.scale_log2;
       const bool rescale = mx > m_ref + TC_RESCALE;   // also true for the first finite max
       float alpha = 1.f;
@@ -475,7 +535,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
         alpha = exp2f(m_ref - mx);                     // 0 when m_ref = -inf
         m_ref = mx;
       }
-      const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+      const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
+      // PV_g(j-1) must be done before O_g is rescaled and before P_g is overwritten
+      if (j >= 1) {
+        if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (j - 1) & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+      }
       // if any row of the warp moved its max after the first tile, the whole warp rescales its O
       // rows (alpha is 1 for the rows that did not move)
       if (__any_sync(0xffffffffu, rescale && j > 0)) {
@@ -489,23 +557,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const P
           tmem_st32(to + lane_off + c * 32, ob);
         }
       }
-      // P = 2^(scale*S - m) as fp16, one FMA and one ex2 per score; 128 scores -> 64 columns
-      // written over the scores already read
-      float sum = 0.f;
-      const float nref = -ref;
+      // P = 2^(scale*S - m) as fp16: one FMA and one ex2 per score, four partial sums
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[TC_BN / 2];
 #pragma unroll
-      for (int c = 0; c < TC_BN / 64; ++c) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float e0 = fast_exp2(fmaf(sv[c * 64 + 2 * e], p.scale_log2, nref));
-          const float e1 = fast_exp2(fmaf(sv[c * 64 + 2 * e + 1], p.scale_log2, nref));
-          sum += e0 + e1;
-          pk[e] = pack_half2(e0, e1);
-        }
-        tmem_st32(ts + lane_off + c * 32, pk);
+      for (int e = 0; e < TC_BN / 2; ++e) {
+        const float e0 = fast_exp2(fmaf(sv[2 * e], p.scale_log2, nref));
+        const float e1 = fast_exp2(fmaf(sv[2 * e + 1], p.scale_log2, nref));
+        sum4[e & 3] += e0 + e1;
+        pk[e] = pack_half2(e0, e1);
       }
-      l = l * alpha + sum;
+      tmem_st32(tp + lane_off, pk);
+      l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full(g));
@@ -578,6 +641,42 @@ int launch_prefill(const PrefillParams& p, int num_seqs, int max_query_len, cuda
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, fetched once through the runtime (no link against libcuda).
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// A pool [num_blocks][H][B][D] fp16 as the 3-D tensor (D, H*B, num_blocks); a box is one head's
+// B rows of one 64-element half of the head dimension, written with the 128-byte swizzle.
+int encode_pool_map(CUtensorMap* map, const void* pool, int D, int H, int B, int num_blocks) {
+  const EncodeTiledFn fn = tensor_map_encoder();
+  if (!fn) return pkv::fail(PKV_ERR_CUDA, "paged prefill: cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H) * B,
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * B * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(B), 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(pool), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pkv::fail(PKV_ERR_CUDA, "paged prefill: tensor map encoding failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -642,6 +741,13 @@ int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, cons
   p.log2_block = lb;
   p.total_q = total_q;
   p.scale_log2 = scale * 1.4426950408889634f;
+  // whole blocks of 8 or more rows are fetched by TMA; smaller blocks by cp.async
+  p.use_tma = block_size >= 8 ? 1 : 0;
+  if (p.use_tma) {
+    int rc = encode_pool_map(&p.tmap_k, k_cache, head_dim, num_heads, block_size, num_blocks);
+    if (rc == PKV_OK) rc = encode_pool_map(&p.tmap_v, v_cache, head_dim, num_heads, block_size, num_blocks);
+    if (rc != PKV_OK) return rc;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int rc = head_dim == 128 ? launch_prefill<128>(p, num_seqs, max_query_len, st)
                                  : launch_prefill<64>(p, num_seqs, max_query_len, st);
