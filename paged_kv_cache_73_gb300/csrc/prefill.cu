@@ -205,6 +205,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
   return false;
 }
+// The same wait, also false once another role has raised the CTA's abort flag.  The flag is read
+// only on the slow path: a generic shared-memory read in an MMA-issuing thread stalls it until
+// the MMAs it has queued are done, so no hot loop reads it.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  if (mbar_try_wait_parity(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait_parity(bar, parity)) return true;
+    if ((it & 255u) == 255u && (*abort_flag != 0 || global_ns() - t0 > 2000000000ull)) return false;
+  }
+  return false;
+}
 
 // Byte offset of (row, 16-byte chunk) in a K-major / MN-major tile with 128-byte swizzle whose
 // head-dimension halves are regions of `rows` x 128 B.
@@ -237,20 +249,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // S_g, a separate P_g and the O_g accumulator, so S_g(j+1) is computed while softmax g is still
 // turning S_g(j) into P_g(j).  Warp roles (12 warps):
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread t of the group owns token row t = TMEM
-//              lane t.  For key tile j it waits S_g(j), copies its row to registers and releases
-//              the S buffer (s_free), masks and takes the row maximum, moves its running max
-//              (rescaling its O row) only when the tile raises it by more than 2^8, waits for
-//              PV_g(j-1) (the last reader of P_g and writer of O_g), writes P = 2^(S - m) as fp16
-//              and arrives on p_full.
-//   warp 8     one lane issues S_0(j) and S_1(j) once K(j) has landed and softmax g has released
-//              S_g(j-1).
-//   warp 11    one lane issues O_g += P_g(j) V(j) once V(j) and P_g(j) are there.  Two issuing
-//              threads keep the tensor cores fed while either one waits on a barrier.
+//              lane t.  For key tile j it waits S_g(j) (and so releases K slot j%4 for the
+//              loader), copies its row to registers and releases the S buffer (s_free, shared by
+//              both groups), masks and takes the row maximum, moves its running max (rescaling its
+//              O row) only when the tile raises it by more than 2^8, waits for PV_g(j-1) (the last
+//              reader of P_g and writer of O_g; this releases V slot (j-1)%4), writes
+//              P = 2^(S - m) as fp16 and arrives on p_full.
+//   warp 8     one lane issues S_0(j) and S_1(j) once K(j) has landed and both groups have
+//              released S(j-1).
+//   warp 11    one lane issues O_g += P_g(j) V(j) once V(j) and P_g(j) are there.  Each commit
+//              or barrier check costs an issuing thread on the order of a hundred cycles, so the
+//              two issuing threads do only the barrier work their own MMAs need; the ring slots
+//              are released by the softmax warps, which see the completions anyway.
 //   warps 9, 10 loads: gather key tile j's K (warp 9) or V (warp 10) through the table into ring
-//              slot j%4 once the MMAs of tile j-4 that read the slot are done (k_free / v_free).
-//              Whole blocks come by TMA (one box per block and head-dimension half, landing in
-//              the 128-byte swizzle); the rest by cp.async.  k_full / v_full complete when every
-//              lane has arrived and the TMA bytes have landed.
+//              slot j%4 once tile j-4 is done with it (k_free / v_free).  Whole blocks come by
+//              TMA (one box per block and head-dimension half, landing in the 128-byte swizzle);
+//              the rest by cp.async.  k_full / v_full complete when every lane has arrived and
+//              the TMA bytes have landed.
 // Per-slot and per-tile barriers keep every waiter within one phase of the barrier it waits on.
 // Every wait is bounded; a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop,
 // the others give up in turn, and the CTA still reaches its final barrier.
@@ -269,10 +284,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   const uint32_t sq = base;                                   // [2][128 rows][D], per-tile regions
   const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + NS * C::KV_BYTES;
   const uint32_t bars = sv + NS * C::KV_BYTES;
-  // per query tile g: s_full (S_g landed), s_free (S_g read out), p_full (P_g written), pv_done;
-  // per ring slot b: k_full / v_full (data landed), k_free / v_free (the MMAs reading it are done)
+  // per query tile g: s_full (S_g landed), p_full (P_g written), pv_done; s_free (both S read
+  // out); per ring slot b: k_full / v_full (data landed), k_free / v_free (the MMAs reading it
+  // are done)
   auto s_full = [&](int g) { return bars + 8u * g; };
-  auto s_free = [&](int g) { return bars + 16u + 8u * g; };
+  const uint32_t s_free = bars + 16u;                         // both query tiles' S read out
   auto p_full = [&](int g) { return bars + 32u + 8u * g; };
   auto pv_done = [&](int g) { return bars + 48u + 8u * g; };
   auto k_full = [&](int b) { return bars + 64u + 8u * b; };
@@ -314,15 +330,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   if (tid == 0) {
     for (int g = 0; g < TC_QTILES; ++g) {
       mbar_init_count(s_full(g), 1);
-      mbar_init_count(s_free(g), 128);
       mbar_init_count(p_full(g), 128);
       mbar_init_count(pv_done(g), 1);
     }
+    mbar_init_count(s_free, 128 * ntile_q);
     for (int b = 0; b < NS; ++b) {
       mbar_init_count(k_full(b), 32);
       mbar_init_count(v_full(b), 32);
-      mbar_init_count(k_free(b), 1);
-      mbar_init_count(v_free(b), 1);
+      // released by one lane of each softmax warp: K once it has seen S(j) complete, V once it
+      // has seen PV(j) complete
+      mbar_init_count(k_free(b), 4 * ntile_q);
+      mbar_init_count(v_free(b), 4 * ntile_q);
     }
     *abort_flag = 0;
   }
@@ -343,6 +361,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   auto t_s = [&](int g) { return tmem + C::S_COL + 64u * g; };
   auto t_p = [&](int g) { return tmem + C::P_COL + 32u * g; };
   auto t_o = [&](int g) { return tmem + C::O_COL + 128u * g; };
+  auto wait = [&](uint32_t bar, uint32_t parity) { return mbar_wait_or_abort(bar, parity, abort_flag); };
   auto give_up = [&]() {
     if (!*abort_flag) record_error(PKV_DEV_WAIT_TIMEOUT);
     *abort_flag = 1;
@@ -364,11 +383,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % NS;
       // slot j%4 is free once the MMAs of tile j-4 that read it are done
-      if (j >= NS && !mbar_wait(is_k ? k_free(st) : v_free(st), (j / NS - 1) & 1)) {
+      if (j >= NS && !wait(is_k ? k_free(st) : v_free(st), (j / NS - 1) & 1)) {
         failed = true;
         break;
       }
-      if (*abort_flag) break;
       const uint32_t full = is_k ? k_full(st) : v_full(st);
       const uint32_t dst = (is_k ? sk : sv) + st * C::KV_BYTES;
       // lane b < nb maps the tile's b-th block: phys = -1 past the context or for a bad entry
@@ -418,19 +436,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
       int issued[TC_QTILES] = {0, 0};
       for (int j = 0; j < n_tiles && !failed; ++j) {
-        if (*abort_flag) break;
-        if (!mbar_wait(k_full(j % NS), (j / NS) & 1)) {
+        if (!wait(k_full(j % NS), (j / NS) & 1)) {
           failed = true;
           break;
         }
+        // both softmax groups have read S(j-1) out of their buffers
+        if (j >= 1 && !wait(s_free, (j - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
         const uint32_t kb = sk + (j % NS) * C::KV_BYTES;
         for (int g = 0; g < ntile_q; ++g) {
-          // softmax g has read S_g(j-1) out of the buffer
-          if (j >= 1 && !mbar_wait(s_free(g), (j - 1) & 1)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
           const uint32_t qb = sq + g * C::Q_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -441,10 +458,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
           umma_commit(s_full(g));
           ++issued[g];
         }
-        if (failed) break;
-        umma_commit(k_free(j % NS));               // every S of tile j issued
       }
-      if (failed || *abort_flag) {
+      if (failed) {
         give_up();
         // let the tensor-core work this lane issued finish (bounded) before memory is released
         for (int g = 0; g < ntile_q; ++g)
@@ -458,15 +473,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       constexpr uint32_t IDESC_PV = umma_idesc_f16(TC_BM, D, true);
       int issued[TC_QTILES] = {0, 0};
       for (int j = 0; j < n_tiles && !failed; ++j) {
-        if (*abort_flag) break;
-        if (!mbar_wait(v_full(j % NS), (j / NS) & 1)) {
+        if (!wait(v_full(j % NS), (j / NS) & 1)) {
           failed = true;
           break;
         }
         const uint32_t vb = sv + (j % NS) * C::KV_BYTES;
         for (int g = 0; g < ntile_q; ++g) {
           // softmax g has written P_g(j) (and finished any rescale of O_g)
-          if (!mbar_wait(p_full(g), j & 1)) {
+          if (!wait(p_full(g), j & 1)) {
             failed = true;
             break;
           }
@@ -479,10 +493,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
           umma_commit(pv_done(g));
           ++issued[g];
         }
-        if (failed) break;
-        umma_commit(v_free(j % NS));               // every PV of tile j issued
       }
-      if (failed || *abort_flag) {
+      if (failed) {
         give_up();
         for (int g = 0; g < ntile_q; ++g)
           if (issued[g] > 0) mbar_wait(pv_done(g), (issued[g] - 1) & 1);
@@ -500,18 +512,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     float m_ref = -INFINITY;
     for (int j = 0; j < n_tiles; ++j) {
       // decisions stay warp-uniform: the tcgen05.ld/st below are warp-collective
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full(g), j & 1))) {
+      if (!__all_sync(0xffffffffu, wait(s_full(g), j & 1))) {
         failed = true;
         break;
       }
       tc_fence_after();
+      if (lane == 0) mbar_arrive(k_free(j % NS));     // S_g(j) is done reading K(j)
       float sv[TC_BN];
       tmem_ld32_nowait(ts + lane_off, *reinterpret_cast<float(*)[32]>(sv));
       tmem_ld32_nowait(ts + lane_off + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(s_free(g));                          // S_g may now be overwritten by S_g(j+1)
+      mbar_arrive(s_free);                             // S_g may now be overwritten by S_g(j+1)
       const int key0 = j * TC_BN;
       if (key0 + TC_BN - 1 > tile_first) {             // the diagonal tiles: keys after the token
 #pragma unroll
@@ -538,11 +550,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
       // PV_g(j-1) must be done before O_g is rescaled and before P_g is overwritten
       if (j >= 1) {
-        if (!__all_sync(0xffffffffu, mbar_wait(pv_done(g), (j - 1) & 1))) {
+        if (!__all_sync(0xffffffffu, wait(pv_done(g), (j - 1) & 1))) {
           failed = true;
           break;
         }
         tc_fence_after();
+        if (lane == 0) mbar_arrive(v_free((j - 1) % NS));   // PV_g(j-1) is done reading V(j-1)
       }
       // if any row of the warp moved its max after the first tile, the whole warp rescales its O
       // rows (alpha is 1 for the rows that did not move)
@@ -573,8 +586,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       tc_fence_before();
       mbar_arrive(p_full(g));
     }
-    if (!failed && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      failed = !__all_sync(0xffffffffu, mbar_wait(pv_done(g), (n_tiles - 1) & 1));
+    if (!failed) {
+      failed = !__all_sync(0xffffffffu, wait(pv_done(g), (n_tiles - 1) & 1));
       tc_fence_after();
     }
     if (failed) give_up();
