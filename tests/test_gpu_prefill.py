@@ -109,3 +109,27 @@ def test_bad_query_range_recorded(cuda_device):
     assert code == 6
     rows, ref = _oracle(w, q, qs, [0])
     assert np.max(np.abs(out.cpu().numpy()[rows].astype(np.float64) - ref)) <= ATOL
+
+
+@pytest.mark.parametrize("B", [4, 16])
+def test_bad_block_id_recorded(cuda_device, B):
+    # an out-of-range and a negative entry inside sequence 0's context: the code is recorded, the
+    # bad sequence's rows are not written, and the other sequence is unaffected (B = 16 takes the
+    # tensor-map path for whole blocks, B = 4 the copy path)
+    w = wl.custom(44 + B, [200, 150], num_heads=2, head_dim=128, block_size=B)
+    news = [40, 60]
+    tables = w.block_tables.copy()
+    tables[0, 1] = w.num_blocks + 5
+    tables[0, 3] = -2
+    qs = np.concatenate([[0], np.cumsum(news)]).astype(np.int32)
+    k, v = w.pools(cuda_device)
+    q = wl.dense_tensor((int(qs[-1]), w.num_heads, w.head_dim), 78, wl.STREAM_Q, cuda_device)
+    out = torch.full_like(q, 7.0)
+    pkv.paged_attention_prefill(q, k, v, torch.from_numpy(tables).to(cuda_device),
+                                torch.from_numpy(w.context_lens).to(cuda_device), torch.from_numpy(qs).to(cuda_device),
+                                w.scale, w.block_size, max(news), out=out)
+    assert pkv.device_error() == 1
+    got = out.cpu().numpy().astype(np.float64)
+    assert (got[: news[0]] == 7.0).all()
+    rows, ref = _oracle(w, q, qs, [1])
+    assert np.max(np.abs(got[rows] - ref)) <= ATOL
