@@ -233,9 +233,10 @@ struct TcCfg {
   // (holding all 512 tensor-memory columns) runs per SM
   static constexpr int SMEM = 1024 /*alignment slack*/ + 2 * TC_BM * 128 * 2 + 2 * STAGES * TC_BN * 128 * 2 + 256;
   static constexpr uint32_t TMEM_COLS = 512;
-  // tensor-memory columns of query tile g: O at 128 g (D used), S at 256 + 64 g, P (fp16 pairs)
-  // at 384 + 32 g
-  static constexpr uint32_t O_COL = 0, S_COL = 256, P_COL = 384;
+  // tensor-memory columns of query tile g: O at 128 g (D used); two S buffers at 256 + 128 g and
+  // 256 + 128 g + 64 (key tile j uses buffer j % 2), P(j) as fp16 pairs over the first 32 columns
+  // of S(j)'s buffer
+  static constexpr uint32_t O_COL = 0, S_COL = 256;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -246,27 +247,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // One CTA owns 256 new tokens of one (sequence, head) as two 128-token query tiles that share
 // every K/V tile it loads.  Key tiles are 64 positions.  Per query tile g tensor memory holds
-// S_g, a separate P_g and the O_g accumulator, so S_g(j+1) is computed while softmax g is still
-// turning S_g(j) into P_g(j).  Warp roles (12 warps):
+// the O_g accumulator and two S buffers: S_g(j) lands in buffer j % 2 and P_g(j) is written back
+// over its first 32 columns, so S_g(j+1) is computed while softmax g still works on tile j.
+// Warp roles (12 warps):
 //   warps 0-3 / 4-7  softmax of query tile 0 / 1: thread t of the group owns token row t = TMEM
 //              lane t.  For key tile j it waits S_g(j) (and so releases K slot j%4 for the
-//              loader), copies its row to registers and releases the S buffer (s_free, shared by
-//              both groups), masks and takes the row maximum, moves its running max (rescaling its
-//              O row) only when the tile raises it by more than 2^8, waits for PV_g(j-1) (the last
-//              reader of P_g and writer of O_g; this releases V slot (j-1)%4), writes
-//              P = 2^(S - m) as fp16 and arrives on p_full.
-//   warp 8     one lane issues S_0(j) and S_1(j) once K(j) has landed and both groups have
-//              released S(j-1).
-//   warp 11    one lane issues O_g += P_g(j) V(j) once V(j) and P_g(j) are there.  Each commit
-//              or barrier check costs an issuing thread on the order of a hundred cycles, so the
-//              two issuing threads do only the barrier work their own MMAs need; the ring slots
-//              are released by the softmax warps, which see the completions anyway.
+//              loader), copies its row to registers, masks and takes the row maximum, moves its
+//              running max only when the tile raises it by more than 2^8 (then, after PV_g(j-1)
+//              is done, rescaling its O row), writes P = 2^(S - m) as fp16 over the scores and
+//              arrives on p_full.
+//   warp 8     one lane issues S_0(j) and S_1(j) once K(j) has landed and PV_g(j-2), the last
+//              reader of buffer j % 2, is done.
+//   warp 11    one lane issues O_g += P_g(j) V(j) once V(j) and P_g(j) are there, then releases
+//              V slot j%4.  Each commit or barrier check costs an issuing thread on the order of
+//              a hundred cycles and the issuing warps share their SM quarter with softmax warps,
+//              so the two issuing threads do little besides issuing (descriptors precomputed).
 //   warps 9, 10 loads: gather key tile j's K (warp 9) or V (warp 10) through the table into ring
 //              slot j%4 once tile j-4 is done with it (k_free / v_free).  Whole blocks come by
 //              TMA (one box per block and head-dimension half, landing in the 128-byte swizzle);
 //              the rest by cp.async.  k_full / v_full complete when every lane has arrived and
 //              the TMA bytes have landed.
-// Per-slot and per-tile barriers keep every waiter within one phase of the barrier it waits on.
+// Per-slot and per-buffer barriers keep every waiter within one phase of the barrier it waits on.
 // Every wait is bounded; a role that gives up records PKV_DEV_WAIT_TIMEOUT and leaves its loop,
 // the others give up in turn, and the CTA still reaches its final barrier.
 constexpr int TC_QTILES = 2;
@@ -284,19 +285,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   const uint32_t sq = base;                                   // [2][128 rows][D], per-tile regions
   const uint32_t sk = sq + TC_QTILES * C::Q_BYTES, sv = sk + NS * C::KV_BYTES;
   const uint32_t bars = sv + NS * C::KV_BYTES;
-  // per query tile g: s_full (S_g landed), p_full (P_g written), pv_done; s_free (both S read
-  // out); per ring slot b: k_full / v_full (data landed), k_free / v_free (the MMAs reading it
-  // are done)
-  auto s_full = [&](int g) { return bars + 8u * g; };
-  const uint32_t s_free = bars + 16u;                         // both query tiles' S read out
-  auto p_full = [&](int g) { return bars + 32u + 8u * g; };
-  auto pv_done = [&](int g) { return bars + 48u + 8u * g; };
-  auto k_full = [&](int b) { return bars + 64u + 8u * b; };
-  auto v_full = [&](int b) { return bars + 96u + 8u * b; };
-  auto k_free = [&](int b) { return bars + 128u + 8u * b; };
-  auto v_free = [&](int b) { return bars + 160u + 8u * b; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 192 - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 196 - base));
+  // per query tile g and S buffer u (key tile j uses u = j % 2): s_full (S_g(j) landed), p_full
+  // (P_g(j) written), pv_done (PV_g(j) done); per ring slot b: k_full / v_full (data landed),
+  // k_free / v_free (the MMAs reading it are done).  A waiter on a per-buffer barrier can never
+  // be two phases behind it, so the phase parity it waits on is unambiguous.
+  auto s_full = [&](int g, int u) { return bars + 8u * (2 * g + u); };
+  auto p_full = [&](int g, int u) { return bars + 32u + 8u * (2 * g + u); };
+  auto pv_done = [&](int g, int u) { return bars + 64u + 8u * (2 * g + u); };
+  auto k_full = [&](int b) { return bars + 96u + 8u * b; };
+  auto v_full = [&](int b) { return bars + 96u + 8u * (NS + b); };
+  auto k_free = [&](int b) { return bars + 96u + 8u * (2 * NS + b); };
+  auto v_free = [&](int b) { return bars + 96u + 8u * (3 * NS + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 96 + 32 * NS - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 100 + 32 * NS - base));
+  static_assert(104 + 32 * NS <= 256, "barrier area");
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -328,19 +330,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     tc_fence_before();
   }
   if (tid == 0) {
-    for (int g = 0; g < TC_QTILES; ++g) {
-      mbar_init_count(s_full(g), 1);
-      mbar_init_count(p_full(g), 128);
-      mbar_init_count(pv_done(g), 1);
-    }
-    mbar_init_count(s_free, 128 * ntile_q);
+    for (int g = 0; g < TC_QTILES; ++g)
+      for (int u = 0; u < 2; ++u) {
+        mbar_init_count(s_full(g, u), 1);
+        mbar_init_count(p_full(g, u), 128);
+        mbar_init_count(pv_done(g, u), 1);
+      }
     for (int b = 0; b < NS; ++b) {
       mbar_init_count(k_full(b), 32);
       mbar_init_count(v_full(b), 32);
-      // released by one lane of each softmax warp: K once it has seen S(j) complete, V once it
-      // has seen PV(j) complete
+      // K: released by one lane of each softmax warp once it has seen S(j) complete; V: by the
+      // PV-issuing thread's commit after the last PV of tile j
       mbar_init_count(k_free(b), 4 * ntile_q);
-      mbar_init_count(v_free(b), 4 * ntile_q);
+      mbar_init_count(v_free(b), 1);
     }
     *abort_flag = 0;
   }
@@ -358,8 +360,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto t_s = [&](int g) { return tmem + C::S_COL + 64u * g; };
-  auto t_p = [&](int g) { return tmem + C::P_COL + 32u * g; };
+  auto t_s = [&](int g, int u) { return tmem + C::S_COL + 128u * g + 64u * u; };
   auto t_o = [&](int g) { return tmem + C::O_COL + 128u * g; };
   auto wait = [&](uint32_t bar, uint32_t parity) { return mbar_wait_or_abort(bar, parity, abort_flag); };
   auto give_up = [&]() {
@@ -434,28 +435,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     // ---------------- S = Q K^T issue (one lane) ----------------
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
+      const uint64_t a_desc0 = umma_smem_desc(sq, 16, 1024), a_desc1 = umma_smem_desc(sq + C::Q_BYTES, 16, 1024);
       int issued[TC_QTILES] = {0, 0};
       for (int j = 0; j < n_tiles && !failed; ++j) {
         if (!wait(k_full(j % NS), (j / NS) & 1)) {
           failed = true;
           break;
         }
-        // both softmax groups have read S(j-1) out of their buffers
-        if (j >= 1 && !wait(s_free, (j - 1) & 1)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
         const uint32_t kb = sk + (j % NS) * C::KV_BYTES;
+        const int u = j & 1;
+        // the descriptors of a K-step differ from the first by the start-address field alone
+        // (shared-memory byte offset / 16, far from overflowing its 14 bits): one add per MMA
+        const uint64_t b0 = umma_smem_desc(kb, 16, 1024);
         for (int g = 0; g < ntile_q; ++g) {
-          const uint32_t qb = sq + g * C::Q_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = umma_smem_desc(qb + (kk >> 2) * (TC_BM * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = umma_smem_desc(kb + (kk >> 2) * (TC_BN * 128) + (kk & 3) * 32, 16, 1024);
-            umma_ss(t_s(g), a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+          // S buffer u of tile g is free once PV_g(j-2), which read P_g(j-2) from it, is done
+          if (j >= 2 && !wait(pv_done(g, u), ((j - 2) >> 1) & 1)) {
+            failed = true;
+            break;
           }
-          umma_commit(s_full(g));
+          tc_fence_after();
+          const uint64_t a0 = g == 0 ? a_desc0 : a_desc1;
+          const uint32_t d = t_s(g, u);
+          umma_ss(d, a0, b0, IDESC_QK, 0u);
+#pragma unroll
+          for (int kk = 1; kk < D / 16; ++kk)
+            umma_ss(d, a0 + (((kk >> 2) * (TC_BM * 128) + (kk & 3) * 32) >> 4),
+                    b0 + (((kk >> 2) * (TC_BN * 128) + (kk & 3) * 32) >> 4), IDESC_QK, 1u);
+          umma_commit(s_full(g, u));
           ++issued[g];
         }
       }
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
         give_up();
         // let the tensor-core work this lane issued finish (bounded) before memory is released
         for (int g = 0; g < ntile_q; ++g)
-          if (issued[g] > 0) mbar_wait(s_full(g), (issued[g] - 1) & 1);
+          if (issued[g] > 0) mbar_wait(s_full(g, (issued[g] - 1) & 1), ((issued[g] - 1) >> 1) & 1);
       }
     }
     __syncwarp();
@@ -478,26 +484,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
           break;
         }
         const uint32_t vb = sv + (j % NS) * C::KV_BYTES;
+        const int u = j & 1;
         for (int g = 0; g < ntile_q; ++g) {
           // softmax g has written P_g(j) (and finished any rescale of O_g)
-          if (!wait(p_full(g), j & 1)) {
+          if (!wait(p_full(g, u), (j >> 1) & 1)) {
             failed = true;
             break;
           }
           tc_fence_after();
+          const uint64_t v0 = umma_smem_desc(vb, TC_BN * 128, 1024);
+          const uint32_t o = t_o(g), pa = t_s(g, u);
+          umma_ts(o, pa, v0, IDESC_PV, j > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < TC_BN / 16; ++kk) {
-            const uint64_t b = umma_smem_desc(vb + kk * 16 * 128, TC_BN * 128, 1024);
-            umma_ts(t_o(g), t_p(g) + kk * 8, b, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(pv_done(g));
+          for (int kk = 1; kk < TC_BN / 16; ++kk) umma_ts(o, pa + kk * 8, v0 + ((kk * 16 * 128) >> 4), IDESC_PV, 1u);
+          umma_commit(pv_done(g, u));
           ++issued[g];
         }
+        if (failed) break;
+        umma_commit(v_free(j % NS));               // every PV of tile j issued
       }
       if (failed) {
         give_up();
         for (int g = 0; g < ntile_q; ++g)
-          if (issued[g] > 0) mbar_wait(pv_done(g), (issued[g] - 1) & 1);
+          if (issued[g] > 0) mbar_wait(pv_done(g, (issued[g] - 1) & 1), ((issued[g] - 1) >> 1) & 1);
       }
     }
     __syncwarp();
@@ -505,14 +514,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     // ---------------- softmax (warps 0-3: query tile 0, warps 4-7: query tile 1) ----------------
     const int g = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t ts = t_s(g), tp = t_p(g), to = t_o(g);
+    const uint32_t to = t_o(g);
     const int row_i = i0 + tid;                        // tid = g * 128 + row within the tile
     const int pos = ctx - n + row_i;
     const int tile_first = first_pos + g * TC_BM;      // position of the tile's first token
     float m_ref = -INFINITY;
     for (int j = 0; j < n_tiles; ++j) {
       // decisions stay warp-uniform: the tcgen05.ld/st below are warp-collective
-      if (!__all_sync(0xffffffffu, wait(s_full(g), j & 1))) {
+      const int u = j & 1;
+      const uint32_t ts = t_s(g, u);
+      if (!__all_sync(0xffffffffu, wait(s_full(g, u), (j >> 1) & 1))) {
         failed = true;
         break;
       }
@@ -522,8 +533,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       tmem_ld32_nowait(ts + lane_off, *reinterpret_cast<float(*)[32]>(sv));
       tmem_ld32_nowait(ts + lane_off + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(s_free);                             // S_g may now be overwritten by S_g(j+1)
       const int key0 = j * TC_BN;
       if (key0 + TC_BN - 1 > tile_first) {             // the diagonal tiles: keys after the token
 #pragma unroll
@@ -548,18 +557,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
         m_ref = mx;
       }
       const float nref = m_ref == -INFINITY ? 0.f : -m_ref;
-      // PV_g(j-1) must be done before O_g is rescaled and before P_g is overwritten
-      if (j >= 1) {
-        if (!__all_sync(0xffffffffu, wait(pv_done(g), (j - 1) & 1))) {
+      // if any row of the warp moved its max after the first tile, the whole warp rescales its O
+      // rows (alpha is 1 for the rows that did not move), once PV_g(j-1) has finished with O_g
+      if (__any_sync(0xffffffffu, rescale && j > 0)) {
+        if (!__all_sync(0xffffffffu, wait(pv_done(g, (j - 1) & 1), ((j - 1) >> 1) & 1))) {
           failed = true;
           break;
         }
         tc_fence_after();
-        if (lane == 0) mbar_arrive(v_free((j - 1) % NS));   // PV_g(j-1) is done reading V(j-1)
-      }
-      // if any row of the warp moved its max after the first tile, the whole warp rescales its O
-      // rows (alpha is 1 for the rows that did not move)
-      if (__any_sync(0xffffffffu, rescale && j > 0)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -580,14 +585,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
         sum4[e & 3] += e0 + e1;
         pk[e] = pack_half2(e0, e1);
       }
-      tmem_st32(tp + lane_off, pk);
+      tmem_st32(ts + lane_off, pk);                    // P_g(j) over the scores already read
       l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full(g));
+      mbar_arrive(p_full(g, u));
     }
     if (!failed) {
-      failed = !__all_sync(0xffffffffu, wait(pv_done(g), (n_tiles - 1) & 1));
+      failed = !__all_sync(0xffffffffu, wait(pv_done(g, (n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1));
       tc_fence_after();
     }
     if (failed) give_up();
