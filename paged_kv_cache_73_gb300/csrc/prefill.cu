@@ -74,10 +74,10 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 //
 // A softmax thread owns one new-token row, which is one TMEM lane of its query tile.  Per key
 // tile of 64 positions one thread issues S = Q K^T (tcgen05.mma, M=128, N=64, fp16 in, fp32 in
-// TMEM); every softmax thread reads its row of S
-// (tcgen05.ld), masks it, updates its running max/sum and writes P = 2^(S - m) as fp16 to its
-// own TMEM columns (tcgen05.st); one thread issues O += P V (A = P from TMEM, B = V from shared
-// memory, MN-major) into the TMEM accumulator.  MMA groups complete on mbarriers.
+// TMEM); every softmax thread reads its row of S (tcgen05.ld), masks it, updates its running
+// max/sum and writes P = 2^(S - m) as fp16 back over the scores it read (tcgen05.st); one thread
+// issues O += P V (A = P from TMEM, B = V from shared memory, MN-major) into the TMEM
+// accumulator.  MMA groups complete on mbarriers.
 // The running max m of a row is only moved (and O rescaled) when a tile raises it by more than
 // 2^8, so P stays within fp16 range while most tiles skip the O read-modify-write.
 // Q, K and V tiles sit in shared memory in the canonical K-major / MN-major layouts with 128-byte
