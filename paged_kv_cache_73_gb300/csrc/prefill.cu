@@ -244,6 +244,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Paired fp32 arithmetic (one instruction for two lanes of work): the softmax threads share their
+// SM quarter with the MMA-issuing threads, so every instruction they save is issue time for those.
+// (y0, y1) = (x0, x1) * s + c, each rounded once as fmaf would.
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float s, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+// (a0, a1) += (x0, x1)
+__device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 // One CTA owns 256 new tokens of one (sequence, head) as two 128-token query tiles that share
 // every K/V tile it loads.  Key tiles are 64 positions.  Per query tile g tensor memory holds
@@ -539,16 +560,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
         for (int c = 0; c < TC_BN; ++c)
           if (key0 + c > pos) sv[c] = -INFINITY;
       }
-      // row maximum in eight independent chains; scale > 0, so the maximum of the scaled scores
-      // is the scaled maximum
+      // row maximum: three-input maxima in eight independent chains; scale > 0, so the maximum of
+      // the scaled scores is the scaled maximum
       float m8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+      for (int i = 0; i < 8; ++i) m8[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-      for (int c = 8; c < TC_BN; c += 8)
+      for (int c = 16; c < TC_BN; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], sv[c + i]);
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int i = 0; i < 8; ++i) m8[i] = max3(m8[i], sv[c + i], sv[c + 8 + i]);
+      float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       mx *= p.scale_log2;
       const bool rescale = mx > m_ref + TC_RESCALE;   // also true for the first finite max
       float alpha = 1.f;
@@ -575,16 +596,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
           tmem_st32(to + lane_off + c * 32, ob);
         }
       }
-      // P = 2^(scale*S - m) as fp16: one FMA and one ex2 per score, four partial sums
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(scale*S - m) as fp16: one paired FMA per two scores, one ex2 per score, the row
+      // sum in four paired accumulators
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[TC_BN / 2];
 #pragma unroll
       for (int e = 0; e < TC_BN / 2; ++e) {
-        const float e0 = fast_exp2(fmaf(sv[2 * e], p.scale_log2, nref));
-        const float e1 = fast_exp2(fmaf(sv[2 * e + 1], p.scale_log2, nref));
-        sum4[e & 3] += e0 + e1;
+        float x0, x1;
+        fma2(x0, x1, sv[2 * e], sv[2 * e + 1], p.scale_log2, nref);
+        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+        add2(sum8[2 * (e & 3)], sum8[2 * (e & 3) + 1], e0, e1);
         pk[e] = pack_half2(e0, e1);
       }
+      float sum4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum4[i] = sum8[2 * i] + sum8[2 * i + 1];
       tmem_st32(ts + lane_off, pk);                    // P_g(j) over the scores already read
       l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       tmem_st_wait();
