@@ -39,6 +39,8 @@ struct PrefillParams {
   // (encoded only when use_tma is set)
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
+  // q as the 3-D tensor (D, H, total_q), boxes of 64 x 1 x 128 with 128-byte swizzle
+  CUtensorMap tmap_q;
   const __half* q;
   const __half* k;
   const __half* v;
@@ -170,6 +172,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 // Adds `bytes` to the transaction count the barrier's current phase waits for (no arrival).
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Arrives on the barrier and adds `bytes` to the transaction count of its current phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 // TMA tile load of the box at (x, y, z) of a 3-D tensor map into shared memory; completion is
 // counted in bytes on `bar`.  Coordinates outside the tensor read as zero.
@@ -317,9 +323,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   auto v_full = [&](int b) { return bars + 96u + 8u * (NS + b); };
   auto k_free = [&](int b) { return bars + 96u + 8u * (2 * NS + b); };
   auto v_free = [&](int b) { return bars + 96u + 8u * (3 * NS + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 96 + 32 * NS - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 100 + 32 * NS - base));
-  static_assert(104 + 32 * NS <= 256, "barrier area");
+  const uint32_t q_full = bars + 96 + 32 * NS;                // the Q tiles landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bars + 104 + 32 * NS - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bars + 108 + 32 * NS - base));
+  static_assert(112 + 32 * NS <= 256, "barrier area");
 
   pkv::pdl_trigger();
   pkv::pdl_wait();
@@ -366,17 +373,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       mbar_init_count(v_free(b), 1);
     }
     *abort_flag = 0;
-  }
-  if (tid < TC_QTILES * TC_BM) {
-    // Q tiles: softmax thread t copies token row t (rows past the new tokens are zero)
-    const int g = tid >> 7, r = tid & 127;
-    const int i = i0 + tid;
-    const __half* src = p.q + (static_cast<size_t>(q0 + min(i, n - 1)) * H + h) * D;
-    const uint32_t dst = sq + g * C::Q_BYTES;
+    // the Q tiles by TMA, right away, overlapping the first K/V loads: rows i0 + 128 g + r of
+    // head h, landing in the 128-byte swizzle.  Rows past the sequence's new tokens read the next
+    // sequence's (or, past total_q, zeros); their results are never stored.
+    mbar_init_count(q_full, 1);
+    mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(ntile_q) * C::Q_BYTES);
+    for (int g = 0; g < ntile_q; ++g)
 #pragma unroll
-    for (int c = 0; c < CPR; ++c) cp_async16(dst + sw128(r, c, TC_BM), src + c * 8, i < n ? 16 : 0);
-    cp_async_wait_all();
-    fence_proxy_async_smem();
+      for (int half = 0; half < D / 64; ++half)
+        tma_load_3d(sq + g * C::Q_BYTES + half * (TC_BM * 128), &p.tmap_q, half * 64, h, q0 + i0 + g * TC_BM, q_full);
   }
   __syncthreads();
   tc_fence_after();
@@ -402,6 +407,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     const int c = lane % CPR, rsub = lane / CPR;              // this lane's chunk and row offset
     const int nb = TC_BN >> lb;                               // blocks per tile (2..16)
     const uint32_t all_blocks = (nb == 32 ? 0xffffffffu : (1u << nb) - 1u);
+    int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % NS;
       // slot j%4 is free once the MMAs of tile j-4 that read it are done
@@ -450,14 +456,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
         fence_proxy_async_smem();                             // cp.async writes -> tensor-core reads
       }
       mbar_arrive(full);
+      ++issued;
     }
     if (failed) give_up();
+    if (*abort_flag) {
+      // let the copies this warp issued land (bounded) before the CTA's shared memory is released
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        mbar_wait(is_k ? k_full(t % NS) : v_full(t % NS), (t / NS) & 1);
+    }
   } else if (warp == 8) {
     // ---------------- S = Q K^T issue (one lane) ----------------
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = umma_idesc_f16(TC_BM, TC_BN, false);
       const uint64_t a_desc0 = umma_smem_desc(sq, 16, 1024), a_desc1 = umma_smem_desc(sq + C::Q_BYTES, 16, 1024);
       int issued[TC_QTILES] = {0, 0};
+      failed = !wait(q_full, 0);
       for (int j = 0; j < n_tiles && !failed; ++j) {
         if (!wait(k_full(j % NS), (j / NS) & 1)) {
           failed = true;
@@ -628,28 +641,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   bad = __syncthreads_or(bad);
   const bool aborted = *abort_flag != 0;
   if (warp < 4 * ntile_q && !aborted && !bad) {
-    // every lane loads (warp-collective); only rows that are real new tokens are stored
+    // Each thread normalises its O row (every lane loads: tcgen05.ld is warp-collective) and
+    // stages it in the K/V ring, free now that every MMA is done, as 16-byte chunks XOR-ed with
+    // the row's low bits (no bank conflicts either way).  The warp then writes its 32 rows back
+    // whole: each row is D*2 contiguous bytes of out, stored by D/8 lanes at once.  Rows past the
+    // sequence's new tokens are not stored.
     const int g = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int row_i = i0 + tid;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    __half* dst = p.out + (static_cast<size_t>(q0 + min(row_i, n - 1)) * H + h) * D;
+    unsigned char* stage = smem + (sk - base);                // [256 rows][D * 2 bytes]
+    constexpr int RB = D * 2;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       float o[32];
       tmem_ld32(t_o(g) + lane_off + c * 32, o);
-      if (row_i >= n) continue;
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
+      for (int k = 0; k < 4; ++k) {
         uint4 w;
-        w.x = pack_half2(o[e] * inv, o[e + 1] * inv);
-        w.y = pack_half2(o[e + 2] * inv, o[e + 3] * inv);
-        w.z = pack_half2(o[e + 4] * inv, o[e + 5] * inv);
-        w.w = pack_half2(o[e + 6] * inv, o[e + 7] * inv);
-        *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
+        w.x = pack_half2(o[8 * k] * inv, o[8 * k + 1] * inv);
+        w.y = pack_half2(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
+        w.z = pack_half2(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
+        w.w = pack_half2(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
+        *reinterpret_cast<uint4*>(stage + tid * RB + (((c * 4 + k) ^ (tid & (CPR - 1))) << 4)) = w;
+      }
+    }
+    __syncwarp();
+    constexpr int RPI = 32 / CPR;                             // rows per warp-wide store
+    const int c = lane % CPR;
+#pragma unroll 4
+    for (int r0 = 0; r0 < 32; r0 += RPI) {
+      const int row = warp * 32 + r0 + lane / CPR;            // CTA row = token i0 + row
+      if (i0 + row < n) {
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + row * RB + ((c ^ (row & (CPR - 1))) << 4));
+        *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(q0 + i0 + row) * H + h) * D + c * 8) = w;
       }
     }
   }
+  // the Q copies have landed (they have, unless the CTA gave up early): bounded
+  if (tid == 0) mbar_wait(q_full, 0);
   if (bad && tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
   cp_async_wait_all();
   // all tensor-memory reads are done (tcgen05.ld waits inline); release the columns
@@ -721,6 +750,22 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int D, int H, int B, int
   return PKV_OK;
 }
 
+// q [T][H][D] fp16 as the 3-D tensor (D, H, T); a box is 128 tokens of one head and one 64-element
+// half of the head dimension, written with the 128-byte swizzle.
+int encode_q_map(CUtensorMap* map, const void* q, int D, int H, int T) {
+  const EncodeTiledFn fn = tensor_map_encoder();
+  if (!fn) return pkv::fail(PKV_ERR_CUDA, "paged prefill: cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(TC_BM)};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q), dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pkv::fail(PKV_ERR_CUDA, "paged prefill: q tensor map encoding failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -785,6 +830,10 @@ int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, cons
   p.log2_block = lb;
   p.total_q = total_q;
   p.scale_log2 = scale * 1.4426950408889634f;
+  {
+    const int rc = encode_q_map(&p.tmap_q, q, head_dim, num_heads, total_q);
+    if (rc != PKV_OK) return rc;
+  }
   // whole blocks of 8 or more rows are fetched by TMA; smaller blocks by cp.async
   p.use_tma = block_size >= 8 ? 1 : 0;
   if (p.use_tma) {
