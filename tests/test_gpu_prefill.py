@@ -133,3 +133,26 @@ def test_bad_block_id_recorded(cuda_device, B):
     assert (got[: news[0]] == 7.0).all()
     rows, ref = _oracle(w, q, qs, [1])
     assert np.max(np.abs(got[rows] - ref)) <= ATOL
+
+
+def test_long_prompts_full_size_sampled(cuda_device):
+    # the bench's long-prompt launch: 8 prompts x 4096 tokens, nothing cached, 40 heads x 128,
+    # block 16, whole batch on the GPU in one launch; the oracle recomputes sampled rows (tile and
+    # block edges, the first and the last token) of three sequences and three heads row by row
+    w = wl.custom(1009, [4096] * 8, 40, 128, 16, name="prefill_8x4096")
+    news = [4096] * 8
+    out, q, qs, code = _run(w, news, cuda_device)
+    assert code == 0, pkv.DEV_CODES.get(code, code)
+    got = out.cpu().numpy().astype(np.float64)
+    qh = q.cpu().numpy().astype(np.float64)
+    rows = [0, 1, 63, 64, 127, 128, 255, 256, 1000, 2047, 2048, 4031, 4095]
+    for s in (0, 5, 7):
+        kc, vc, tabs, lens = w.compact_pools([s])
+        keys = oracle_attention.gather_sequence(kc.numpy(), tabs[0], int(lens[0]))
+        values = oracle_attention.gather_sequence(vc.numpy(), tabs[0], int(lens[0]))
+        for h in (0, 17, 39):
+            for i in rows:
+                ref = oracle_attention.contiguous_attention(qh[qs[s] + i, h][None], keys[: i + 1, h][:, None],
+                                                           values[: i + 1, h][:, None], w.scale)
+                err = float(np.max(np.abs(got[qs[s] + i, h] - ref.reshape(-1))))
+                assert err <= ATOL, (s, h, i, err)
