@@ -597,30 +597,41 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
     """Same step through the C ABI, with the step's inputs in pinned host memory.
 
     Every step copies q, the new keys/values, slot mapping, copy pairs, block
-    tables and context lengths host->device, runs the kernels, copies the
-    attention output back and waits for it (wall clock).
+    tables and context lengths host->device (packed in one pinned buffer, so one
+    copy), runs the kernels, copies the attention output back and waits for it
+    (wall clock).
     """
     import torch
     from paged_kv_cache_73_gb300 import binding as pkv
 
-    host = {
-        "q": q.cpu().pin_memory(), "key": key.cpu().pin_memory(), "value": value.cpu().pin_memory(),
-        "slots": torch.from_numpy(slots).pin_memory(),
-        "pairs": torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory(),
-        "tables": torch.from_numpy(w.block_tables).pin_memory(),
-        "lens": torch.from_numpy(w.context_lens).pin_memory(),
+    parts = {
+        "q": q.cpu(), "key": key.cpu(), "value": value.cpu(),
+        "slots": torch.from_numpy(slots),
+        "pairs": torch.from_numpy(np.ascontiguousarray(pairs)),
+        "tables": torch.from_numpy(w.block_tables),
+        "lens": torch.from_numpy(w.context_lens),
     }
-    dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    # one pinned byte buffer holding every input at a 256-byte-aligned offset, and its device twin
+    offs, total = {}, 0
+    for n, t in parts.items():
+        offs[n] = total
+        total += -(-(t.numel() * t.element_size()) // 256) * 256
+    host_buf = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    dbuf = {}
+    for n, t in parts.items():
+        nbytes = t.numel() * t.element_size()
+        host_buf[offs[n]:offs[n] + nbytes].copy_(t.contiguous().view(-1).view(torch.uint8))
+        dbuf[n] = dev_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
     out_h = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
     out_d = torch.empty_like(q)
     stream = torch.cuda.current_stream()
     n_pairs = int(pairs.shape[0])
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in parts.values())
     d2h = out_h.numel() * out_h.element_size()
 
     def step():
-        for n, t in host.items():
-            dbuf[n].copy_(t, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         if n_pairs:
             pkv.copy_blocks([k], [v], dbuf["pairs"], stream=stream)
         pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=stream)
