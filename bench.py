@@ -630,17 +630,39 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
     h2d = sum(t.numel() * t.element_size() for t in parts.values())
     d2h = out_h.numel() * out_h.element_size()
 
-    def step():
+    def body(st):
         dev_buf.copy_(host_buf, non_blocking=True)
         if n_pairs:
-            pkv.copy_blocks([k], [v], dbuf["pairs"], stream=stream)
-        pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=stream)
+            pkv.copy_blocks([k], [v], dbuf["pairs"], stream=st)
+        pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=st)
         pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, w.block_size, out=out_d,
-                                   workspace=ws, stream=stream)
+                                   workspace=ws, stream=st)
         out_h.copy_(out_d, non_blocking=True)
-        stream.synchronize()
 
     for _ in range(max(args.warmup, 3)):
+        body(stream)
+        stream.synchronize()
+    # the step as a CUDA graph, recorded once through the same API calls and replayed every step
+    # (what a serving loop does with a fixed-shape decode step); eager calls if capture fails
+    graph, how = None, "eager API calls"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        graph, how = g, "CUDA graph of the API calls, replayed"
+    except Exception as e:  # noqa: BLE001 - any capture failure falls back to the eager step
+        how = f"eager API calls (graph capture failed: {type(e).__name__})"
+        torch.cuda.synchronize()
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            body(stream)
+        stream.synchronize()
+
+    for _ in range(3):
         step()
     K = args.steps
     torch.cuda.synchronize()
@@ -648,7 +670,7 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
     for _ in range(K):
         step()
     dt = (time.perf_counter() - t0) / K
-    return {"e2e_step_ms": dt * 1e3, "h2d": h2d, "d2h": d2h}
+    return {"e2e_step_ms": dt * 1e3, "h2d": h2d, "d2h": d2h, "launch": how}
 
 
 def prepare_cpu_sample(w, seqs, slots, seed):
@@ -827,7 +849,7 @@ def main():
         if "e2e_step_ms" in r:
             line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                            "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                           "ms_per_step": e2e_ms}
+                           "ms_per_step": e2e_ms, "launch": r.get("launch", "eager API calls")}
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
