@@ -60,7 +60,9 @@ enum {
   PKV_DEV_BAD_SLOT = 3,         /* a slot >= num_blocks*block_size */
   PKV_DEV_BAD_COPY_PAIR = 4,    /* a copy pair with an id outside [0, num_blocks) */
   PKV_DEV_WAIT_TIMEOUT = 5,     /* a shared-memory copy did not complete in time */
-  PKV_DEV_BAD_QUERY_RANGE = 6   /* prefill: new tokens outside [0, context_len] or outside q */
+  PKV_DEV_BAD_QUERY_RANGE = 6,  /* prefill: new tokens outside [0, context_len] or outside q */
+  PKV_DEV_PREFIX_MISMATCH = 7   /* shared-prefix decode: a sequence's first prefix blocks differ
+                                   from its group's first sequence's, or a bad group layout */
 };
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
@@ -121,6 +123,47 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
                                int num_seqs, int num_heads, int head_dim, int num_blocks,
                                int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Paged decode attention for batches whose sequences share prefix blocks
+ * ([guide] 04: requests map their first logical blocks onto one cached
+ * prefix; [lecture] Parallel Sampling 场景 and Beam Search 场景: siblings share
+ * their prompt blocks).  Same result as pkv_paged_attention_decode (within its
+ * tolerance); the shared prefix is read once per group instead of once per
+ * sequence.
+ *
+ * Sequences [group_start[g], group_start[g+1]) form group g, whose members map
+ * their first prefix_lens[g] / block_size logical blocks onto the same physical
+ * blocks (the block manager's shared prefix or prompt).  For each group and
+ * head, the prefix part of every member's attention runs as one tensor-core
+ * product (queries of up to 256 members x the prefix keys, read through the
+ * group's first sequence's table row), giving a partial (max, sum, output) per
+ * sequence; the rest of each context [prefix_len, ctx) runs as in
+ * pkv_paged_attention_decode; a log-sum-exp merge combines the parts.
+ *
+ *   group_start    device [num_groups + 1] int32: 0 = group_start[0] <= ... <=
+ *                  group_start[num_groups] = num_seqs (the groups cover the batch)
+ *   prefix_lens    device [num_groups] int32: multiples of block_size, each at
+ *                  most the group's shortest context (0: no shared prefix)
+ *   max_group_size host: the largest group_start[g+1] - group_start[g] (sizes the
+ *                  grid; members past it are not processed)
+ *   workspace      at least pkv_paged_attention_shared_prefix_workspace_size(...)
+ *                  bytes, 16-byte aligned, required.
+ *   other arguments as for pkv_paged_attention_decode.
+ *
+ * A member whose first prefix blocks differ from the group's first sequence's,
+ * or a group layout that does not cover the batch, records
+ * PKV_DEV_PREFIX_MISMATCH (the prefix is then the first sequence's).
+ * ------------------------------------------------------------------------- */
+size_t pkv_paged_attention_shared_prefix_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                                        int max_blocks_per_seq, int block_size);
+
+int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             const int32_t* group_start, const int32_t* prefix_lens, int num_groups,
+                                             int max_group_size, int num_seqs, int num_heads, int head_dim,
+                                             int num_blocks, int max_blocks_per_seq, float scale, int block_size,
+                                             uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Paged prefill attention: the new tokens of each sequence (the task input)

@@ -27,7 +27,7 @@ PKV_ERR_DEVICE_CHECK = -6
 PKV_ERR_NOT_FOUND = -7
 
 DEV_CODES = {0: "ok", 1: "bad block id", 2: "bad context length", 3: "bad slot", 4: "bad copy pair",
-             5: "wait timeout", 6: "bad query range"}
+             5: "wait timeout", 6: "bad query range", 7: "shared prefix mismatch"}
 
 
 class PkvError(RuntimeError):
@@ -53,6 +53,9 @@ _SIGNATURES = {
     "pkv_paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_plan": (_I, [_I, _I, _I, _I, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I, _P, _P, _SZ, _P]),
+    "pkv_paged_attention_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                                      _c.c_float, _I, _P, _P, _SZ, _P]),
     "pkv_paged_attention_static_workspace_bytes": (_SZ, []),
     "pkv_paged_attention_decode_static_workspace": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I,
                                                          _P, _P]),
@@ -197,6 +200,49 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
         S, H, D, N, max_blocks, float(scale), block_size, out.data_ptr(), _ptr(workspace), ws_bytes,
         _stream(stream)))
+    return out
+
+
+def paged_attention_shared_prefix_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
+                                                 max_blocks_per_seq: int, block_size: int) -> int:
+    return int(load().pkv_paged_attention_shared_prefix_workspace_size(num_seqs, num_heads, head_dim,
+                                                                       max_blocks_per_seq, block_size))
+
+
+def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                         block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                         group_start: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
+                                         block_size: int, max_group_size: int, out: Optional[torch.Tensor] = None,
+                                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """As paged_attention_decode, for sequences grouped by a shared prefix (read once per group)."""
+    _need(q, "q", torch.float16, 3)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(group_start, "group_start", torch.int32, 1)
+    _need(prefix_lens, "prefix_lens", torch.int32, 1)
+    S, H, D = q.shape
+    N = k_cache.shape[0]
+    G = prefix_lens.shape[0]
+    if tuple(k_cache.shape) != (N, H, block_size, D) or v_cache.shape != k_cache.shape:
+        raise PkvError(PKV_ERR_INVALID_ARG, f"cache shape {tuple(k_cache.shape)} does not match "
+                                            f"[N, {H}, {block_size}, {D}]")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S or group_start.shape[0] != G + 1:
+        raise PkvError(PKV_ERR_INVALID_ARG, "block_tables / context_lens rows != num_seqs or group_start != groups + 1")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", torch.float16, 3)
+    max_blocks = block_tables.shape[1]
+    if workspace is None:
+        n = paged_attention_shared_prefix_workspace_size(S, H, D, max_blocks, block_size)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_attention_decode_shared_prefix(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+        group_start.data_ptr(), prefix_lens.data_ptr(), G, int(max_group_size), S, H, D, N, max_blocks,
+        float(scale), block_size, out.data_ptr(), _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

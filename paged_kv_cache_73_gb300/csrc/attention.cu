@@ -129,6 +129,13 @@ struct AttnParams {
   __half* out;
   float* ws_ml;  // [S, H, max_parts, 2] (m, l) in base-2 log domain
   float* ws_o;   // [S, H, max_parts, D] unnormalised partial outputs
+  // shared-prefix groups (null for plain decode): sequences [group_start[g], group_start[g+1])
+  // share their first prefix_lens[g] tokens; their partitions then cover tokens from
+  // prefix_lens[g] on, written from slot part_base = 1 (slot 0 holds the prefix partial)
+  const int32_t* group_start;
+  const int32_t* prefix_lens;
+  int num_groups;
+  int part_base;
   int num_heads;
   int num_blocks;
   int max_blocks;
@@ -138,10 +145,19 @@ struct AttnParams {
   float scale_log2;
 };
 
-// Number of partitions of a sequence; a bad or empty context has one (which writes zeros).
-__device__ __forceinline__ int num_parts(int ctx, int max_ctx, int part_tokens) {
-  if (ctx <= 0 || ctx > max_ctx) return 1;
-  return (ctx + part_tokens - 1) / part_tokens;
+// First token of sequence s's own range: 0 for plain decode, else its group's shared-prefix
+// length (binary search over the group starts; *first = the group's first sequence); -1 if s is
+// in no group.
+__device__ __forceinline__ int range_start(const AttnParams& p, int s, int* first = nullptr) {
+  if (p.group_start == nullptr) return 0;
+  int lo = 0, hi = p.num_groups;                       // find g with group_start[g] <= s < group_start[g+1]
+  if (p.group_start[0] > s || p.group_start[hi] <= s) return -1;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.group_start[mid] <= s) lo = mid; else hi = mid;
+  }
+  if (first) *first = p.group_start[lo];
+  return p.prefix_lens[lo];
 }
 
 // Sum of per-lane partial dots over the CPR lanes of a row, for NJ rows at once.
@@ -241,19 +257,50 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const int B = p.block_size;
   const int H = p.num_heads;
   const int max_ctx = p.max_blocks * B;
-  const int ctx = p.lens[s];
-  const int nparts = num_parts(ctx, max_ctx, p.part_tokens);
+  // this CTA's tokens: partition `part` of [start, ctx) (start = 0 unless a shared prefix precedes)
+  const int ctx_full = p.lens[s];
+  int first = s;
+  const int start = range_start(p, s, &first);
+  const bool bad_range = start < 0 || start % B != 0 || ctx_full <= start || ctx_full > max_ctx;
+  const int ctx = ctx_full - start;                    // tokens of the range
+  const int nparts = bad_range ? 1 : (ctx + p.part_tokens - 1) / p.part_tokens;
   if (part >= nparts) return;
   const size_t out_off = (static_cast<size_t>(s) * H + h) * D;
-  if (ctx <= 0 || ctx > max_ctx) {
-    if (ctx != 0 && tid == 0) record_error(PKV_DEV_BAD_CONTEXT_LEN);
-    for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
+  if (bad_range) {
+    // an empty range (ctx = 0, or a context that is exactly its shared prefix) is no error; a
+    // sequence in no group, a prefix that is not whole blocks or longer than the context is a
+    // bad group layout
+    if (tid == 0) {
+      if (ctx_full > max_ctx || (p.group_start == nullptr && ctx_full < 0))
+        record_error(PKV_DEV_BAD_CONTEXT_LEN);
+      else if (start < 0 || start % B != 0 || ctx_full < start)
+        record_error(PKV_DEV_PREFIX_MISMATCH);
+    }
+    if (p.part_base == 0) {
+      for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
+    } else {
+      const size_t w = (static_cast<size_t>(s) * H + h) * p.max_parts + p.part_base;
+      for (int d = tid; d < D; d += NW * 32) p.ws_o[w * D + d] = 0.f;
+      if (tid == 0) {
+        p.ws_ml[2 * w] = -INFINITY;
+        p.ws_ml[2 * w + 1] = 0.f;
+      }
+    }
     return;
   }
 
   const int chunks_per_block = B / R;
   const int chunks_per_part = p.part_tokens / R;
   const int total_chunks = (ctx + R - 1) / R;
+  const int block0 = start / B;                        // first block of the range
+  if (block0 > 0 && part == 0 && h == 0) {
+    // the shared prefix is read once, through the group's first sequence: the others must map
+    // their first blocks onto the same physical blocks
+    int differs = 0;
+    for (int j = tid; j < block0; j += NW * 32)
+      differs |= p.tables[static_cast<size_t>(s) * p.max_blocks + j] != p.tables[static_cast<size_t>(first) * p.max_blocks + j];
+    if (__syncthreads_or(differs) && tid == 0) record_error(PKV_DEV_PREFIX_MISMATCH);
+  }
   const int c_begin = part * chunks_per_part;
   const int n_chunks = min(chunks_per_part, total_chunks - c_begin);
 
@@ -263,7 +310,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     const int c = c_begin + i;
     const int j = c / chunks_per_block;
     const int sub = c - j * chunks_per_block;
-    const int phys = p.tables[static_cast<size_t>(s) * p.max_blocks + j];
+    const int phys = p.tables[static_cast<size_t>(s) * p.max_blocks + block0 + j];
     if (phys < 0 || phys >= p.num_blocks) {
       bad = 1;
       chunk_off[i] = 0;
@@ -278,10 +325,10 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
-    if (nparts == 1) {
+    if (nparts == 1 && p.part_base == 0) {
       for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
     } else {
-      const size_t w = (static_cast<size_t>(s) * H + h) * p.max_parts + part;
+      const size_t w = (static_cast<size_t>(s) * H + h) * p.max_parts + p.part_base + part;
       for (int d = tid; d < D; d += NW * 32) p.ws_o[w * D + d] = 0.f;
       if (tid == 0) {
         p.ws_ml[2 * w] = -INFINITY;
@@ -394,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     wgt[w] = exp2f(comb[w * (D + 2) + D] - M);
     L = fmaf(comb[w * (D + 2) + D + 1], wgt[w], L);
   }
-  if (nparts == 1) {
+  if (nparts == 1 && p.part_base == 0) {
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int d = tid; d < D; d += NW * 32) {
       float o = 0.f;
@@ -403,7 +450,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
       p.out[out_off + d] = __float2half_rn(o * inv);
     }
   } else {
-    const size_t w0 = (static_cast<size_t>(s) * H + h) * p.max_parts + part;
+    const size_t w0 = (static_cast<size_t>(s) * H + h) * p.max_parts + p.part_base + part;
     for (int d = tid; d < D; d += NW * 32) {
       float o = 0.f;
 #pragma unroll
@@ -427,7 +474,11 @@ __global__ void __launch_bounds__(128) paged_attention_merge_kernel(const AttnPa
   const int h = blockIdx.x * 4 + warp, s = blockIdx.y;
   if (h >= p.num_heads) return;
   const int ctx = p.lens[s];
-  const int nparts = num_parts(ctx, p.max_blocks * p.block_size, p.part_tokens);
+  const int start = range_start(p, s);
+  const int max_ctx = p.max_blocks * p.block_size;
+  const bool bad_range = start < 0 || start % p.block_size != 0 || ctx <= start || ctx > max_ctx;
+  // slots: the shared-prefix partial (if any) and the partitions of [start, ctx)
+  const int nparts = p.part_base + (bad_range ? 1 : (ctx - start + p.part_tokens - 1) / p.part_tokens);
   if (nparts <= 1) return;
   const size_t w0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_parts;
   float M = -INFINITY;
@@ -530,7 +581,7 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention setup: %s", cudaGetErrorString(e));
   const int max_ctx = p.max_blocks * p.block_size;
   p.part_tokens = part_tokens;
-  p.max_parts = (max_ctx + part_tokens - 1) / part_tokens;
+  p.max_parts = (max_ctx + part_tokens - 1) / part_tokens + p.part_base;
   if (p.max_parts > 1) {
     const size_t pairs = static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts;
     const size_t need = (ws_ml_floats(pairs) + pairs * D) * sizeof(float);
@@ -650,6 +701,100 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc;
   // chunk rows R = min(B, 16): a block of 32 rows is read as two chunks
+  if (head_dim == 128) {
+    rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
+         : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                           : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  } else {
+    rc = block_size == 4   ? launch<64, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
+         : block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                           : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  }
+  if (rc == PKV_OK) pkv::clear_error();
+  return rc;
+}
+
+size_t pkv_paged_attention_shared_prefix_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                                        int max_blocks_per_seq, int block_size) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0) return 0;
+  const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+  const long long parts = (max_ctx + kMinPartTokens - 1) / kMinPartTokens + 1;   // + the prefix slot
+  const size_t pairs = static_cast<size_t>(num_seqs) * num_heads * parts;
+  return (ws_ml_floats(pairs) + pairs * head_dim) * sizeof(float);
+}
+
+int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             const int32_t* group_start, const int32_t* prefix_lens, int num_groups,
+                                             int max_group_size, int num_seqs, int num_heads, int head_dim,
+                                             int num_blocks, int max_blocks_per_seq, float scale, int block_size,
+                                             uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || num_groups <= 0 ||
+      max_group_size <= 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG,
+                     "pkv_paged_attention_decode_shared_prefix: num_seqs=%d num_heads=%d num_blocks=%d "
+                     "max_blocks_per_seq=%d num_groups=%d max_group_size=%d",
+                     num_seqs, num_heads, num_blocks, max_blocks_per_seq, num_groups, max_group_size);
+  if (head_dim != 64 && head_dim != 128)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode_shared_prefix: head_dim %d not in {64, 128}",
+                     head_dim);
+  if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED,
+                     "pkv_paged_attention_decode_shared_prefix: block_size %d not in {4, 8, 16, 32}", block_size);
+  if (num_seqs == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (num_seqs > 65535 || num_heads > 65535 || num_groups > 65535)
+    return pkv::fail(PKV_ERR_UNSUPPORTED,
+                     "pkv_paged_attention_decode_shared_prefix: num_seqs/num_heads/num_groups above 65535");
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > (1LL << 30))
+    return pkv::fail(PKV_ERR_UNSUPPORTED,
+                     "pkv_paged_attention_decode_shared_prefix: context capacity above 2^30 tokens");
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !group_start || !prefix_lens || !out ||
+      !workspace)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode_shared_prefix: null pointer");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+    return pkv::fail(PKV_ERR_INVALID_ARG,
+                     "pkv_paged_attention_decode_shared_prefix: q, caches, out, workspace must be 16-byte aligned");
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode_shared_prefix: scale must be finite and positive");
+
+  AttnParams p{};
+  p.q = reinterpret_cast<const __half*>(q);
+  p.k = reinterpret_cast<const __half*>(k_cache);
+  p.v = reinterpret_cast<const __half*>(v_cache);
+  p.tables = block_tables;
+  p.lens = context_lens;
+  p.out = reinterpret_cast<__half*>(out);
+  p.num_heads = num_heads;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = block_size;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.group_start = group_start;
+  p.prefix_lens = prefix_lens;
+  p.num_groups = num_groups;
+  p.part_base = 1;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const int max_ctx = max_blocks_per_seq * block_size;
+  const int pt = choose_part_tokens(num_seqs, num_heads, max_ctx, device_sms(dev));
+  const int max_parts = (max_ctx + pt - 1) / pt + 1;
+  const size_t pairs = static_cast<size_t>(num_seqs) * num_heads * max_parts;
+  const size_t need = (ws_ml_floats(pairs) + pairs * head_dim) * sizeof(float);
+  if (workspace_bytes < need)
+    return pkv::fail(PKV_ERR_WORKSPACE, "pkv_paged_attention_decode_shared_prefix: workspace of %zu bytes needed, %zu given",
+                     need, workspace_bytes);
+  float* ws_ml = static_cast<float*>(workspace);
+  float* ws_o = ws_ml + ws_ml_floats(pairs);
+  // 1. the prefix partials (slot 0), 2. the partitions of each [prefix_len, ctx) and 3. the merge
+  int rc = pkv::launch_prefix_partials(q, k_cache, v_cache, block_tables, group_start, prefix_lens, num_groups,
+                                       max_group_size, num_seqs, num_heads, head_dim, num_blocks, max_blocks_per_seq,
+                                       scale, block_size, ws_ml, ws_o, max_parts, stream);
+  if (rc != PKV_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (head_dim == 128) {
     rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
          : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)

@@ -24,4 +24,15 @@ int read_device_error_attention(int reset, int* code);
 int read_device_error_cache_ops(int reset, int* code);
 int read_device_error_prefill(int reset, int* code);
 
+// Shared-prefix partials (prefill.cu, tensor cores): for every member s of every group g and every
+// head h, the partial (max m and sum l in the base-2 log domain of scale * q.k, unnormalised
+// output o) of q[s, h] over the keys [0, prefix_lens[g]) read through block_tables row
+// group_start[g], written to slot 0 of the decode workspace: ws_ml[2 w], ws_ml[2 w + 1], ws_o[w D ..]
+// with w = (s * num_heads + h) * max_parts.  Validates nothing the caller checked already.
+int launch_prefix_partials(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                           const int32_t* block_tables, const int32_t* group_start, const int32_t* prefix_lens,
+                           int num_groups, int max_group_size, int num_seqs, int num_heads, int head_dim,
+                           int num_blocks, int max_blocks_per_seq, float scale, int block_size, float* ws_ml,
+                           float* ws_o, int max_parts, void* stream);
+
 }  // namespace pkv

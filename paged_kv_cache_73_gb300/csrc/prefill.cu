@@ -54,6 +54,14 @@ struct PrefillParams {
   int log2_block;
   int total_q;
   int use_tma;
+  // shared-prefix partials (PARTIAL kernels only): blockIdx.z is a group of sequences
+  // [group_start[g], group_start[g+1]) (the query rows) sharing keys [0, prefix_lens[g]); each
+  // row's (m, l, o) goes to slot 0 of the decode workspace
+  const int32_t* group_start;
+  const int32_t* prefix_lens;
+  float* ws_ml;
+  float* ws_o;
+  int max_parts;
   float scale_log2;
 };
 
@@ -300,7 +308,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 constexpr int TC_QTILES = 2;
 constexpr int TC_THREADS = 384;
 
-template <int D>
+// PARTIAL = false: prefill (rows = a sequence's new tokens, causal, normalised fp16 output).
+// PARTIAL = true: shared-prefix partials (rows = the members of a group, every row sees every
+// prefix key, unnormalised fp32 (m, l, o) into the decode workspace).
+template <int D, bool PARTIAL>
 __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   using C = TcCfg<D>;
   constexpr int CPR = D / 8;                                  // 16-byte chunks per row
@@ -336,18 +347,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   const int H = p.num_heads;
   const int lb = p.log2_block;
   const int B = 1 << lb;
-  const int ctx = p.lens[s];
-  const int q0 = p.qstart[s];
-  const int n = p.qstart[s + 1] - q0;
   const int i0 = qt * TC_QTILES * TC_BM;
-  if (n < 0 || n > ctx || ctx > p.max_blocks * B || q0 < 0 || q0 + n > p.total_q) {
-    if (tid == 0 && qt == 0) record_error(ctx > p.max_blocks * B ? PKV_DEV_BAD_CONTEXT_LEN : PKV_DEV_BAD_QUERY_RANGE);
-    return;
+  // keys [0, ctx) through table row `trow`; query rows q0 + i0 + r, r < n - i0
+  int ctx, q0, n, trow;
+  if constexpr (PARTIAL) {
+    q0 = p.group_start[s];
+    n = p.group_start[s + 1] - q0;
+    ctx = p.prefix_lens[s];
+    trow = q0;
+    if (q0 < 0 || n < 0 || q0 + n > p.total_q || ctx < 0 || ctx > p.max_blocks * B || (ctx & (B - 1)) != 0) {
+      if (tid == 0 && qt == 0 && h == 0) record_error(PKV_DEV_PREFIX_MISMATCH);
+      return;
+    }
+    if (i0 >= n) return;
+    if (ctx == 0) {
+      // no shared prefix: an empty partial for every row
+      if (tid < TC_QTILES * TC_BM && i0 + tid < n) {
+        const size_t w = (static_cast<size_t>(q0 + i0 + tid) * H + h) * p.max_parts;
+        p.ws_ml[2 * w] = -INFINITY;
+        p.ws_ml[2 * w + 1] = 0.f;
+        for (int d = 0; d < D; d += 4) *reinterpret_cast<float4*>(p.ws_o + w * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      return;
+    }
+  } else {
+    ctx = p.lens[s];
+    q0 = p.qstart[s];
+    n = p.qstart[s + 1] - q0;
+    trow = s;
+    if (n < 0 || n > ctx || ctx > p.max_blocks * B || q0 < 0 || q0 + n > p.total_q) {
+      if (tid == 0 && qt == 0) record_error(ctx > p.max_blocks * B ? PKV_DEV_BAD_CONTEXT_LEN : PKV_DEV_BAD_QUERY_RANGE);
+      return;
+    }
+    if (i0 >= n) return;
   }
-  if (i0 >= n) return;
   const int ntile_q = i0 + TC_BM < n ? 2 : 1;                 // query tiles with real tokens
-  const int first_pos = ctx - n + i0;
-  const int last_pos = ctx - n + min(i0 + TC_QTILES * TC_BM, n) - 1;
+  // positions of the first and last query rows (every partial row sits after the whole prefix)
+  const int first_pos = PARTIAL ? ctx - 1 : ctx - n + i0;
+  const int last_pos = PARTIAL ? ctx - 1 : ctx - n + min(i0 + TC_QTILES * TC_BM, n) - 1;
   const int n_tiles = last_pos / TC_BN + 1;
 
   if (warp == 0) {
@@ -395,14 +432,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   };
   int bad = 0;
   bool failed = false;
-  float l = 0.f;
+  float l = 0.f, m_ref = -INFINITY;
 
   if (warp == 9 || warp == 10) {
     // ---------------- loads: warp 9 gathers K tiles, warp 10 V tiles ----------------
     const bool is_k = warp == 9;
     const __half* pool = is_k ? p.k : p.v;
     const CUtensorMap* map = is_k ? &p.tmap_k : &p.tmap_v;
-    const int32_t* table = p.tables + static_cast<size_t>(s) * p.max_blocks;
+    const int32_t* table = p.tables + static_cast<size_t>(trow) * p.max_blocks;
     constexpr int ROWS = 32 / CPR;                            // rows per warp-wide cp.async
     const int c = lane % CPR, rsub = lane / CPR;              // this lane's chunk and row offset
     const int nb = TC_BN >> lb;                               // blocks per tile (2..16)
@@ -550,9 +587,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t to = t_o(g);
     const int row_i = i0 + tid;                        // tid = g * 128 + row within the tile
-    const int pos = ctx - n + row_i;
-    const int tile_first = first_pos + g * TC_BM;      // position of the tile's first token
-    float m_ref = -INFINITY;
+    const int pos = PARTIAL ? ctx - 1 : ctx - n + row_i;
+    const int tile_first = PARTIAL ? ctx - 1 : first_pos + g * TC_BM;   // the tile's first token
     for (int j = 0; j < n_tiles; ++j) {
       // decisions stay warp-uniform: the tcgen05.ld/st below are warp-collective
       const int u = j & 1;
@@ -640,7 +676,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   // ---------------- epilogue (all warps) ----------------
   bad = __syncthreads_or(bad);
   const bool aborted = *abort_flag != 0;
-  if (warp < 4 * ntile_q && !aborted && !bad) {
+  if (PARTIAL && warp < 4 * ntile_q) {
+    // each member's partial straight from tensor memory (every lane loads: tcgen05.ld is
+    // warp-collective): m and l in the base-2 log domain, o unnormalised; an empty partial if a
+    // block id was bad or a role gave up
+    const int g = warp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool ok = !aborted && !bad;
+    const bool row_ok = i0 + tid < n;
+    const size_t w = (static_cast<size_t>(q0 + i0 + min(tid, n - 1 - i0)) * H + h) * p.max_parts;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      float o[32];
+      tmem_ld32(t_o(g) + lane_off + c * 32, o);
+      if (row_ok) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(p.ws_o + w * D + c * 32 + e) =
+              ok ? make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (row_ok) {
+      p.ws_ml[2 * w] = ok ? m_ref : -INFINITY;
+      p.ws_ml[2 * w + 1] = ok ? l : 0.f;
+    }
+  } else if (!PARTIAL && warp < 4 * ntile_q && !aborted && !bad) {
     // Each thread normalises its O row (every lane loads: tcgen05.ld is warp-collective) and
     // stages it in the K/V ring, free now that every MMA is done, as 16-byte chunks XOR-ed with
     // the row's low bits (no bank conflicts either way).  The warp then writes its 32 rows back
@@ -690,7 +750,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
   }
 }
 
-template <int D>
+template <int D, bool PARTIAL>
 int launch_prefill(const PrefillParams& p, int num_seqs, int max_query_len, cudaStream_t st) {
   static std::mutex mu;
   static bool done[64] = {false};
@@ -699,14 +759,14 @@ int launch_prefill(const PrefillParams& p, int num_seqs, int max_query_len, cuda
   if (e == cudaSuccess) {
     std::lock_guard<std::mutex> g(mu);
     if (dev < 0 || dev >= 64 || !done[dev]) {
-      e = cudaFuncSetAttribute(paged_prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(paged_prefill_tc_kernel<D, PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                TcCfg<D>::SMEM);
       if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     }
   }
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill setup: %s", cudaGetErrorString(e));
   dim3 grid((max_query_len + TC_QTILES * TC_BM - 1) / (TC_QTILES * TC_BM), p.num_heads, num_seqs);
-  e = pkv::launch_pdl(paged_prefill_tc_kernel<D>, grid, dim3(TC_THREADS), TcCfg<D>::SMEM, st, p);
+  e = pkv::launch_pdl(paged_prefill_tc_kernel<D, PARTIAL>, grid, dim3(TC_THREADS), TcCfg<D>::SMEM, st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged prefill launch: %s", cudaGetErrorString(e));
   return PKV_OK;
@@ -842,10 +902,49 @@ int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, cons
     if (rc != PKV_OK) return rc;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int rc = head_dim == 128 ? launch_prefill<128>(p, num_seqs, max_query_len, st)
-                                 : launch_prefill<64>(p, num_seqs, max_query_len, st);
+  const int rc = head_dim == 128 ? launch_prefill<128, false>(p, num_seqs, max_query_len, st)
+                                 : launch_prefill<64, false>(p, num_seqs, max_query_len, st);
   if (rc == PKV_OK) pkv::clear_error();
   return rc;
 }
 
 }  // extern "C"
+
+namespace pkv {
+int launch_prefix_partials(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                           const int32_t* block_tables, const int32_t* group_start, const int32_t* prefix_lens,
+                           int num_groups, int max_group_size, int num_seqs, int num_heads, int head_dim,
+                           int num_blocks, int max_blocks_per_seq, float scale, int block_size, float* ws_ml,
+                           float* ws_o, int max_parts, void* stream) {
+  PrefillParams p{};
+  p.q = reinterpret_cast<const __half*>(q);
+  p.k = reinterpret_cast<const __half*>(k_cache);
+  p.v = reinterpret_cast<const __half*>(v_cache);
+  p.tables = block_tables;
+  p.group_start = group_start;
+  p.prefix_lens = prefix_lens;
+  p.ws_ml = ws_ml;
+  p.ws_o = ws_o;
+  p.max_parts = max_parts;
+  p.num_heads = num_heads;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  int lb = 0;
+  while ((1 << lb) < block_size) ++lb;
+  p.log2_block = lb;
+  p.total_q = num_seqs;                                // q [num_seqs][H][D]: one row per sequence
+  p.scale_log2 = scale * 1.4426950408889634f;
+  int rc = encode_q_map(&p.tmap_q, q, head_dim, num_heads, num_seqs);
+  if (rc != PKV_OK) return rc;
+  p.use_tma = block_size >= 8 ? 1 : 0;
+  if (p.use_tma) {
+    rc = encode_pool_map(&p.tmap_k, k_cache, head_dim, num_heads, block_size, num_blocks);
+    if (rc == PKV_OK) rc = encode_pool_map(&p.tmap_v, v_cache, head_dim, num_heads, block_size, num_blocks);
+    if (rc != PKV_OK) return rc;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // grid: (256-member query tiles, heads, groups)
+  return head_dim == 128 ? launch_prefill<128, true>(p, num_groups, max_group_size, st)
+                         : launch_prefill<64, true>(p, num_groups, max_group_size, st);
+}
+}  // namespace pkv
