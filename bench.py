@@ -77,6 +77,9 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop (profiling runs)")
+    ap.add_argument("--grouped", action="store_true",
+                    help="read each shared prefix once per group of sequences (shared-prefix decode entry); "
+                         "groups come from the block manager's shared leading blocks")
     ap.add_argument("--workload", choices=WORKLOADS + AUX_WORKLOADS, default="opt13b",
                     help="opt13b (the headline batch) or another decode batch of the same shape family")
     ap.add_argument("--capacity-seqs", type=int, default=64, help="capacity workload: sequences (ctx 2048 each)")
@@ -178,6 +181,27 @@ def attention_algorithmic_bytes(w) -> int:
         c = int(c)
         total += H * (2 * c * D * 2 + 2 * D * 2) + 4 * math.ceil(c / B) + 4
     return total
+
+
+def shared_prefix_groups(tables, lens, B):
+    """Groups of consecutive sequences whose leading blocks are the same physical blocks (the block
+    manager's shared prompt or prefix) and each group's shared whole-block prefix length."""
+    S = len(lens)
+    starts, prefixes = [0], []
+    s = 0
+    while s < S:
+        e = s + 1
+        while e < S and tables[e, 0] == tables[s, 0]:
+            e += 1
+        nb = 0
+        if e - s > 1:
+            cap = min(int(lens[i]) for i in range(s, e)) // B      # blocks full in every member
+            while nb < cap and all(tables[i, nb] == tables[s, nb] for i in range(s + 1, e)):
+                nb += 1
+        prefixes.append(nb * B)
+        starts.append(e)
+        s = e
+    return np.array(starts, dtype=np.int32), np.array(prefixes, dtype=np.int32)
 
 
 def _grow(bm, seqs, targets):
@@ -332,6 +356,22 @@ def run_gpu(args, rank, world, dev):
     part_tokens, attn_kernels = pkv.paged_attention_plan(S, H, D, MB, B)
     stream = torch.cuda.current_stream()
     n_pairs = int(pairs.shape[0])
+    grouped = None
+    if args.grouped:
+        gs_h, pl_h = shared_prefix_groups(w.block_tables, w.context_lens, B)
+        n_ws = pkv.paged_attention_shared_prefix_workspace_size(S, H, D, MB, B)
+        grouped = {"gs": torch.from_numpy(gs_h).to(dev), "pl": torch.from_numpy(pl_h).to(dev),
+                   "max_group": int(np.max(np.diff(gs_h))), "groups": int(len(pl_h)),
+                   "prefix_tokens": int(pl_h.sum()), "gs_h": gs_h, "pl_h": pl_h}
+        ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device=dev)
+        attn_kernels = 3                                 # prefix partials, partitions, merge
+
+    def attention(qq, tt, ll, st):
+        if grouped is None:
+            pkv.paged_attention_decode(qq, k, v, tt, ll, w.scale, B, out=out, workspace=ws, stream=st)
+        else:
+            pkv.paged_attention_decode_shared_prefix(qq, k, v, tt, ll, grouped["gs"], grouped["pl"], w.scale, B,
+                                                     grouped["max_group"], out=out, workspace=ws, stream=st)
 
     copy = None
     if len(x["setup_pairs"]):
@@ -355,7 +395,7 @@ def run_gpu(args, rank, world, dev):
         pkv.reshape_and_cache(key, value, k, v, slots_d, stream=stream)
         if ev0 is not None:
             ev0.record(stream)
-        pkv.paged_attention_decode(q, k, v, tables, lens, w.scale, B, out=out, workspace=ws, stream=stream)
+        attention(q, tables, lens, stream)
         if ev1 is not None:
             ev1.record(stream)
 
@@ -389,12 +429,16 @@ def run_gpu(args, rank, world, dev):
 
     res = {"step_ms": step_ms, "attn_ms": sum(attn_ms) / len(attn_ms), "attn_ms_median": statistics.median(attn_ms),
            "kv_bytes": w.logical_kv_bytes(), "phys_bytes": w.physical_kv_bytes(),
-           "attn_bytes": attention_algorithmic_bytes(w), "num_seqs": S,
+           # grouped: each shared prefix is read once, so the call's bytes are the distinct slots
+           "attn_bytes": attention_algorithmic_bytes(w) if grouped is None
+           else w.physical_kv_bytes() + S * H * D * 2 * 2,
+           "grouped": None if grouped is None else {k_: grouped[k_] for k_ in ("groups", "max_group", "prefix_tokens")},
+           "num_seqs": S,
            "launches": K * ((1 if n_pairs else 0) + 1 + attn_kernels), "part_tokens": part_tokens,
            "host_slot_us": x["host_us"], "clocks": clocks.summary(), "n_pairs": n_pairs, "copy": copy,
            "desc": x["desc"], "num_blocks": w.num_blocks}
     if not args.no_e2e:
-        res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws))
+        res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped))
     return res
 
 
@@ -593,7 +637,7 @@ def physical_gpu_index(local: int) -> int:
     return local
 
 
-def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
+def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None):
     """Same step through the C ABI, with the step's inputs in pinned host memory.
 
     Every step copies q, the new keys/values, slot mapping, copy pairs, block
@@ -611,6 +655,9 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
         "tables": torch.from_numpy(w.block_tables),
         "lens": torch.from_numpy(w.context_lens),
     }
+    if grouped is not None:
+        parts["gs"] = torch.from_numpy(grouped["gs_h"])
+        parts["pl"] = torch.from_numpy(grouped["pl_h"])
     # one pinned byte buffer holding every input at a 256-byte-aligned offset, and its device twin
     offs, total = {}, 0
     for n, t in parts.items():
@@ -635,8 +682,13 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws):
         if n_pairs:
             pkv.copy_blocks([k], [v], dbuf["pairs"], stream=st)
         pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=st)
-        pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, w.block_size, out=out_d,
-                                   workspace=ws, stream=st)
+        if grouped is None:
+            pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, w.block_size,
+                                       out=out_d, workspace=ws, stream=st)
+        else:
+            pkv.paged_attention_decode_shared_prefix(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], dbuf["gs"],
+                                                     dbuf["pl"], w.scale, w.block_size, grouped["max_group"],
+                                                     out=out_d, workspace=ws, stream=st)
         out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(max(args.warmup, 3)):
@@ -820,7 +872,7 @@ def main():
     if rank == 0:
         peak, peak_src = measured_hbm_peak()
         achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
-        traffic = NCU_TRAFFIC.get((args.workload, attention_source_sha()))
+        traffic = None if args.grouped else NCU_TRAFFIC.get((args.workload, attention_source_sha()))
         value = kv_total / (step_ms * 1e-3) / 1e9
         S = r["num_seqs"]
         line = {
@@ -836,7 +888,10 @@ def main():
             "tokens_per_s": S * world / (step_ms * 1e-3),
             "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
             "host_slot_assignment_us": r["host_slot_us"],
-            "roofline": {"bound": "hbm", "kernel": "paged attention call (partition + merge kernels)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "paged attention call (partition + merge kernels)" if r["grouped"] is None
+                         else "shared-prefix attention call (prefix partials on tensor cores + partition + merge); "
+                              "bytes = distinct K/V slots + q + out",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
                          "launch_ms": attn_ms, "timed_launches": (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
@@ -846,6 +901,8 @@ def main():
         }
         if r["copy"] is not None:
             line["copy_blocks_setup"] = r["copy"]
+        if r["grouped"] is not None:
+            line["grouped"] = r["grouped"]
         if "e2e_step_ms" in r:
             line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                            "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],

@@ -151,9 +151,13 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
  *                  bytes, 16-byte aligned, required.
  *   other arguments as for pkv_paged_attention_decode.
  *
- * A member whose first prefix blocks differ from the group's first sequence's,
- * or a group layout that does not cover the batch, records
- * PKV_DEV_PREFIX_MISMATCH (the prefix is then the first sequence's).
+ * Groups of fewer than 8 members read their prefix per sequence, as plain
+ * decode does (a shared block then mostly comes from L2, and the product's
+ * 128-row tile would be nearly empty); if no group reaches 8 members the call
+ * is pkv_paged_attention_decode.  A member of a larger group whose first prefix
+ * blocks differ from the group's first sequence's, or a group layout that does
+ * not cover the batch, records PKV_DEV_PREFIX_MISMATCH (the prefix is then the
+ * first sequence's).
  * ------------------------------------------------------------------------- */
 size_t pkv_paged_attention_shared_prefix_workspace_size(int num_seqs, int num_heads, int head_dim,
                                                         int max_blocks_per_seq, int block_size);

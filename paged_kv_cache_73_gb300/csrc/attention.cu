@@ -157,6 +157,7 @@ __device__ __forceinline__ int range_start(const AttnParams& p, int s, int* firs
     if (p.group_start[mid] <= s) lo = mid; else hi = mid;
   }
   if (first) *first = p.group_start[lo];
+  if (p.group_start[lo + 1] - p.group_start[lo] < pkv::kMinSharedGroup) return 0;   // small group: no cascade
   return p.prefix_lens[lo];
 }
 
@@ -787,6 +788,10 @@ int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* 
   if (workspace_bytes < need)
     return pkv::fail(PKV_ERR_WORKSPACE, "pkv_paged_attention_decode_shared_prefix: workspace of %zu bytes needed, %zu given",
                      need, workspace_bytes);
+  if (max_group_size < pkv::kMinSharedGroup)        // every group is small: plain decode
+    return pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads, head_dim,
+                                      num_blocks, max_blocks_per_seq, scale, block_size, out, workspace,
+                                      workspace_bytes, stream);
   float* ws_ml = static_cast<float*>(workspace);
   float* ws_o = ws_ml + ws_ml_floats(pairs);
   // 1. the prefix partials (slot 0), 2. the partitions of each [prefix_len, ctx) and 3. the merge

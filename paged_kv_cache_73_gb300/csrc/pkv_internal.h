@@ -24,6 +24,12 @@ int read_device_error_attention(int reset, int* code);
 int read_device_error_cache_ops(int reset, int* code);
 int read_device_error_prefill(int reset, int* code);
 
+// Shared-prefix decode reads a group's prefix once only for groups of at least this many members;
+// smaller groups (where the prefix mostly comes from L2 anyway and a 128-row tensor-core tile would
+// be nearly empty) run their whole context through the split-K decode kernel.  Measured on a
+// 1024-token prefix: 4 members break even, 8 are 1.4x faster, 64 are 1.9x.
+constexpr int kMinSharedGroup = 8;
+
 // Shared-prefix partials (prefill.cu, tensor cores): for every member s of every group g and every
 // head h, the partial (max m and sum l in the base-2 log domain of scale * q.k, unnormalised
 // output o) of q[s, h] over the keys [0, prefix_lens[g]) read through block_tables row

@@ -360,8 +360,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       return;
     }
     if (i0 >= n) return;
-    if (ctx == 0) {
-      // no shared prefix: an empty partial for every row
+    if (ctx == 0 || n < pkv::kMinSharedGroup) {
+      // no shared prefix, or a group too small to share it (its members read their whole context
+      // in the split-K decode): an empty partial for every row
       if (tid < TC_QTILES * TC_BM && i0 + tid < n) {
         const size_t w = (static_cast<size_t>(q0 + i0 + tid) * H + h) * p.max_parts;
         p.ws_ml[2 * w] = -INFINITY;

@@ -65,8 +65,9 @@ def test_shared_prefix_full_size(cuda_device):
 
 @pytest.mark.parametrize("prompt_len,shared", [(512, 512), (511, 496)])
 def test_parallel_sampling_groups(cuda_device, prompt_len, shared):
-    # 32 prompts x 4 samples (prompt-major): groups of 4 share the prompt's whole blocks; with a
-    # 511-token prompt the partly filled last block was copied on write, so 31 blocks are shared
+    # 32 prompts x 4 samples (prompt-major): groups of 4 share the prompt's whole blocks (with a
+    # 511-token prompt the partly filled last block was copied on write, so 31 blocks are shared);
+    # groups this small are read per sequence, so the call is plain decode
     w = wl.parallel_sampling(prompt_len=prompt_len)
     groups = list(range(0, w.num_seqs + 1, 4))
     out, plain, q, code = _run(w, groups, [shared] * (len(groups) - 1), cuda_device)
@@ -76,10 +77,11 @@ def test_parallel_sampling_groups(cuda_device, prompt_len, shared):
 
 
 def _grouped(D, B, seed):
-    # groups [0, 3) prefix 64, [3, 4) no prefix, [4, 8) prefix 96 (member 5's context is exactly its
-    # prefix), [8, 9) prefix 32: members map their first blocks onto the group's first sequence's
-    lens = [300, 70, 129, 17, 200, 96, 97, 160, 33]
-    groups, prefixes = [0, 3, 4, 8, 9], [64, 0, 96, 32]
+    # groups [0, 9) prefix 64, [9, 10) no prefix, [10, 18) prefix 96 (member 11's context is exactly
+    # its prefix), [18, 20) prefix 32 (fewer than 8 members: read per sequence): members map their
+    # first blocks onto the group's first sequence's
+    lens = [300, 70, 129, 65, 200, 96, 97, 160, 64, 17, 200, 96, 97, 160, 400, 129, 250, 111, 33, 40]
+    groups, prefixes = [0, 9, 10, 18, 20], [64, 0, 96, 32]
     base = wl.custom(seed, lens, num_heads=3, head_dim=D, block_size=B)
     tables = base.block_tables.copy()
     for g in range(len(prefixes)):
@@ -100,17 +102,17 @@ def test_groups_every_shape(cuda_device, D, B):
 
 
 def test_prefix_mismatch_recorded(cuda_device):
-    # member 2 of group [0, 3) maps its first block elsewhere: the kernel reads the prefix through
+    # member 2 of group [0, 9) maps its first block elsewhere: the kernel reads the prefix through
     # member 0's row and records the mismatch
     w, groups, prefixes = _grouped(128, 16, 611)
     tables = w.block_tables.copy()
-    tables[2, 0] = tables[8, 1]
+    tables[2, 0] = tables[19, 1]
     out, plain, q, code = _run(w, groups, prefixes, cuda_device, tables=tables)
     assert code == 7
 
 
 def test_groups_not_covering_the_batch_recorded(cuda_device):
     w, groups, prefixes = _grouped(64, 8, 612)
-    out, plain, q, code = _run(w, groups[:-1], prefixes[:-1], cuda_device)   # sequence 8 in no group
+    out, plain, q, code = _run(w, groups[:-1], prefixes[:-1], cuda_device)   # 18, 19 in no group
     assert code == 7
-    _check(w, out, q, list(range(8)))
+    _check(w, out, q, list(range(18)))
