@@ -574,8 +574,10 @@ int choose_part_tokens(int num_seqs, int num_heads, int max_ctx, int sms) {
   return kMinPartTokens;
 }
 
+// join: if not null, the merge waits for this event (the shared-prefix product on a side stream).
 template <int D, int R>
-int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* ws, cudaStream_t st) {
+int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* ws, cudaStream_t st,
+           cudaEvent_t join = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = prepare_kernel<D, R>(dev);
@@ -598,6 +600,10 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
   if (p.max_parts > 1) {
+    if (join != nullptr) {
+      e = cudaStreamWaitEvent(st, join, 0);
+      if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention join: %s", cudaGetErrorString(e));
+    }
     e = pkv::launch_pdl(paged_attention_merge_kernel<D>, dim3((p.num_heads + 3) / 4, num_seqs), dim3(128), 0, st,
                         p);
     if (e == cudaSuccess) e = cudaGetLastError();
@@ -607,6 +613,36 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Per device: a non-blocking side stream and fork/join events for the shared-prefix product, which
+// needs nothing from the split-K partitions and so runs beside them (a few dozen CTAs next to
+// thousands).  Callers of the shared-prefix entry hold side_mutex() while they enqueue, so two host
+// threads never interleave records and waits on the same events.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex& side_mutex() {
+  static std::mutex mu;
+  return mu;
+}
+// Under side_mutex(): the device's side stream, created on first use.
+int side_stream(int dev, SideStream** out) {
+  static SideStream side[64];
+  if (dev < 0 || dev >= 64) return pkv::fail(PKV_ERR_UNSUPPORTED, "shared-prefix attention: device ordinal %d above 63", dev);
+  SideStream& sd = side[dev];
+  if (sd.stream == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      sd = SideStream{};
+      return pkv::fail(PKV_ERR_CUDA, "shared-prefix attention: side stream: %s", cudaGetErrorString(e));
+    }
+  }
+  *out = &sd;
+  return PKV_OK;
+}
 
 }  // namespace
 
@@ -794,21 +830,37 @@ int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* 
                                       workspace_bytes, stream);
   float* ws_ml = static_cast<float*>(workspace);
   float* ws_o = ws_ml + ws_ml_floats(pairs);
-  // 1. the prefix partials (slot 0), 2. the partitions of each [prefix_len, ctx) and 3. the merge
-  int rc = pkv::launch_prefix_partials(q, k_cache, v_cache, block_tables, group_start, prefix_lens, num_groups,
-                                       max_group_size, num_seqs, num_heads, head_dim, num_blocks, max_blocks_per_seq,
-                                       scale, block_size, ws_ml, ws_o, max_parts, stream);
-  if (rc != PKV_OK) return rc;
+  // the prefix partials (slot 0) on the side stream, forked from and joined back to the caller's
+  // stream; the partitions of each [prefix_len, ctx) on the caller's stream; the merge after both
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (head_dim == 128) {
-    rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
-         : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
-                           : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
-  } else {
-    rc = block_size == 4   ? launch<64, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
-         : block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
-                           : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  std::lock_guard<std::mutex> guard(side_mutex());
+  SideStream* side = nullptr;
+  int rc = side_stream(dev, &side);
+  if (rc != PKV_OK) return rc;
+  cudaError_t e = cudaEventRecord(side->fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+  if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "shared-prefix attention: fork: %s", cudaGetErrorString(e));
+  rc = pkv::launch_prefix_partials(q, k_cache, v_cache, block_tables, group_start, prefix_lens, num_groups,
+                                   max_group_size, num_seqs, num_heads, head_dim, num_blocks, max_blocks_per_seq,
+                                   scale, block_size, ws_ml, ws_o, max_parts, side->stream);
+  if (rc == PKV_OK) {
+    e = cudaEventRecord(side->join, side->stream);
+    if (e != cudaSuccess) rc = pkv::fail(PKV_ERR_CUDA, "shared-prefix attention: join: %s", cudaGetErrorString(e));
   }
+  if (rc != PKV_OK) {
+    cudaStreamWaitEvent(st, side->fork, 0);      // leave the caller's stream consistent
+    return rc;
+  }
+  if (head_dim == 128) {
+    rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st, side->join)
+         : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st, side->join)
+                           : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st, side->join);
+  } else {
+    rc = block_size == 4   ? launch<64, 4>(p, num_seqs, pt, workspace_bytes, workspace, st, side->join)
+         : block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st, side->join)
+                           : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st, side->join);
+  }
+  if (rc != PKV_OK) cudaStreamWaitEvent(st, side->join, 0);   // join even when a launch failed
   if (rc == PKV_OK) pkv::clear_error();
   return rc;
 }
