@@ -63,9 +63,9 @@ EVENT_EVERY = 16
 # kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
 # on); a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # partition kernel 1,373,087,000 B read + 4,354,048 B written, merge kernel 1,261,000 B read
+    # partition kernel 1,373,077,000 B read + 4,009,856 B written, merge kernel 1,260,000 B read
     # (mean of two launches; profiles/paged_attention_opt13b_decode.md)
-    ("opt13b", "09b401f77065cea01980ce5dcb16498a77d194812797fa17f25ef115f9ff342d"): 1_378_702_000,
+    ("opt13b", "34e1a9eea67b3a895aed25baf04ae6eb978840e16a333f4241d8072a0e55b4ec"): 1_378_347_000,
 }
 
 
