@@ -17,7 +17,7 @@ the measured HBM copy bandwidth.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity|beam_search
                               |swap|layers40|prefill]
-                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F]
+                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F] [--grouped]
 
 `--workload swap`, `--workload layers40` and `--workload prefill` print their
 own lines (swap_blocks between HBM and page-locked host memory; 40-layer
@@ -28,6 +28,12 @@ The default workload is the headline one above.  The others build their batch
 through the same block manager (prompt forks with copy-on-write, a shared
 prefix, full 2048-token contexts); their copy-on-write copies are timed as
 one copy_blocks call (`copy_blocks_setup`).
+
+--grouped makes the attention call pkv_paged_attention_decode_shared_prefix:
+consecutive sequences whose leading blocks are the same physical blocks form a
+group whose shared prefix is read once (groups under 8 members still read it
+per sequence); the metric is unchanged and `roofline` then counts distinct K/V
+slots.
 
 --impl reference times the CPU oracle on the host cores instead (a bounded
 sample of the same workload per step) and prints the same metric.
