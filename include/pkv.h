@@ -184,13 +184,17 @@ int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* 
  * Tensor cores: fp16 products, fp32 accumulation; the softmax weights are
  * rounded to fp16 before they multiply V.
  *
- *   q, out        device [total_q, num_heads, head_dim] fp16, 16-byte aligned
+ *   q, out        device [total_q, num_heads, head_dim] fp16, 16-byte aligned;
+ *                 out must not overlap the inputs
  *   query_start   device [num_seqs + 1] int32, non-decreasing, last = total_q
  *   max_query_len host: the largest n_s (sizes the grid; larger n_s are not
  *                 fully processed)
  *   pools, tables, context_lens as for pkv_paged_attention_decode.
  * scale must be positive.  A sequence with n_s = 0 is skipped; n_s > ctx_s or
- * rows outside q record PKV_DEV_BAD_QUERY_RANGE.  No workspace.
+ * rows outside q record PKV_DEV_BAD_QUERY_RANGE; a table entry outside
+ * [0, num_blocks) within the context records PKV_DEV_BAD_BLOCK_ID and the
+ * sequence's rows (of the affected 256-token tile) are not written.  No
+ * workspace.
  * ------------------------------------------------------------------------- */
 int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                                 const int32_t* block_tables, const int32_t* context_lens,
