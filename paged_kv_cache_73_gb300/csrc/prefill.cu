@@ -12,11 +12,18 @@
 // Design: a dense contraction, so it runs on the fifth-generation tensor cores
 // (tcgen05.mma, fp16 inputs, fp32 accumulation in tensor memory); see the
 // kernel's comment below.  Key tiles of 64 positions are gathered block by
-// block through the table with 16-byte cp.async copies into the 128-byte
-// swizzled layout the tensor cores read, through a four-slot ring.  P is rounded to
-// fp16 for the second product, as flash attention does.  Key rows past the
-// context are zero-filled (never read), so stale NaN/Inf in unfilled slots
-// cannot reach a product.
+// block through the table into the 128-byte swizzled layout the tensor cores
+// read, through a four-slot ring: whole blocks by TMA (one tensor-map box per
+// block), the block holding the context's end by 16-byte cp.async copies.  Q
+// arrives by TMA as well.  P is rounded to fp16 for the second product, as flash
+// attention does.  Key rows past the context are zero-filled (never read), so
+// stale NaN/Inf in unfilled slots cannot reach a product.
+//
+// The same kernel, in its PARTIAL mode, gives the shared-prefix decode its
+// prefix part: the decode queries of a group of sequences sharing prefix blocks
+// form the query rows, every row sees every prefix key, and each row's
+// unnormalised (max, sum, output) goes to the decode workspace for the
+// log-sum-exp merge.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched through the runtime
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
