@@ -644,12 +644,18 @@ def physical_gpu_index(local: int) -> int:
 
 
 def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None):
-    """Same step through the C ABI, with the step's inputs in pinned host memory.
+    """Same step through the C ABI, with the step's inputs in pinned host memory, two ways.
 
-    Every step copies q, the new keys/values, slot mapping, copy pairs, block
-    tables and context lengths host->device (packed in one pinned buffer, so one
-    copy), runs the kernels, copies the attention output back and waits for it
-    (wall clock).
+    direct: the kernels read q, the new keys/values, slot mapping, copy pairs,
+    block tables and context lengths from the page-locked host buffer across the
+    host link (NVLink-C2C) and write the attention output into page-locked host
+    memory; the step ends when the stream has finished (wall clock).  Each step's
+    1.4 GB K/V stream evicts the previous step's lines from L2, so every step's
+    inputs cross the link again.
+    staged: one packed host->device copy of the same inputs, the kernels, and a
+    device->host copy of the output, then the wait.
+    The shared-prefix entry loads q by TMA from device memory, so a grouped step
+    is measured staged only.
     """
     import torch
     from paged_kv_cache_73_gb300 import binding as pkv
@@ -671,64 +677,80 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None):
         total += -(-(t.numel() * t.element_size()) // 256) * 256
     host_buf = torch.zeros(total, dtype=torch.uint8).pin_memory()
     dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    dbuf = {}
+    dbuf, hbuf = {}, {}
     for n, t in parts.items():
         nbytes = t.numel() * t.element_size()
         host_buf[offs[n]:offs[n] + nbytes].copy_(t.contiguous().view(-1).view(torch.uint8))
         dbuf[n] = dev_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+        hbuf[n] = host_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
     out_h = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
     out_d = torch.empty_like(q)
-    stream = torch.cuda.current_stream()
     n_pairs = int(pairs.shape[0])
     h2d = sum(t.numel() * t.element_size() for t in parts.values())
     d2h = out_h.numel() * out_h.element_size()
 
-    def body(st):
-        dev_buf.copy_(host_buf, non_blocking=True)
+    def step_calls(st, src, out):
         if n_pairs:
-            pkv.copy_blocks([k], [v], dbuf["pairs"], stream=st)
-        pkv.reshape_and_cache(dbuf["key"], dbuf["value"], k, v, dbuf["slots"], stream=st)
+            pkv.copy_blocks([k], [v], src["pairs"], stream=st)
+        pkv.reshape_and_cache(src["key"], src["value"], k, v, src["slots"], stream=st)
         if grouped is None:
-            pkv.paged_attention_decode(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], w.scale, w.block_size,
-                                       out=out_d, workspace=ws, stream=st)
+            pkv.paged_attention_decode(src["q"], k, v, src["tables"], src["lens"], w.scale, w.block_size,
+                                       out=out, workspace=ws, stream=st)
         else:
-            pkv.paged_attention_decode_shared_prefix(dbuf["q"], k, v, dbuf["tables"], dbuf["lens"], dbuf["gs"],
-                                                     dbuf["pl"], w.scale, w.block_size, grouped["max_group"],
-                                                     out=out_d, workspace=ws, stream=st)
+            pkv.paged_attention_decode_shared_prefix(src["q"], k, v, src["tables"], src["lens"], src["gs"],
+                                                     src["pl"], w.scale, w.block_size, grouped["max_group"],
+                                                     out=out, workspace=ws, stream=st)
+
+    def staged(st):
+        dev_buf.copy_(host_buf, non_blocking=True)
+        step_calls(st, dbuf, out_d)
         out_h.copy_(out_d, non_blocking=True)
 
-    for _ in range(max(args.warmup, 3)):
-        body(stream)
-        stream.synchronize()
-    # the step as a CUDA graph, recorded once through the same API calls and replayed every step
-    # (what a serving loop does with a fixed-shape decode step); eager calls if capture fails
-    graph, how = None, "eager API calls"
-    try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            body(torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        graph, how = g, "CUDA graph of the API calls, replayed"
-    except Exception as e:  # noqa: BLE001 - any capture failure falls back to the eager step
-        how = f"eager API calls (graph capture failed: {type(e).__name__})"
-        torch.cuda.synchronize()
+    def direct(st):
+        step_calls(st, hbuf, out_h)
 
-    def step():
-        if graph is not None:
-            graph.replay()
-        else:
+    def timed(body):
+        stream = torch.cuda.current_stream()
+        for _ in range(max(args.warmup, 3)):
             body(stream)
-        stream.synchronize()
+            stream.synchronize()
+        # the step as a CUDA graph, recorded once through the same API calls and replayed every
+        # step (what a serving loop does with a fixed-shape decode step); eager calls if capture fails
+        graph, how = None, "eager API calls"
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            graph, how = g, "CUDA graph of the API calls, replayed"
+        except Exception as e:  # noqa: BLE001 - any capture failure falls back to the eager step
+            how = f"eager API calls (graph capture failed: {type(e).__name__})"
+            torch.cuda.synchronize()
 
-    for _ in range(3):
-        step()
-    K = args.steps
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(K):
-        step()
-    dt = (time.perf_counter() - t0) / K
-    return {"e2e_step_ms": dt * 1e3, "h2d": h2d, "d2h": d2h, "launch": how}
+        def step():
+            if graph is not None:
+                graph.replay()
+            else:
+                body(stream)
+            stream.synchronize()
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step()
+        return (time.perf_counter() - t0) / args.steps * 1e3, how
+
+    staged_ms, how = timed(staged)
+    res = {"e2e_staged_ms": staged_ms, "h2d": h2d, "d2h": d2h}
+    if grouped is None:
+        direct_ms, how_d = timed(direct)
+        res.update(e2e_step_ms=direct_ms, launch=how_d + "; the kernels read the inputs from page-locked "
+                   "host memory over NVLink-C2C and write the output there (no staging copies)")
+    else:
+        res.update(e2e_step_ms=staged_ms, launch=how + "; one staging copy each way")
+    return res
 
 
 def prepare_cpu_sample(w, seqs, slots, seed):
@@ -871,8 +893,9 @@ def main():
     r = run_gpu(args, rank, world, dev)
 
     # whole-job numbers: bytes of all ranks over the slowest rank's time
-    (step_ms, e2e_ms, attn_ms), (kv_total, phys_total) = reduce_over_ranks(
-        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"]], [float(r["kv_bytes"]), float(r["phys_bytes"])],
+    (step_ms, e2e_ms, attn_ms, staged_ms), (kv_total, phys_total) = reduce_over_ranks(
+        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"], r.get("e2e_staged_ms", 0.0)],
+        [float(r["kv_bytes"]), float(r["phys_bytes"])],
         world, dev)
 
     if rank == 0:
@@ -912,7 +935,9 @@ def main():
         if "e2e_step_ms" in r:
             line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                            "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                           "ms_per_step": e2e_ms, "launch": r.get("launch", "eager API calls")}
+                           "ms_per_step": e2e_ms, "launch": r.get("launch", "eager API calls"),
+                           "staged_value": kv_total / (staged_ms * 1e-3) / 1e9,
+                           "staged_ms_per_step": staged_ms}
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

@@ -13,6 +13,17 @@
  *     pointers into ordinary host memory.  The caller owns every buffer and the
  *     stream; the library never allocates device memory, never frees caller
  *     memory and keeps no pointer after a call returns.
+ *   - The per-step inputs of the decode path may instead be page-locked host
+ *     memory mapped into the device's address space (cudaHostAlloc; with unified
+ *     addressing its host address is its device address).  These are q,
+ *     block_tables, context_lens and out of pkv_paged_attention_decode; the same
+ *     except q for pkv_paged_attention_decode_shared_prefix, plus group_start and
+ *     prefix_lens; and key, value and slot_mapping of pkv_reshape_and_cache.
+ *     The kernels then read or write them across the host link (NVLink-C2C on a
+ *     Grace-Blackwell node) with plain loads and stores, and no staging copy is
+ *     needed.  K/V pools and workspaces must be device memory.  As with device
+ *     buffers, the caller keeps such memory allocated and unchanged until the
+ *     stream has finished the call.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work is
  *     asynchronous on it; arguments are validated on the host first.
  *   - Return value: PKV_OK or a negative pkv_status; pkv_last_error() gives a

@@ -127,11 +127,23 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dim: int, cuda: bool = True) -> None:
-    if t.dtype != dtype or t.dim() != dim or not t.is_contiguous() or (cuda and not t.is_cuda):
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dim: int, cuda: bool = True,
+          host_ok: bool = False) -> None:
+    """dtype, rank and contiguity; on the device, or (host_ok) in page-locked host memory, which
+    the kernels read or write directly across the host link."""
+    placed = t.is_cuda or (host_ok and t.is_pinned())
+    if t.dtype != dtype or t.dim() != dim or not t.is_contiguous() or (cuda and not placed):
+        where = "CUDA or page-locked host " if host_ok else ("CUDA " if cuda else "")
         raise PkvError(PKV_ERR_INVALID_ARG,
-                       f"{name}: want a contiguous {'CUDA ' if cuda else ''}{dtype} tensor of rank {dim}, "
+                       f"{name}: want a contiguous {where}{dtype} tensor of rank {dim}, "
                        f"got {t.dtype} {tuple(t.shape)} contiguous={t.is_contiguous()} device={t.device}")
+
+
+def _out_like(q: torch.Tensor) -> torch.Tensor:
+    """A result buffer shaped as q: on the device, or page-locked if q is page-locked host memory."""
+    if q.is_cuda:
+        return torch.empty_like(q)
+    return torch.empty(tuple(q.shape), dtype=q.dtype).pin_memory()
 
 
 # ---- device entry points -------------------------------------------------------------------
@@ -175,12 +187,15 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                            block_size: int, out: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """out[s, h] = softmax attention of q[s, h] over the sequence's paged K/V (fp32 accumulate, fp16 out)."""
-    _need(q, "q", torch.float16, 3)
+    """out[s, h] = softmax attention of q[s, h] over the sequence's paged K/V (fp32 accumulate, fp16 out).
+
+    q, block_tables, context_lens and out may be page-locked host tensors: the kernels read and
+    write them across the host link (no staging copy).  The pools and the workspace are device memory."""
+    _need(q, "q", torch.float16, 3, host_ok=True)
     _need(k_cache, "k_cache", torch.float16, 4)
     _need(v_cache, "v_cache", torch.float16, 4)
-    _need(block_tables, "block_tables", torch.int32, 2)
-    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2, host_ok=True)
+    _need(context_lens, "context_lens", torch.int32, 1, host_ok=True)
     S, H, D = q.shape
     N = k_cache.shape[0]
     if tuple(k_cache.shape) != (N, H, block_size, D) or v_cache.shape != k_cache.shape:
@@ -189,12 +204,12 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if block_tables.shape[0] != S or context_lens.shape[0] != S:
         raise PkvError(PKV_ERR_INVALID_ARG, "block_tables / context_lens rows != num_seqs")
     if out is None:
-        out = torch.empty_like(q)
+        out = _out_like(q)
     else:
-        _need(out, "out", torch.float16, 3)
+        _need(out, "out", torch.float16, 3, host_ok=True)
     max_blocks = block_tables.shape[1]
     if workspace is None:
-        workspace = workspace_for(S, H, D, max_blocks, block_size, q.device)
+        workspace = workspace_for(S, H, D, max_blocks, block_size, k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().pkv_paged_attention_decode(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
@@ -214,14 +229,16 @@ def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
                                          group_start: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
                                          block_size: int, max_group_size: int, out: Optional[torch.Tensor] = None,
                                          workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """As paged_attention_decode, for sequences grouped by a shared prefix (read once per group)."""
+    """As paged_attention_decode, for sequences grouped by a shared prefix (read once per group).
+    block_tables, context_lens, group_start, prefix_lens and out may be page-locked host tensors;
+    q must be on the device (the prefix part loads it by TMA)."""
     _need(q, "q", torch.float16, 3)
     _need(k_cache, "k_cache", torch.float16, 4)
     _need(v_cache, "v_cache", torch.float16, 4)
-    _need(block_tables, "block_tables", torch.int32, 2)
-    _need(context_lens, "context_lens", torch.int32, 1)
-    _need(group_start, "group_start", torch.int32, 1)
-    _need(prefix_lens, "prefix_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2, host_ok=True)
+    _need(context_lens, "context_lens", torch.int32, 1, host_ok=True)
+    _need(group_start, "group_start", torch.int32, 1, host_ok=True)
+    _need(prefix_lens, "prefix_lens", torch.int32, 1, host_ok=True)
     S, H, D = q.shape
     N = k_cache.shape[0]
     G = prefix_lens.shape[0]
@@ -231,13 +248,13 @@ def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
     if block_tables.shape[0] != S or context_lens.shape[0] != S or group_start.shape[0] != G + 1:
         raise PkvError(PKV_ERR_INVALID_ARG, "block_tables / context_lens rows != num_seqs or group_start != groups + 1")
     if out is None:
-        out = torch.empty_like(q)
+        out = _out_like(q)
     else:
-        _need(out, "out", torch.float16, 3)
+        _need(out, "out", torch.float16, 3, host_ok=True)
     max_blocks = block_tables.shape[1]
     if workspace is None:
         n = paged_attention_shared_prefix_workspace_size(S, H, D, max_blocks, block_size)
-        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=k_cache.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(load().pkv_paged_attention_decode_shared_prefix(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
@@ -303,12 +320,13 @@ def paged_attention_decode_static_workspace(q: torch.Tensor, k_cache: torch.Tens
 
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       slot_mapping: torch.Tensor, stream=None) -> None:
-    """Store key[t], value[t] at slot_mapping[t] (negative = skip) in the paged pools."""
-    _need(key, "key", torch.float16, 3)
-    _need(value, "value", torch.float16, 3)
+    """Store key[t], value[t] at slot_mapping[t] (negative = skip) in the paged pools.
+    key, value and slot_mapping may be page-locked host tensors (read across the host link)."""
+    _need(key, "key", torch.float16, 3, host_ok=True)
+    _need(value, "value", torch.float16, 3, host_ok=True)
     _need(k_cache, "k_cache", torch.float16, 4)
     _need(v_cache, "v_cache", torch.float16, 4)
-    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, host_ok=True)
     T, H, D = key.shape
     N, H2, B, D2 = k_cache.shape
     if value.shape != key.shape or (H2, D2) != (H, D) or v_cache.shape != k_cache.shape or slot_mapping.shape[0] != T:
