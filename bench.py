@@ -69,9 +69,9 @@ EVENT_EVERY = 16
 # kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
 # on); a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # partition kernel 1,373,077,000 B read + 4,009,856 B written, merge kernel 1,260,000 B read
+    # partition kernel 1,373,076,500 B read + 4,127,232 B written, merge kernel 1,280,000 B read
     # (mean of two launches; profiles/paged_attention_opt13b_decode.md)
-    ("opt13b", "34e1a9eea67b3a895aed25baf04ae6eb978840e16a333f4241d8072a0e55b4ec"): 1_378_347_000,
+    ("opt13b", "1287c25da493ba0bad68cb905b4198a04887c68d579d889da18b81fae25b08ac"): 1_378_484_000,
 }
 
 
@@ -411,29 +411,48 @@ def run_gpu(args, rank, world, dev):
     assert pkv.device_error() == 0
 
     K = args.steps
-    # events around the attention call on every EVENT_EVERY-th step only: an event between two
-    # kernels stops the next launch from overlapping the previous kernel's tail (PDL)
-    n_ev = (K + EVENT_EVERY - 1) // EVENT_EVERY
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l2_bytes = l2_cache_bytes(dev)
+    flush = w.physical_kv_bytes() < 2 * l2_bytes
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
-        start.record(stream)
-        for i in range(K):
-            if i % EVENT_EVERY == 0:
-                step(*ev[i // EVENT_EVERY])
-            else:
-                step()
-        stop.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    step_ms = start.elapsed_time(stop) / K
-    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    if flush:
+        # a step whose K/V would stay in L2: a write of twice the L2 size before every step, outside
+        # the timed region, and each step timed by its own events (start, attention, end)
+        scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+        with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
+            for i in range(K):
+                scratch.fill_(i & 255)
+                e0, e1, e2 = evs[i]
+                e0.record(stream)
+                step(e1, e2)
+            torch.cuda.synchronize()
+        barrier(world)
+        step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in evs) / K
+        attn_ms = [e1.elapsed_time(e2) for _, e1, e2 in evs]
+    else:
+        # events around the attention call on every EVENT_EVERY-th step only: an event between two
+        # kernels stops the next launch from overlapping the previous kernel's tail (PDL)
+        n_ev = (K + EVENT_EVERY - 1) // EVENT_EVERY
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
+            start.record(stream)
+            for i in range(K):
+                if i % EVENT_EVERY == 0:
+                    step(*ev[i // EVENT_EVERY])
+                else:
+                    step()
+            stop.record(stream)
+            torch.cuda.synchronize()
+        barrier(world)
+        step_ms = start.elapsed_time(stop) / K
+        attn_ms = [a.elapsed_time(b) for a, b in ev]
     code = pkv.device_error()
     assert code == 0, f"device check {code}"
 
     res = {"step_ms": step_ms, "attn_ms": sum(attn_ms) / len(attn_ms), "attn_ms_median": statistics.median(attn_ms),
+           "l2_flushed": flush,
            "kv_bytes": w.logical_kv_bytes(), "phys_bytes": w.physical_kv_bytes(),
            # grouped: each shared prefix is read once, so the call's bytes are the distinct slots
            "attn_bytes": attention_algorithmic_bytes(w) if grouped is None
@@ -817,11 +836,19 @@ def barrier(world):
         dist.barrier()
 
 
-def config_block(args, desc, num_seqs, extra=None):
+def l2_cache_bytes(dev) -> int:
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    return int(getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024)
+
+
+def config_block(args, desc, num_seqs, extra=None, flushed=False):
     c = {"workload": desc, "num_seqs": num_seqs, "num_heads": 40, "head_dim": 128,
          "block_size": args.capacity_block if args.workload == "capacity" else 16,
          "seed": f"{SEED} (+7919*rank)", "kv_storage": "f16",
-         "l2": "inputs larger than L2: the step reads far more K/V than the 129 MB L2"}
+         "l2": ("L2 flushed before every step (a write of twice the L2 size, outside the timed region); "
+                "each step timed by its own events") if flushed
+               else "inputs larger than L2: the step reads more than twice the L2 size of distinct K/V"}
     if extra:
         c.update(extra)
     return c
@@ -911,7 +938,7 @@ def main():
             "config": config_block(args, r["desc"], S,
                                    {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                                     "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"],
-                                    "pool_blocks": r["num_blocks"]}),
+                                    "pool_blocks": r["num_blocks"]}, flushed=r["l2_flushed"]),
             "hbm_frac_of_measured": value / peak,
             "physical_kv_GBps": phys_total / (step_ms * 1e-3) / 1e9,
             "tokens_per_s": S * world / (step_ms * 1e-3),
@@ -923,7 +950,7 @@ def main():
                               "bytes = distinct K/V slots + q + out",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
-                         "launch_ms": attn_ms, "timed_launches": (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
+                         "launch_ms": attn_ms, "timed_launches": args.steps if r["l2_flushed"] else (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
                          "peak_source": peak_src + ", of measured"},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],

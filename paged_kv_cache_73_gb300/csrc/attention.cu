@@ -9,7 +9,8 @@
 //
 // GB300 design (decode attention is a batched GEMV: ~1 flop per byte, so HBM
 // bandwidth is the roofline and no tensor cores are used):
-//  * The context is split into partitions of `part_tokens` (128..1024) tokens; one CTA
+//  * The context is split into partitions of `part_tokens` (128..1024) tokens, the longest
+//    that still gives every SM a CTA; one CTA
 //    handles one (partition, head, sequence).  A second tiny kernel merges the
 //    partitions of a (sequence, head) with the log-sum-exp identity
 //    m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p 2^(m_p - m) / l.
@@ -474,6 +475,12 @@ __global__ void __launch_bounds__(128) paged_attention_merge_kernel(const AttnPa
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 4 + warp, s = blockIdx.y;
   if (h >= p.num_heads) return;
+  const size_t w0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_parts;
+  // The (m, l) of slots 0..31 are loaded together with the context length, before the slot count
+  // is known (every slot below max_parts is inside the workspace; the ones past the count are
+  // dropped below), so the chain of dependent memory round trips stays short.
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < p.max_parts) ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * (w0 + lane));
   const int ctx = p.lens[s];
   const int start = range_start(p, s);
   const int max_ctx = p.max_blocks * p.block_size;
@@ -481,35 +488,56 @@ __global__ void __launch_bounds__(128) paged_attention_merge_kernel(const AttnPa
   // slots: the shared-prefix partial (if any) and the partitions of [start, ctx)
   const int nparts = p.part_base + (bad_range ? 1 : (ctx - start + p.part_tokens - 1) / p.part_tokens);
   if (nparts <= 1) return;
-  const size_t w0 = (static_cast<size_t>(s) * p.num_heads + h) * p.max_parts;
-  float M = -INFINITY;
-  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[2 * (w0 + i)]);
-#pragma unroll
-  for (int o = 16; o > 0; o /= 2) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
   constexpr int V = D / 32;
   float acc[V];
 #pragma unroll
   for (int c = 0; c < V; ++c) acc[c] = 0.f;
-  float L = 0.f;
+  float M = -INFINITY, L = 0.f;
+  // slots in batches of 32 (one per lane for m and l); more than one batch only past 32 slots
   for (int base = 0; base < nparts; base += 32) {
     const int i = base + lane;
-    const float mi = i < nparts ? p.ws_ml[2 * (w0 + i)] : -INFINITY;
-    const float wi = mi == -INFINITY ? 0.f : exp2f(mi - M);
-    if (i < nparts) L = fmaf(p.ws_ml[2 * (w0 + i) + 1], wi, L);
+    if (base > 0) ml = i < nparts ? *reinterpret_cast<const float2*>(p.ws_ml + 2 * (w0 + i)) : make_float2(-INFINITY, 0.f);
+    if (i >= nparts) ml = make_float2(-INFINITY, 0.f);
+    float Mb = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o /= 2) Mb = fmaxf(Mb, __shfl_xor_sync(FULL, Mb, o));
+    // fold the batch into the running (M, L, acc): rescale what came before if the max moved
+    const float Mn = fmaxf(M, Mb);
+    const float carry = M == -INFINITY ? 0.f : exp2f(M - Mn);
+    L *= carry;
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[c] *= carry;
+    M = Mn;
+    const float wi = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+    L = fmaf(ml.y, wi, L);
     const int n = min(32, nparts - base);
-    for (int j = 0; j < n; ++j) {
-      const float wj = __shfl_sync(FULL, wi, j);
-      const float* src = p.ws_o + (w0 + base + j) * D + lane * V;
-      if constexpr (V == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] = fmaf(wj, x.x, acc[0]);
-        acc[1] = fmaf(wj, x.y, acc[1]);
-        acc[2] = fmaf(wj, x.z, acc[2]);
-        acc[3] = fmaf(wj, x.w, acc[3]);
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] = fmaf(wj, x.x, acc[0]);
-        acc[1] = fmaf(wj, x.y, acc[1]);
+    // eight slots' partial outputs in flight at a time
+    for (int j0 = 0; j0 < n; j0 += 8) {
+      float4 x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 + u < n) {
+          const float* src = p.ws_o + (w0 + base + j0 + u) * D + lane * V;
+          if constexpr (V == 4) {
+            x[u] = *reinterpret_cast<const float4*>(src);
+          } else {
+            const float2 t = *reinterpret_cast<const float2*>(src);
+            x[u] = make_float4(t.x, t.y, 0.f, 0.f);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wj = __shfl_sync(FULL, wi, (j0 + u) & 31);
+        if (j0 + u < n) {
+          acc[0] = fmaf(wj, x[u].x, acc[0]);
+          acc[1] = fmaf(wj, x[u].y, acc[1]);
+          if constexpr (V == 4) {
+            acc[2] = fmaf(wj, x[u].z, acc[2]);
+            acc[3] = fmaf(wj, x[u].w, acc[3]);
+          }
+        }
       }
     }
   }
@@ -564,9 +592,11 @@ cudaError_t prepare_kernel(int dev) {
 }
 
 int choose_part_tokens(int num_seqs, int num_heads, int max_ctx, int sms) {
-  // The longest partition that still gives about two full waves at three CTAs
-  // per SM (fewer pipeline fills and less merge traffic per byte read).
-  const long long target = 2LL * 3 * sms;
+  // The longest partition that still gives every SM a CTA: fewer, longer K/V streams per CTA
+  // (fewer pipeline fills, less merge traffic) until the grid would leave SMs idle.  Measured with
+  // L2 flushed between steps, ctx 2048, 40 heads: one sequence 26.4 us at 512 tokens (160 CTAs)
+  // against 29.7 us at 128 and 30.1 us at 1024; four sequences 46.8 us at 1024 against 48.9 at 256.
+  const long long target = sms;
   for (int pt : {1024, 512, 256}) {
     const long long ctas = static_cast<long long>(num_seqs) * num_heads * ((max_ctx + pt - 1) / pt);
     if (ctas >= target) return pt;
