@@ -67,6 +67,20 @@ def test_workspace_size(lib):
     assert pkv.paged_attention_workspace_size(64, 40, 128, 128, 16) == 64 * 40 * 16 * 130 * 4
 
 
+@pytest.mark.parametrize("S,H,D,max_blocks,want", [
+    (1, 40, 128, 128, 512),      # ctx 2048: 1024-token partitions would leave SMs idle (80 CTAs)
+    (4, 40, 128, 128, 1024),     # 320 CTAs of 1024 tokens already cover every SM
+    (64, 40, 128, 128, 1024),    # the OPT-13B-shaped batch
+    (1, 2, 64, 256, 128),        # too few (sequence, head) pairs for any partition to fill the GPU
+])
+def test_partition_plan(lib, S, H, D, max_blocks, want):
+    # the longest partition that still gives every SM a CTA (the rule holds for 148-160 SMs, and
+    # without a device the library assumes 148)
+    part, kernels = pkv.paged_attention_plan(S, H, D, max_blocks, 16)
+    assert part == want
+    assert kernels == (2 if max_blocks * 16 > part else 1)
+
+
 def test_cache_ops_host_validation(lib):
     assert lib.pkv_reshape_and_cache(16, 16, 16, 16, 16, 4, 2, 80, 16, 8, None) == pkv.PKV_ERR_UNSUPPORTED
     assert lib.pkv_reshape_and_cache(16, 16, 16, 16, 16, 0, 2, 64, 16, 8, None) == pkv.PKV_OK
