@@ -18,7 +18,8 @@
  *     addressing its host address is its device address).  These are q,
  *     block_tables, context_lens and out of pkv_paged_attention_decode; the same
  *     except q for pkv_paged_attention_decode_shared_prefix, plus group_start and
- *     prefix_lens; and key, value and slot_mapping of pkv_reshape_and_cache.
+ *     prefix_lens; key, value and slot_mapping of pkv_reshape_and_cache; and
+ *     block_mapping of pkv_copy_blocks.
  *     The kernels then read or write them across the host link (NVLink-C2C on a
  *     Grace-Blackwell node) with plain loads and stores, and no staging copy is
  *     needed.  K/V pools and workspaces must be device memory.  As with device
@@ -283,7 +284,7 @@ int pkv_reshape_and_cache_layers(const uint16_t* const* keys, const uint16_t* co
  *
  *   k_caches,
  *   v_caches      HOST arrays of num_layers device pool pointers (16-byte aligned)
- *   block_mapping device [num_pairs, 2] int64
+ *   block_mapping device or page-locked host [num_pairs, 2] int64
  * ------------------------------------------------------------------------- */
 int pkv_copy_blocks(uint16_t* const* k_caches, uint16_t* const* v_caches, int num_layers,
                     const int64_t* block_mapping, int num_pairs, int num_heads, int head_dim,

@@ -362,14 +362,15 @@ def reshape_and_cache_layers(keys: Sequence[torch.Tensor], values: Sequence[torc
 
 def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], block_mapping: torch.Tensor,
                 stream=None) -> None:
-    """For each (src, dst) row of block_mapping and each layer: block dst := block src (K and V)."""
+    """For each (src, dst) row of block_mapping and each layer: block dst := block src (K and V).
+    block_mapping may be a page-locked host tensor (read across the host link)."""
     if len(k_caches) != len(v_caches) or len(k_caches) == 0:
         raise PkvError(PKV_ERR_INVALID_ARG, "copy_blocks: need as many K as V pools, at least one")
     for t in list(k_caches) + list(v_caches):
         _need(t, "cache", torch.float16, 4)
         if t.shape != k_caches[0].shape:
             raise PkvError(PKV_ERR_INVALID_ARG, "copy_blocks: pools differ in shape")
-    _need(block_mapping, "block_mapping", torch.int64, 2)
+    _need(block_mapping, "block_mapping", torch.int64, 2, host_ok=True)
     if block_mapping.shape[1] != 2:
         raise PkvError(PKV_ERR_INVALID_ARG, "copy_blocks: block_mapping must be [P, 2]")
     N, H, B, D = k_caches[0].shape

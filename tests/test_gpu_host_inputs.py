@@ -96,3 +96,16 @@ def test_pageable_host_memory_is_refused(cuda_device):
     with pytest.raises(pkv.PkvError):
         pkv.paged_attention_decode(w.q("cpu"), k, v, torch.from_numpy(w.block_tables).to(cuda_device),
                                    torch.from_numpy(w.context_lens).to(cuda_device), w.scale, 8)
+
+
+def test_copy_blocks_reads_host_mapping(cuda_device):
+    w = wl.custom(909, [64, 48, 30], num_heads=2, head_dim=64, block_size=16)
+    k1, v1 = w.pools(cuda_device)
+    k2, v2 = k1.clone(), v1.clone()
+    pairs = torch.tensor([[0, w.num_blocks - 1], [2, w.num_blocks - 2], [1, 3]], dtype=torch.int64)
+    pkv.copy_blocks([k1], [v1], pairs.to(cuda_device))
+    pkv.copy_blocks([k2], [v2], _pinned(pairs))
+    assert pkv.device_error() == 0
+    torch.cuda.synchronize()
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
