@@ -74,9 +74,10 @@ EVENT_EVERY = 16
 # kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
 # on); a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # partition kernel 1,373,076,500 B read + 4,127,232 B written, merge kernel 1,280,000 B read
-    # (mean of two launches; profiles/paged_attention_opt13b_decode.md)
-    ("opt13b", "1287c25da493ba0bad68cb905b4198a04887c68d579d889da18b81fae25b08ac"): 1_378_484_000,
+    # the headline step's fused call: partition kernel 1,373,082,000 B read + 4,771,584 B written
+    # (the appended rows included), merge kernel 1,280,500 B read (mean of two launches;
+    # profiles/paged_attention_opt13b_decode.md)
+    ("opt13b+append", "021c61e6e19b4625b9a203bcb611acf0091f72b285ae6d512971dbf720884988"): 1_379_134_000,
 }
 
 
@@ -88,6 +89,9 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop (profiling runs)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="write the new tokens with a separate reshape_and_cache call before attention "
+                         "(default: pkv_paged_attention_decode_append, one launch)")
     ap.add_argument("--grouped", action="store_true",
                     help="read each shared prefix once per group of sequences (shared-prefix decode entry); "
                          "groups come from the block manager's shared leading blocks")
@@ -400,13 +404,22 @@ def run_gpu(args, rank, world, dev):
         moved = 2 * 2 * len(sp) * H * B * D * 2           # K and V, read and written
         copy = {"pairs": int(len(sp)), "ms": ms, "GB/s": moved / (ms * 1e-3) / 1e9}
 
+    fused = grouped is None and not args.unfused
+
     def step(ev0=None, ev1=None):
         if n_pairs:
             pkv.copy_blocks([k], [v], pairs_d, stream=stream)
-        pkv.reshape_and_cache(key, value, k, v, slots_d, stream=stream)
-        if ev0 is not None:
-            ev0.record(stream)
-        attention(q, tables, lens, stream)
+        if fused:
+            # the new tokens' K/V write and the attention in one launch
+            if ev0 is not None:
+                ev0.record(stream)
+            pkv.paged_attention_decode_append(q, key, value, slots_d, k, v, tables, lens, w.scale, B, out=out,
+                                              workspace=ws, stream=stream)
+        else:
+            pkv.reshape_and_cache(key, value, k, v, slots_d, stream=stream)
+            if ev0 is not None:
+                ev0.record(stream)
+            attention(q, tables, lens, stream)
         if ev1 is not None:
             ev1.record(stream)
 
@@ -459,16 +472,18 @@ def run_gpu(args, rank, world, dev):
     res = {"step_ms": step_ms, "attn_ms": sum(attn_ms) / len(attn_ms), "attn_ms_median": statistics.median(attn_ms),
            "l2_flushed": flush,
            "kv_bytes": w.logical_kv_bytes(), "phys_bytes": w.physical_kv_bytes(),
-           # grouped: each shared prefix is read once, so the call's bytes are the distinct slots
-           "attn_bytes": attention_algorithmic_bytes(w) if grouped is None
+           # grouped: each shared prefix is read once, so the call's bytes are the distinct slots;
+           # fused: the call also reads the new K/V rows and writes them into the pools
+           "attn_bytes": (attention_algorithmic_bytes(w) + (4 * S * H * D * 2 if fused else 0)) if grouped is None
            else w.physical_kv_bytes() + S * H * D * 2 * 2,
+           "fused": fused,
            "grouped": None if grouped is None else {k_: grouped[k_] for k_ in ("groups", "max_group", "prefix_tokens")},
            "num_seqs": S,
-           "launches": K * ((1 if n_pairs else 0) + 1 + attn_kernels), "part_tokens": part_tokens,
+           "launches": K * ((1 if n_pairs else 0) + (0 if fused else 1) + attn_kernels), "part_tokens": part_tokens,
            "host_slot_us": x["host_us"], "clocks": clocks.summary(), "n_pairs": n_pairs, "copy": copy,
            "desc": x["desc"], "num_blocks": w.num_blocks}
     if not args.no_e2e:
-        res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped))
+        res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped, fused))
     return res
 
 
@@ -700,7 +715,7 @@ def physical_gpu_index(local: int) -> int:
     return local
 
 
-def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None):
+def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None, fused=False):
     """Same step through the C ABI, with the step's inputs in pinned host memory, two ways.
 
     direct: the kernels read q, the new keys/values, slot mapping, copy pairs,
@@ -749,6 +764,10 @@ def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None):
     def step_calls(st, src, out):
         if n_pairs:
             pkv.copy_blocks([k], [v], src["pairs"], stream=st)
+        if fused:
+            pkv.paged_attention_decode_append(src["q"], src["key"], src["value"], src["slots"], k, v, src["tables"],
+                                              src["lens"], w.scale, w.block_size, out=out, workspace=ws, stream=st)
+            return
         pkv.reshape_and_cache(src["key"], src["value"], k, v, src["slots"], stream=st)
         if grouped is None:
             pkv.paged_attention_decode(src["q"], k, v, src["tables"], src["lens"], w.scale, w.block_size,
@@ -999,7 +1018,8 @@ def main():
     if rank == 0:
         peak, peak_src = measured_hbm_peak()
         achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
-        traffic = None if args.grouped else NCU_TRAFFIC.get((args.workload, attention_source_sha()))
+        traffic = None if args.grouped else NCU_TRAFFIC.get(
+            (args.workload + ("+append" if r["fused"] else ""), attention_source_sha()))
         value = kv_total / (step_ms * 1e-3) / 1e9
         S = r["num_seqs"]
         line = {
@@ -1016,7 +1036,10 @@ def main():
             "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
             "host_slot_assignment_us": r["host_slot_us"],
             "roofline": {"bound": "hbm",
-                         "kernel": "paged attention call (partition + merge kernels)" if r["grouped"] is None
+                         "kernel": ("paged attention call with the new tokens' K/V append (partition + merge "
+                                    "kernels); bytes include the appended rows read and written"
+                                    if r["fused"] else "paged attention call (partition + merge kernels)")
+                         if r["grouped"] is None
                          else "shared-prefix attention call (prefix partials on tensor cores + partition + merge); "
                               "bytes = distinct K/V slots + q + out",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

@@ -20,6 +20,8 @@
  *     except q for pkv_paged_attention_decode_shared_prefix, plus group_start and
  *     prefix_lens; key, value and slot_mapping of pkv_reshape_and_cache; and
  *     block_mapping of pkv_copy_blocks.
+ *     pkv_paged_attention_decode_append takes the same, plus key, value and
+ *     slot_mapping.
  *     The kernels then read or write them across the host link (NVLink-C2C on a
  *     Grace-Blackwell node) with plain loads and stores, and no staging copy is
  *     needed.  K/V pools and workspaces must be device memory.  As with device
@@ -135,6 +137,34 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
                                int num_seqs, int num_heads, int head_dim, int num_blocks,
                                int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode step with the new token's K/V write fused in: exactly
+ * pkv_reshape_and_cache(key, value, slot_mapping) followed by
+ * pkv_paged_attention_decode, in one launch (the write-then-attend order of
+ * [note] 关键设计 1: the sum runs to t = i, so the new token attends to
+ * itself).  Sequence s has one new token, rows key[s] and value[s]
+ * ([num_seqs, num_heads, head_dim] fp16, 16-byte aligned), stored at
+ * slot_mapping[s] (int64; < 0: none); context_lens[s] already counts it.
+ *
+ * The CTA that reads the context's last position stores the row and, where
+ * the table maps that position to slot_mapping[s], uses the row it stored
+ * instead of the copy in the pool.  The result and the pools then equal
+ * those of the two separate calls, provided no other sequence of the batch
+ * reads an appended slot.  Slots from pkv_bm_append_slot(s) meet that: a
+ * shared block is copied before it is written.  A slot >= num_blocks *
+ * block_size records PKV_DEV_BAD_SLOT and is not written.  Arguments, the
+ * workspace and the error behaviour are otherwise those of
+ * pkv_paged_attention_decode, including page-locked host memory for q,
+ * key, value, slot_mapping, the tables, the lengths and out.  k_cache and
+ * v_cache are written.
+ * ------------------------------------------------------------------------- */
+int pkv_paged_attention_decode_append(const uint16_t* q, const uint16_t* key, const uint16_t* value,
+                                      const int64_t* slot_mapping, uint16_t* k_cache, uint16_t* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                      int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq,
+                                      float scale, int block_size, uint16_t* out, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Paged decode attention for batches whose sequences share prefix blocks

@@ -53,6 +53,8 @@ _SIGNATURES = {
     "pkv_paged_attention_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_plan": (_I, [_I, _I, _I, _I, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I, _P, _P, _SZ, _P]),
+    "pkv_paged_attention_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I,
+                                               _P, _P, _SZ, _P]),
     "pkv_paged_attention_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                                       _c.c_float, _I, _P, _P, _SZ, _P]),
@@ -215,6 +217,46 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
         S, H, D, N, max_blocks, float(scale), block_size, out.data_ptr(), _ptr(workspace), ws_bytes,
         _stream(stream)))
+    return out
+
+
+def paged_attention_decode_append(q: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                                  slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                  block_size: int, out: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """reshape_and_cache(key, value, slot_mapping) then paged_attention_decode, in one launch: each
+    sequence's new K/V row is stored at its slot and attended to in the same kernel.  The step
+    inputs (q, key, value, slot_mapping, tables, lengths) and out may be page-locked host tensors."""
+    _need(q, "q", torch.float16, 3, host_ok=True)
+    _need(key, "key", torch.float16, 3, host_ok=True)
+    _need(value, "value", torch.float16, 3, host_ok=True)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, host_ok=True)
+    _need(k_cache, "k_cache", torch.float16, 4)
+    _need(v_cache, "v_cache", torch.float16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2, host_ok=True)
+    _need(context_lens, "context_lens", torch.int32, 1, host_ok=True)
+    S, H, D = q.shape
+    N = k_cache.shape[0]
+    if tuple(k_cache.shape) != (N, H, block_size, D) or v_cache.shape != k_cache.shape:
+        raise PkvError(PKV_ERR_INVALID_ARG, f"cache shape {tuple(k_cache.shape)} does not match "
+                                            f"[N, {H}, {block_size}, {D}]")
+    if key.shape != q.shape or value.shape != q.shape or slot_mapping.shape[0] != S:
+        raise PkvError(PKV_ERR_INVALID_ARG, "key / value must be [num_seqs, H, D] and slot_mapping [num_seqs]")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise PkvError(PKV_ERR_INVALID_ARG, "block_tables / context_lens rows != num_seqs")
+    if out is None:
+        out = _out_like(q)
+    else:
+        _need(out, "out", torch.float16, 3, host_ok=True)
+    max_blocks = block_tables.shape[1]
+    if workspace is None:
+        workspace = workspace_for(S, H, D, max_blocks, block_size, k_cache.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().pkv_paged_attention_decode_append(
+        q.data_ptr(), key.data_ptr(), value.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, H, D, N, max_blocks,
+        float(scale), block_size, out.data_ptr(), _ptr(workspace), ws_bytes, _stream(stream)))
     return out
 
 

@@ -144,6 +144,11 @@ struct AttnParams {
   int part_tokens;
   int max_parts;
   float scale_log2;
+  // append (null for plain decode): sequence s's new token, rows new_k / new_v [S, H, D], goes to
+  // pool slot new_slot[s] (< 0: none) before the token attends, as reshape_and_cache would write it
+  const __half* new_k;
+  const __half* new_v;
+  const int64_t* new_slot;
 };
 
 // First token of sequence s's own range: 0 for plain decode, else its group's shared-prefix
@@ -268,6 +273,37 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const int nparts = bad_range ? 1 : (ctx + p.part_tokens - 1) / p.part_tokens;
   if (part >= nparts) return;
   const size_t out_off = (static_cast<size_t>(s) * H + h) * D;
+  // Append: the CTA of the last partition stores head h of the sequence's new K/V row at its slot,
+  // as reshape_and_cache would before the call.  When the table maps the context's last position
+  // to that slot, the row is also written over the staged copy of that chunk (the bulk copy may or
+  // may not have seen the store), by the warp that owns the chunk: lanes 0..D/8-1 hold the K row,
+  // the next D/8 lanes the V row, one 16-byte vector each.
+  uint4 new_row = make_uint4(0, 0, 0, 0);
+  int patch_chunk = -1, patch_row = 0;                 // local chunk and row to patch, -1 = none
+  if (p.new_slot != nullptr && part == nparts - 1) {
+    const int64_t slot = p.new_slot[s];
+    const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * B;
+    if (slot >= num_slots) {
+      if (tid == 0) record_error(PKV_DEV_BAD_SLOT);
+    } else if (slot >= 0) {
+      if (!bad_range) {
+        const int last = ctx - 1;                        // relative to the range start
+        const int64_t phys = p.tables[static_cast<size_t>(s) * p.max_blocks + (start + last) / B];
+        if (phys * B + (start + last) % B == slot) {
+          patch_chunk = last / R - part * (p.part_tokens / R);
+          patch_row = last % R;
+        }
+      }
+      const int row_warp = patch_chunk >= 0 ? patch_chunk % NW : 0;
+      if (warp == row_warp && lane < 2 * C::CPR) {
+        const bool is_v = lane >= C::CPR;
+        const int col = is_v ? lane - C::CPR : lane;
+        new_row = *reinterpret_cast<const uint4*>((is_v ? p.new_v : p.new_k) + out_off + col * 8);
+        __half* pool = const_cast<__half*>(is_v ? p.v : p.k);
+        *reinterpret_cast<uint4*>(pool + (((slot / B) * H + h) * B + slot % B) * D + col * 8) = new_row;
+      }
+    }
+  }
   if (bad_range) {
     // an empty range (ctx = 0, or a context that is exactly its shared prefix) is no error; a
     // sequence in no group, a prefix that is not whole blocks or longer than the context is a
@@ -394,6 +430,18 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
       break;
     }
     const unsigned char* ks = wring + stage * C::STAGE_BYTES;
+    if (warp + k * NW == patch_chunk) {
+      // the appended row replaces what the copy brought (this warp's stage, after it landed)
+      if (lane < 2 * C::CPR) {
+        const bool is_v = lane >= C::CPR;
+        const int col = is_v ? lane - C::CPR : lane;
+        *reinterpret_cast<uint4*>(const_cast<unsigned char*>(ks) + (is_v ? C::CHUNK_BYTES : 0) +
+                                  (patch_row * D + col * 8) * 2) = new_row;
+        // before a later bulk copy (async proxy) refills this stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
+    }
     const int c = c_begin + warp + k * NW;
     const int valid = min(R, ctx - c * R);
     if (valid == R)
@@ -674,6 +722,72 @@ int side_stream(int dev, SideStream** out) {
   return PKV_OK;
 }
 
+// pkv_paged_attention_decode, and with new_slot set pkv_paged_attention_decode_append (fn names
+// the entry in messages)
+int decode_entry(const char* fn, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
+                 int head_dim, int num_blocks, int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
+                 void* workspace, size_t workspace_bytes, void* stream, const uint16_t* new_k,
+                 const uint16_t* new_v, const int64_t* new_slot) {
+  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG,
+                     "%s: num_seqs=%d num_heads=%d num_blocks=%d max_blocks_per_seq=%d", fn,
+                     num_seqs, num_heads, num_blocks, max_blocks_per_seq);
+  if (head_dim != 64 && head_dim != 128)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: head_dim %d not in {64, 128}", fn, head_dim);
+  if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: block_size %d not in {4, 8, 16, 32}", fn,
+                     block_size);
+  if (num_seqs == 0) {
+    pkv::clear_error();
+    return PKV_OK;
+  }
+  if (num_seqs > 65535 || num_heads > 65535)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: num_seqs/num_heads above 65535", fn);
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > (1LL << 30))
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "%s: context capacity above 2^30 tokens", fn);
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "%s: q, caches, out, workspace must be 16-byte aligned", fn);
+  if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID_ARG, "%s: scale not finite", fn);
+
+  AttnParams p{};
+  p.new_k = reinterpret_cast<const __half*>(new_k);
+  p.new_v = reinterpret_cast<const __half*>(new_v);
+  p.new_slot = new_slot;
+  p.q = reinterpret_cast<const __half*>(q);
+  p.k = reinterpret_cast<const __half*>(k_cache);
+  p.v = reinterpret_cast<const __half*>(v_cache);
+  p.tables = block_tables;
+  p.lens = context_lens;
+  p.out = reinterpret_cast<__half*>(out);
+  p.num_heads = num_heads;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks_per_seq;
+  p.block_size = block_size;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const int pt = choose_part_tokens(num_seqs, num_heads, max_blocks_per_seq * block_size, device_sms(dev));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc;
+  // chunk rows R = min(B, 16): a block of 32 rows is read as two chunks
+  if (head_dim == 128) {
+    rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
+         : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                           : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  } else {
+    rc = block_size == 4   ? launch<64, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
+         : block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
+                           : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
+  }
+  if (rc == PKV_OK) pkv::clear_error();
+  return rc;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -725,60 +839,24 @@ int pkv_paged_attention_decode(const uint16_t* q, const uint16_t* k_cache, const
                                int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq, float scale,
                                int block_size, uint16_t* out, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
-    return pkv::fail(PKV_ERR_INVALID_ARG,
-                     "pkv_paged_attention_decode: num_seqs=%d num_heads=%d num_blocks=%d max_blocks_per_seq=%d",
-                     num_seqs, num_heads, num_blocks, max_blocks_per_seq);
-  if (head_dim != 64 && head_dim != 128)
-    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: head_dim %d not in {64, 128}", head_dim);
-  if (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32)
-    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: block_size %d not in {4, 8, 16, 32}",
-                     block_size);
-  if (num_seqs == 0) {
-    pkv::clear_error();
-    return PKV_OK;
-  }
-  if (num_seqs > 65535 || num_heads > 65535)
-    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: num_seqs/num_heads above 65535");
-  if (static_cast<long long>(max_blocks_per_seq) * block_size > (1LL << 30))
-    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: context capacity above 2^30 tokens");
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: null pointer");
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (workspace && !aligned16(workspace)))
-    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: q, caches, out, workspace must be 16-byte aligned");
-  if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: scale not finite");
+  return decode_entry("pkv_paged_attention_decode", q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                      num_heads, head_dim, num_blocks, max_blocks_per_seq, scale, block_size, out, workspace,
+                      workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
 
-  AttnParams p{};
-  p.q = reinterpret_cast<const __half*>(q);
-  p.k = reinterpret_cast<const __half*>(k_cache);
-  p.v = reinterpret_cast<const __half*>(v_cache);
-  p.tables = block_tables;
-  p.lens = context_lens;
-  p.out = reinterpret_cast<__half*>(out);
-  p.num_heads = num_heads;
-  p.num_blocks = num_blocks;
-  p.max_blocks = max_blocks_per_seq;
-  p.block_size = block_size;
-  p.scale_log2 = scale * 1.4426950408889634f;
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  const int pt = choose_part_tokens(num_seqs, num_heads, max_blocks_per_seq * block_size, device_sms(dev));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc;
-  // chunk rows R = min(B, 16): a block of 32 rows is read as two chunks
-  if (head_dim == 128) {
-    rc = block_size == 4   ? launch<128, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
-         : block_size == 8 ? launch<128, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
-                           : launch<128, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
-  } else {
-    rc = block_size == 4   ? launch<64, 4>(p, num_seqs, pt, workspace_bytes, workspace, st)
-         : block_size == 8 ? launch<64, 8>(p, num_seqs, pt, workspace_bytes, workspace, st)
-                           : launch<64, 16>(p, num_seqs, pt, workspace_bytes, workspace, st);
-  }
-  if (rc == PKV_OK) pkv::clear_error();
-  return rc;
+int pkv_paged_attention_decode_append(const uint16_t* q, const uint16_t* key, const uint16_t* value,
+                                      const int64_t* slot_mapping, uint16_t* k_cache, uint16_t* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                      int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq,
+                                      float scale, int block_size, uint16_t* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (num_seqs > 0 && (!key || !value || !slot_mapping))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode_append: null key, value or slot_mapping");
+  if (num_seqs > 0 && (!aligned16(key) || !aligned16(value)))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode_append: key and value must be 16-byte aligned");
+  return decode_entry("pkv_paged_attention_decode_append", q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                      num_heads, head_dim, num_blocks, max_blocks_per_seq, scale, block_size, out, workspace,
+                      workspace_bytes, stream, key, value, slot_mapping);
 }
 
 size_t pkv_paged_attention_shared_prefix_workspace_size(int num_seqs, int num_heads, int head_dim,
