@@ -42,6 +42,8 @@ sample of the same workload per step) and prints the same metric.
 from __future__ import annotations
 
 import argparse
+import atexit
+import datetime
 import hashlib
 import json
 import math
@@ -65,9 +67,10 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention effective KV GB/s (% of HBM peak) and decode tokens/s"
 UNIT = "GB/s"
 WORKLOAD = ("opt13b_decode_step: 64 seqs, 40 heads x 128, block 16, ctx ~ U[128,2048], shuffled blocks, "
-            "+ reshape_and_cache of 64 new tokens")
+            "+ the K/V write of 64 new tokens (in the attention launch; --unfused: reshape_and_cache first)")
 SEED = 1002
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0                                # GB300 HBM3e, nominal
 EVENT_EVERY = 16
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call (partition + merge
@@ -121,66 +124,120 @@ def measured_hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms by a child process.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler starts before the warm-up steps and runs until the run ends. Each sample carries
+    nvidia-smi's own timestamp. `summary(t0, t1)` keeps the samples whose timestamps fall inside the
+    timed region [t0, t1] (host wall clock). When the region is shorter than three intervals it also
+    keeps the last sample before t0 and the first after t1; the warm-up keeps the GPU busy before."""
+
+    INTERVAL_MS = 100
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.out = None
 
-    def __enter__(self):
+    def start(self):
         fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
         os.close(fd)
         try:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         return self
 
-    def __exit__(self, *exc):
-        if self.proc is not None:
+    def stop(self):
+        if self.proc is not None and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-        self.out.close()
+                self.proc.wait()
+        if self.out is not None:
+            self.out.close()
+            self.out = None
+        if self.path is not None and os.path.exists(self.path):
+            os.unlink(self.path)
 
-    def summary(self):
+    def __enter__(self):
+        return self.start()
+
+    def __exit__(self, *exc):
+        self.stop()
+
+    @staticmethod
+    def _stamp(text):
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
+    def _rows(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 10:
+                        rows.append((self._stamp(parts[0]), parts))
+        except OSError:
+            pass
+        return rows
+
+    def summary(self, t0: float, t1: float):
         if self.proc is None:
             return None
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
+        # wait (bounded) for the first sample after the region
+        deadline = time.time() + 1.0
+        rows = self._rows()
+        while time.time() < deadline and not any(t is not None and t > t1 for t, _ in rows):
+            time.sleep(0.05)
+            rows = self._rows()
         if not rows:
             return None
+        stamped = [(t, r) for t, r in rows if t is not None]
+        if stamped:
+            inside = [r for t, r in stamped if t0 <= t <= t1]
+            window = "inside the timed region"
+            if len(inside) < 3:
+                before = [r for t, r in stamped if t < t0][-1:]
+                after = [r for t, r in stamped if t > t1][:1]
+                inside = before + inside + after
+                window = "inside the timed region, plus the last sample before it and the first after it"
+            picked = inside
+        else:
+            picked = [r for _, r in rows]
+            window = "unparsed timestamps: every sample since the sampler started"
+        if not picked:
+            return None
+
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        sm = [num(r[2]) for r in picked if num(r[2]) is not None]
         reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            for name, val in zip(names, r[5:9]):
+        for r in picked:
+            for name, val in zip(self.REASONS, r[6:10]):
                 if val.lower() in ("active", "1", "yes"):
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": num(rows[0][2]), "samples": len(rows),
-                "power_w_max": max((num(r[3]) or 0.0) for r in rows), "reasons": sorted(reasons)}
-
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_min_mhz": min(sm) if sm else None,
+                "sm_max_mhz": num(picked[0][3]), "samples": len(picked), "interval_ms": self.INTERVAL_MS,
+                "window": window, "region_s": t1 - t0,
+                "power_w_max": max((num(r[4]) or 0.0) for r in picked), "reasons": sorted(reasons)}
 
 
 # ---- workloads -------------------------------------------------------------------------------------
@@ -423,6 +480,9 @@ def run_gpu(args, rank, world, dev):
         if ev1 is not None:
             ev1.record(stream)
 
+    # clocks sampled from before the warm-up on; stopped at exit as well, should the run raise
+    clocks = ClockSampler(physical_gpu_index(torch.cuda.current_device())).start()
+    atexit.register(clocks.stop)
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -438,13 +498,14 @@ def run_gpu(args, rank, world, dev):
         # the timed region, and each step timed by its own events (start, attention, end)
         scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
         evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
-        with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
-            for i in range(K):
-                scratch.fill_(i & 255)
-                e0, e1, e2 = evs[i]
-                e0.record(stream)
-                step(e1, e2)
-            torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(K):
+            scratch.fill_(i & 255)
+            e0, e1, e2 = evs[i]
+            e0.record(stream)
+            step(e1, e2)
+        torch.cuda.synchronize()
+        t1 = time.time()
         barrier(world)
         step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in evs) / K
         attn_ms = [e1.elapsed_time(e2) for _, e1, e2 in evs]
@@ -454,18 +515,21 @@ def run_gpu(args, rank, world, dev):
         n_ev = (K + EVENT_EVERY - 1) // EVENT_EVERY
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
-            start.record(stream)
-            for i in range(K):
-                if i % EVENT_EVERY == 0:
-                    step(*ev[i // EVENT_EVERY])
-                else:
-                    step()
-            stop.record(stream)
-            torch.cuda.synchronize()
+        t0 = time.time()
+        start.record(stream)
+        for i in range(K):
+            if i % EVENT_EVERY == 0:
+                step(*ev[i // EVENT_EVERY])
+            else:
+                step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
         barrier(world)
         step_ms = start.elapsed_time(stop) / K
         attn_ms = [a.elapsed_time(b) for a, b in ev]
+    clock_summary = clocks.summary(t0, t1)
+    clocks.stop()
     code = pkv.device_error()
     assert code == 0, f"device check {code}"
 
@@ -480,7 +544,7 @@ def run_gpu(args, rank, world, dev):
            "grouped": None if grouped is None else {k_: grouped[k_] for k_ in ("groups", "max_group", "prefix_tokens")},
            "num_seqs": S,
            "launches": K * ((1 if n_pairs else 0) + (0 if fused else 1) + attn_kernels), "part_tokens": part_tokens,
-           "host_slot_us": x["host_us"], "clocks": clocks.summary(), "n_pairs": n_pairs, "copy": copy,
+           "host_slot_us": x["host_us"], "clocks": clock_summary, "n_pairs": n_pairs, "copy": copy,
            "desc": x["desc"], "num_blocks": w.num_blocks}
     if not args.no_e2e:
         res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped, fused))
@@ -663,9 +727,15 @@ def run_prefill(args, dev):
 
     steps = max(3, min(args.steps, 50))
     with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        t0 = time.time()
         t_step = _timed(step, reps=steps, warm=max(args.warmup, 3))
         t_attn = _timed(attn, reps=steps, warm=3)
         t_long = _timed(attn2, reps=steps, warm=3)
+        t1 = time.time()
+        clock_summary = clocks.summary(t0, t1)
     assert pkv.device_error() == 0
     peak = measured_tensor_peak()
     achieved = flops / (t_attn * 1e-3) / 1e12
@@ -683,7 +753,7 @@ def run_prefill(args, dev):
             "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc_kernel", "achieved": achieved,
                          "peak": peak[0], "unit": "TFLOP/s", "frac": achieved / peak[0], "traffic": None,
                          "launch_ms": t_attn, "peak_source": peak[1]},
-            "clocks": clocks.summary()}
+            "clocks": clock_summary}
 
 
 def measured_tensor_peak():
@@ -1031,6 +1101,7 @@ def main():
                                     "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"],
                                     "pool_blocks": r["num_blocks"]}, flushed=r["l2_flushed"]),
             "hbm_frac_of_measured": value / peak,
+            "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
             "physical_kv_GBps": phys_total / (step_ms * 1e-3) / 1e9,
             "tokens_per_s": S * world / (step_ms * 1e-3),
             "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
