@@ -247,7 +247,9 @@ __device__ __forceinline__ void chunk_update(const unsigned char* ks, const unsi
   }
 }
 
-template <int D, int R>
+// APPEND: the fused new-token write of pkv_paged_attention_decode_append.  A compile-time switch:
+// the plain decode kernel carries none of its registers or branches.
+template <int D, int R, bool APPEND>
 __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partition_kernel(const AttnParams p) {
   using C = Cfg<D, R>;
   constexpr int NW = C::NW, NST = C::NST;
@@ -255,7 +257,10 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   unsigned char* ring = smem;                                                   // [NW][NST][K|V]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NST * C::STAGE_BYTES);  // [NW][NST]
   float* comb = reinterpret_cast<float*>(bars + NW * NST);                      // [NW][D + 2]
-  int64_t* chunk_off = reinterpret_cast<int64_t*>(comb + NW * (D + 2));        // [chunks per part]
+  // append only: the new K/V row of head h, handed from the warp that loads it to the one that
+  // patches the staged chunk ([2 * D / 8] 16-byte vectors)
+  uint4* row_stage = reinterpret_cast<uint4*>(comb + NW * (D + 2));
+  int64_t* chunk_off = reinterpret_cast<int64_t*>(row_stage + (APPEND ? 2 * C::CPR : 0));  // [chunks per part]
 
   const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -263,6 +268,22 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   pkv::pdl_wait();  // inputs may come from the previous kernel on the stream
   const int B = p.block_size;
   const int H = p.num_heads;
+  const size_t out_off = (static_cast<size_t>(s) * H + h) * D;
+  // Append: the CTA of the last partition stores head h of the sequence's new K/V row at its slot,
+  // as reshape_and_cache would before the call.  Which CTA that is depends on the context length,
+  // so the slot and the row are read at once, beside the length, by every CTA: lanes 0..D/8-1 of
+  // the last warp the K row, the next D/8 lanes the V row, one 16-byte vector each.  This CTA's
+  // bulk copies may read the pool before or after the store, so where the table maps the
+  // context's last position to the slot, the warp that owns that chunk writes the row over its
+  // staged copy.  No other CTA reads the slot: other partitions end before the last position.
+  const bool row_lane = lane < 2 * C::CPR;
+  const bool row_is_v = lane >= C::CPR;
+  const int row_col = row_is_v ? lane - C::CPR : lane;
+  const bool row_loader = APPEND && warp == NW - 1 && row_lane;
+  const int64_t slot = APPEND ? p.new_slot[s] : -1;
+  uint4 new_row = make_uint4(0, 0, 0, 0);
+  if (row_loader)
+    new_row = *reinterpret_cast<const uint4*>((row_is_v ? p.new_v : p.new_k) + out_off + row_col * 8);
   const int max_ctx = p.max_blocks * B;
   // this CTA's tokens: partition `part` of [start, ctx) (start = 0 unless a shared prefix precedes)
   const int ctx_full = p.lens[s];
@@ -272,38 +293,13 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const int ctx = ctx_full - start;                    // tokens of the range
   const int nparts = bad_range ? 1 : (ctx + p.part_tokens - 1) / p.part_tokens;
   if (part >= nparts) return;
-  const size_t out_off = (static_cast<size_t>(s) * H + h) * D;
-  // Append: the CTA of the last partition stores head h of the sequence's new K/V row at its slot,
-  // as reshape_and_cache would before the call.  When the table maps the context's last position
-  // to that slot, the row is also written over the staged copy of that chunk (the bulk copy may or
-  // may not have seen the store), by the warp that owns the chunk: lanes 0..D/8-1 hold the K row,
-  // the next D/8 lanes the V row, one 16-byte vector each.
-  uint4 new_row = make_uint4(0, 0, 0, 0);
-  int patch_chunk = -1, patch_row = 0;                 // local chunk and row to patch, -1 = none
-  if (p.new_slot != nullptr && part == nparts - 1) {
-    const int64_t slot = p.new_slot[s];
-    const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * B;
-    if (slot >= num_slots) {
-      if (tid == 0) record_error(PKV_DEV_BAD_SLOT);
-    } else if (slot >= 0) {
-      if (!bad_range) {
-        const int last = ctx - 1;                        // relative to the range start
-        const int64_t phys = p.tables[static_cast<size_t>(s) * p.max_blocks + (start + last) / B];
-        if (phys * B + (start + last) % B == slot) {
-          patch_chunk = last / R - part * (p.part_tokens / R);
-          patch_row = last % R;
-        }
-      }
-      const int row_warp = patch_chunk >= 0 ? patch_chunk % NW : 0;
-      if (warp == row_warp && lane < 2 * C::CPR) {
-        const bool is_v = lane >= C::CPR;
-        const int col = is_v ? lane - C::CPR : lane;
-        new_row = *reinterpret_cast<const uint4*>((is_v ? p.new_v : p.new_k) + out_off + col * 8);
-        __half* pool = const_cast<__half*>(is_v ? p.v : p.k);
-        *reinterpret_cast<uint4*>(pool + (((slot / B) * H + h) * B + slot % B) * D + col * 8) = new_row;
-      }
-    }
-  }
+  const bool appends = APPEND && part == nparts - 1;
+  const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * B;
+  const bool slot_ok = appends && slot >= 0 && slot < num_slots;
+  auto store_row = [&]() {
+    __half* pool = const_cast<__half*>(row_is_v ? p.v : p.k);
+    *reinterpret_cast<uint4*>(pool + (((slot / B) * H + h) * B + slot % B) * D + row_col * 8) = new_row;
+  };
   if (bad_range) {
     // an empty range (ctx = 0, or a context that is exactly its shared prefix) is no error; a
     // sequence in no group, a prefix that is not whole blocks or longer than the context is a
@@ -314,6 +310,8 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
       else if (start < 0 || start % B != 0 || ctx_full < start)
         record_error(PKV_DEV_PREFIX_MISMATCH);
     }
+    if (appends && slot >= num_slots && tid == 0) record_error(PKV_DEV_BAD_SLOT);
+    if (slot_ok && row_loader) store_row();
     if (p.part_base == 0) {
       for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
     } else {
@@ -360,7 +358,23 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     for (int i = 0; i < NW * NST; ++i) mbar_init(smem_u32(&bars[i]), 1);
     fence_mbar_init();
   }
+  if (appends && row_loader) {
+    row_stage[lane] = new_row;
+    if (slot_ok) store_row();
+  }
   bad = __syncthreads_or(bad);
+  // the appended row: which staged chunk and row it replaces, -1 = none
+  int patch_chunk = -1, patch_row = 0;
+  if (appends && slot >= num_slots && tid == 0) record_error(PKV_DEV_BAD_SLOT);
+  if (slot_ok && !bad) {
+    // element offset of the last position's row through the table (the last chunk's tile plus the
+    // row within it) against the slot's: equal exactly when the table maps the position to it
+    const int last_row = (ctx - 1) % R;
+    if (chunk_off[n_chunks - 1] + static_cast<int64_t>(last_row) * D == (((slot / B) * H + h) * B + slot % B) * D) {
+      patch_chunk = n_chunks - 1;
+      patch_row = last_row;
+    }
+  }
   if (bad) {
     if (tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
     if (nparts == 1 && p.part_base == 0) {
@@ -431,15 +445,11 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     }
     const unsigned char* ks = wring + stage * C::STAGE_BYTES;
     if (warp + k * NW == patch_chunk) {
-      // the appended row replaces what the copy brought (this warp's stage, after it landed)
-      if (lane < 2 * C::CPR) {
-        const bool is_v = lane >= C::CPR;
-        const int col = is_v ? lane - C::CPR : lane;
-        *reinterpret_cast<uint4*>(const_cast<unsigned char*>(ks) + (is_v ? C::CHUNK_BYTES : 0) +
-                                  (patch_row * D + col * 8) * 2) = new_row;
-        // before a later bulk copy (async proxy) refills this stage
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      }
+      // the appended row replaces what the copy brought (this warp's stage, after it landed).  It is
+      // the warp's last chunk, so no later bulk copy refills the stage and no proxy fence is needed.
+      if (row_lane)
+        *reinterpret_cast<uint4*>(const_cast<unsigned char*>(ks) + (row_is_v ? C::CHUNK_BYTES : 0) +
+                                  (patch_row * D + row_col * 8) * 2) = row_stage[lane];
       __syncwarp();
     }
     const int c = c_begin + warp + k * NW;
@@ -607,10 +617,11 @@ constexpr int kMinPartTokens = 128;
 constexpr int kMaxPartTokens = 1024;
 
 template <int D, int R>
-constexpr size_t smem_bytes(int part_tokens) {
+constexpr size_t smem_bytes(int part_tokens, bool append) {
   using C = Cfg<D, R>;
   return static_cast<size_t>(C::NW) * C::NST * C::STAGE_BYTES + C::NW * C::NST * 8 +
-         C::NW * (D + 2) * sizeof(float) + static_cast<size_t>(part_tokens / R) * sizeof(int64_t);
+         C::NW * (D + 2) * sizeof(float) + (append ? 2 * C::CPR * 16 : 0) +
+         static_cast<size_t>(part_tokens / R) * sizeof(int64_t);
 }
 
 int device_sms(int dev) {
@@ -632,9 +643,13 @@ cudaError_t prepare_kernel(int dev) {
   static bool done[64] = {false};
   std::lock_guard<std::mutex> g(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R>,
+  cudaError_t e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes<D, R>(kMaxPartTokens)));
+                                       static_cast<int>(smem_bytes<D, R>(kMaxPartTokens, false)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<D, R>(kMaxPartTokens, true)));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -673,8 +688,12 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
     p.ws_o = p.ws_ml + ws_ml_floats(pairs);
   }
   dim3 grid(p.max_parts, p.num_heads, num_seqs);
-  e = pkv::launch_pdl(paged_attention_partition_kernel<D, R>, grid, dim3(Cfg<D, R>::NW * 32),
-                      smem_bytes<D, R>(part_tokens), st, p);
+  if (p.new_slot != nullptr)
+    e = pkv::launch_pdl(paged_attention_partition_kernel<D, R, true>, grid, dim3(Cfg<D, R>::NW * 32),
+                        smem_bytes<D, R>(part_tokens, true), st, p);
+  else
+    e = pkv::launch_pdl(paged_attention_partition_kernel<D, R, false>, grid, dim3(Cfg<D, R>::NW * 32),
+                        smem_bytes<D, R>(part_tokens, false), st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
   if (p.max_parts > 1) {
