@@ -77,10 +77,10 @@ EVENT_EVERY = 16
 # kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
 # on); a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # the headline step's fused call: partition kernel 1,373,082,000 B read + 4,771,584 B written
-    # (the appended rows included), merge kernel 1,280,500 B read (mean of two launches;
+    # the headline step's fused call: partition kernel 1,373,120,500 B read + 4,829,440 B written
+    # (the appended rows included), merge kernel 1,280,500 B read (means of two launches each;
     # profiles/paged_attention_opt13b_decode.md)
-    ("opt13b+append", "021c61e6e19b4625b9a203bcb611acf0091f72b285ae6d512971dbf720884988"): 1_379_134_000,
+    ("opt13b+append", "1b872730a3d5673c058e261c0f9dae076989907932c9e80d40249aec3422fc06"): 1_379_230_000,
 }
 
 
