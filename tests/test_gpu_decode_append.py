@@ -4,14 +4,15 @@ reshape_and_cache(key, value, slots) followed by paged_attention_decode must giv
 the same attention output and the same pools as the single fused launch, and both must match the
 fp64 oracle.  Covered: every head size and block size, one and several partitions per sequence,
 a padding slot (-1), a slot the table does not map the last position to, a slot outside the pool,
-and inputs in page-locked host memory."""
+inputs in page-locked host memory, and the full-size OPT-13B-shaped batch in the launch
+configuration the bench times."""
 import numpy as np
 import pytest
 import torch
 
 from paged_kv_cache_73_gb300 import binding as pkv
 from paged_kv_cache_73_gb300 import workloads as wl
-from tests.helpers import ATOL, max_err
+from tests.helpers import ATOL, max_err, sample_seqs
 
 pytestmark = pytest.mark.gpu
 
@@ -128,3 +129,30 @@ def test_append_reads_host_inputs(cuda_device):
     assert not got.is_cuda
     assert torch.equal(got, ref.cpu())
     assert _same_pools(pools_ref, pools_got)
+
+
+@pytest.mark.parametrize("batch", ["opt13b", "capacity_1x2048"])
+def test_append_full_size(cuda_device, batch):
+    # the OPT-13B-shaped step (1024-token partitions, as the bench times it) and one 2048-token
+    # sequence (512-token partitions, the new token in the fourth): the fused launch equals the two
+    # calls bit for bit, output and both pools; sampled sequences match the oracle on blocks
+    # regenerated on the CPU with the new rows at their slots
+    w = wl.opt13b() if batch == "opt13b" else wl.capacity(num_seqs=1, block_size=16)
+    slots = _last_slots(w)
+    ref, got, code_ref, code, pools_ref, pools_got, key, value = _both(w, slots, cuda_device)
+    assert code_ref == 0 and code == 0
+    assert torch.equal(got, ref)
+    assert _same_pools(pools_ref, pools_got)
+    del pools_ref, pools_got
+    seqs = sample_seqs(w, 6)
+    kc, vc, tabs, lens = w.compact_pools(seqs)
+    B = w.block_size
+    for i, s in enumerate(seqs):
+        last = int(lens[i]) - 1
+        blk, row = int(tabs[i, last // B]), last % B
+        kc[blk, :, row, :] = key[s].cpu()
+        vc[blk, :, row, :] = value[s].cpu()
+    from oracle import attention as oracle_attention
+    expect = oracle_attention.paged_decode_attention(w.q("cpu").numpy()[seqs], kc.numpy(), vc.numpy(), tabs, lens,
+                                                     w.scale)
+    assert max_err(got[seqs], expect) <= ATOL
