@@ -60,6 +60,32 @@ def test_attention_host_validation(lib, kw, status):
         assert lib.pkv_last_error()
 
 
+def _decode_append(lib, **kw):
+    a = dict(q=16, key=16, value=16, slots=16, k=16, v=16, tables=16, lens=16, S=2, H=2, D=64, N=8, maxb=4,
+             scale=0.125, B=16, out=16, ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.pkv_paged_attention_decode_append(a["q"], a["key"], a["value"], a["slots"], a["k"], a["v"],
+                                                 a["tables"], a["lens"], a["S"], a["H"], a["D"], a["N"], a["maxb"],
+                                                 a["scale"], a["B"], a["out"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(key=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(value=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(slots=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(key=40), pkv.PKV_ERR_INVALID_ARG),               # not 16-byte aligned
+    (dict(value=8), pkv.PKV_ERR_INVALID_ARG),
+    (dict(q=None), pkv.PKV_ERR_INVALID_ARG),               # the decode checks follow
+    (dict(D=96), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(B=12), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(S=0, key=None, value=None, slots=None), pkv.PKV_OK),   # empty batch: nothing to do
+])
+def test_decode_append_host_validation(lib, kw, status):
+    assert _decode_append(lib, **kw) == status
+    if status != pkv.PKV_OK:
+        assert lib.pkv_last_error()
+
+
 def test_workspace_size(lib):
     # one partition (<= 128 tokens of capacity) needs no workspace
     assert pkv.paged_attention_workspace_size(4, 2, 64, 8, 16) == 0
