@@ -117,6 +117,8 @@ struct Cfg {
   static constexpr int NW = 4;                       // warps per CTA
   static constexpr int RING_BYTES = 64 * 1024;       // shared-memory ring per CTA
   static constexpr int NST = RING_BYTES / (NW * STAGE_BYTES) < 8 ? RING_BYTES / (NW * STAGE_BYTES) : 8;
+  static constexpr int MAX_PART_TOKENS = 1024;       // longest partition the host plans
+  static constexpr int SPEC = (MAX_PART_TOKENS / R + NW * 32 - 1) / (NW * 32);  // table reads per thread
   static_assert(NJ >= 1 && NJ <= CPR, "row split");
   static_assert(NST >= 1, "stages");
 };
@@ -285,6 +287,20 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   if (row_loader)
     new_row = *reinterpret_cast<const uint4*>((row_is_v ? p.new_v : p.new_k) + out_off + row_col * 8);
   const int max_ctx = p.max_blocks * B;
+  // Without groups every range starts at 0, so this partition's table entries are known before the
+  // context length: they are read now, beside it, one per chunk (an index past the table row is not
+  // read).  Entries past the context are dropped once the length is known.
+  const bool spec = p.group_start == nullptr;
+  int spec_phys[C::SPEC];
+  if (spec) {
+#pragma unroll
+    for (int it = 0; it < C::SPEC; ++it) {
+      const int i = tid + it * NW * 32;
+      const int j = (part * (p.part_tokens / R) + i) / (B / R);
+      spec_phys[it] = i < p.part_tokens / R && j < p.max_blocks
+                          ? p.tables[static_cast<size_t>(s) * p.max_blocks + j] : -1;
+    }
+  }
   // this CTA's tokens: partition `part` of [start, ctx) (start = 0 unless a shared prefix precedes)
   const int ctx_full = p.lens[s];
   int first = s;
@@ -340,18 +356,23 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const int c_begin = part * chunks_per_part;
   const int n_chunks = min(chunks_per_part, total_chunks - c_begin);
 
-  // Table slice of this partition -> element offset of each chunk's K (and V) tile.
+  // Table slice of this partition -> element offset of each chunk's K (and V) tile
+  // (n_chunks <= MAX_PART_TOKENS / R: SPEC passes cover it).
   int bad = 0;
-  for (int i = tid; i < n_chunks; i += NW * 32) {
-    const int c = c_begin + i;
-    const int j = c / chunks_per_block;
-    const int sub = c - j * chunks_per_block;
-    const int phys = p.tables[static_cast<size_t>(s) * p.max_blocks + block0 + j];
-    if (phys < 0 || phys >= p.num_blocks) {
-      bad = 1;
-      chunk_off[i] = 0;
-    } else {
-      chunk_off[i] = ((static_cast<int64_t>(phys) * H + h) * B + sub * R) * D;
+#pragma unroll
+  for (int it = 0; it < C::SPEC; ++it) {
+    const int i = tid + it * NW * 32;
+    if (i < n_chunks) {
+      const int c = c_begin + i;
+      const int j = c / chunks_per_block;
+      const int sub = c - j * chunks_per_block;
+      const int phys = spec ? spec_phys[it] : p.tables[static_cast<size_t>(s) * p.max_blocks + block0 + j];
+      if (phys < 0 || phys >= p.num_blocks) {
+        bad = 1;
+        chunk_off[i] = 0;
+      } else {
+        chunk_off[i] = ((static_cast<int64_t>(phys) * H + h) * B + sub * R) * D;
+      }
     }
   }
   if (tid == 0) {
@@ -615,6 +636,7 @@ __host__ __device__ constexpr size_t ws_ml_floats(size_t pairs) { return (pairs 
 // ---- host side ---------------------------------------------------------------------------------
 constexpr int kMinPartTokens = 128;
 constexpr int kMaxPartTokens = 1024;
+static_assert(kMaxPartTokens == Cfg<128, 16>::MAX_PART_TOKENS, "the kernel's table pass covers the longest partition");
 
 template <int D, int R>
 constexpr size_t smem_bytes(int part_tokens, bool append) {
@@ -675,6 +697,8 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = prepare_kernel<D, R>(dev);
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention setup: %s", cudaGetErrorString(e));
+  if (part_tokens > kMaxPartTokens || part_tokens % R != 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "paged attention: partition of %d tokens", part_tokens);
   const int max_ctx = p.max_blocks * p.block_size;
   p.part_tokens = part_tokens;
   p.max_parts = (max_ctx + part_tokens - 1) / part_tokens + p.part_base;
