@@ -77,10 +77,10 @@ EVENT_EVERY = 16
 # kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
 # on); a changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # the headline step's fused call: partition kernel 1,373,120,500 B read + 4,829,440 B written
-    # (the appended rows included), merge kernel 1,280,500 B read (means of two launches each;
+    # the headline step's fused call: partition kernel 1,373,092,500 B read + 4,835,200 B written
+    # (the appended rows included), merge kernel 1,280,000 B read (means of two launches each;
     # profiles/paged_attention_opt13b_decode.md)
-    ("opt13b+append", "1b872730a3d5673c058e261c0f9dae076989907932c9e80d40249aec3422fc06"): 1_379_230_000,
+    ("opt13b+append", "671088f0e41c98d54388d9adf6d37918ab4fe62f8d2a93ac461b7372c3e93531"): 1_379_208_000,
 }
 
 
