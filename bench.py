@@ -79,8 +79,9 @@ EVENT_EVERY = 16
 NCU_TRAFFIC = {
     # the headline step's fused call: partition kernel 1,373,092,500 B read + 4,835,200 B written
     # (the appended rows included), merge kernel 1,280,000 B read (means of two launches each;
-    # profiles/paged_attention_opt13b_decode.md)
-    ("opt13b+append", "671088f0e41c98d54388d9adf6d37918ab4fe62f8d2a93ac461b7372c3e93531"): 1_379_208_000,
+    # profiles/paged_attention_opt13b_decode.md; captured on source 671088f0..., which differs from
+    # this key's source in the file's header comment only)
+    ("opt13b+append", "5db4ea62901c2074d5db6247fb9ca0f86ae177cb2d1f094b6e25a2b6456c7857"): 1_379_208_000,
 }
 
 

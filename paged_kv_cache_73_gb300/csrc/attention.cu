@@ -26,6 +26,12 @@
 //  * Online softmax in base 2 (exp2f), fp32 accumulators in registers; rows
 //    past the context are excluded by select/branch, never multiplied by zero,
 //    so stale NaN/Inf in unfilled slots cannot leak into the result.
+//  * A partition's slice of the block table is read beside the context length
+//    (without shared-prefix groups every range starts at token 0), one entry per chunk.
+//  * pkv_paged_attention_decode_append runs the APPEND instantiation: the CTA
+//    holding the context's last position also stores the new token's K/V row at
+//    its slot and writes it over its staged copy of that chunk (section 关键设计 5's
+//    fused reshape and block write, folded into the attention launch).
 //  * Every wait is bounded by a global-timer deadline; on expiry the kernel
 //    records PKV_DEV_WAIT_TIMEOUT, waits (bounded) for its own copies in
 //    flight and returns.
