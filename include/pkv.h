@@ -102,7 +102,9 @@ int pkv_device_error(void* stream, int reset, int* code);
  * with k_t = k_cache[block_tables[s, t / B], h, t % B, :] (v_t likewise) and
  * ctx_s = context_lens[s].  The softmax normalises over all ctx_s tokens.
  * ctx_s = 0 gives a zero row.  Table entries at column >= ceil(ctx_s / B) are
- * never read.  Accumulation is fp32; out is rounded to nearest even.
+ * never used and may hold anything: they can be read (within the table row),
+ * but no K/V is fetched through them and they are not checked.  Accumulation is
+ * fp32; out is rounded to nearest even.
  *
  *   q            device [num_seqs, num_heads, head_dim] fp16, 16-byte aligned
  *   k_cache,

@@ -89,7 +89,7 @@ def test_garbage_in_unused_table_columns_is_ignored(cuda_device):
     q, k, v, tables, lens = device_inputs(w, cuda_device)
     base = gpu_attention(w, cuda_device, (q, k, v, tables, lens))
     junk = tables.clone()
-    junk[junk < 0] = 123456789                       # far outside the pool, never read
+    junk[junk < 0] = 123456789                       # far outside the pool, never used
     assert torch.equal(gpu_attention(w, cuda_device, (q, k, v, junk, lens)), base)
 
 
