@@ -1081,8 +1081,8 @@ def main():
     r = run_gpu(args, rank, world, dev)
 
     # whole-job numbers: bytes of all ranks over the slowest rank's time
-    (step_ms, e2e_ms, attn_ms, staged_ms), (kv_total, phys_total) = reduce_over_ranks(
-        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"], r.get("e2e_staged_ms", 0.0)],
+    (step_ms, e2e_ms, attn_ms, staged_ms, attn_med), (kv_total, phys_total) = reduce_over_ranks(
+        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"], r.get("e2e_staged_ms", 0.0), r["attn_ms_median"]],
         [float(r["kv_bytes"]), float(r["phys_bytes"])],
         world, dev)
 
@@ -1116,7 +1116,7 @@ def main():
                               "bytes = distinct K/V slots + q + out",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
-                         "launch_ms": attn_ms, "timed_launches": args.steps if r["l2_flushed"] else (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
+                         "launch_ms": attn_ms, "launch_ms_median": attn_med, "timed_launches": args.steps if r["l2_flushed"] else (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
                          "peak_source": peak_src + ", of measured"},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
