@@ -1042,6 +1042,59 @@ def run_reference(args, rank):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def headline_line(args, r, world, cpu, step_ms, e2e_ms, attn_ms, staged_ms, attn_med, kv_total, phys_total):
+    """The JSON line of a decode run: `r` is this rank's run_gpu result, the times (ms) are maxima
+    over ranks and the byte counts sums over ranks."""
+    peak, peak_src = measured_hbm_peak()
+    achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
+    traffic = None if args.grouped else NCU_TRAFFIC.get(
+        (args.workload + ("+append" if r["fused"] else ""), attention_source_sha()))
+    value = kv_total / (step_ms * 1e-3) / 1e9
+    S = r["num_seqs"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
+        "config": config_block(args, r["desc"], S,
+                               {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                                "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"],
+                                "pool_blocks": r["num_blocks"]}, flushed=r["l2_flushed"]),
+        "hbm_frac_of_measured": value / peak,
+        "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
+        "physical_kv_GBps": phys_total / (step_ms * 1e-3) / 1e9,
+        "tokens_per_s": S * world / (step_ms * 1e-3),
+        "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
+        "host_slot_assignment_us": r["host_slot_us"],
+        "roofline": {"bound": "hbm",
+                     "kernel": ("paged attention call with the new tokens' K/V append (partition + merge "
+                                "kernels); bytes include the appended rows read and written"
+                                if r["fused"] else "paged attention call (partition + merge kernels)")
+                     if r["grouped"] is None
+                     else "shared-prefix attention call (prefix partials on tensor cores + partition + merge); "
+                          "bytes = distinct K/V slots + q + out",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
+                     "launch_ms": attn_ms, "launch_ms_median": attn_med,
+                     "timed_launches": args.steps if r["l2_flushed"] else (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
+                     "peak_source": peak_src + ", of measured"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if r["copy"] is not None:
+        line["copy_blocks_setup"] = r["copy"]
+    if r["grouped"] is not None:
+        line["grouped"] = r["grouped"]
+    if "e2e_step_ms" in r:
+        line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                       "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                       "ms_per_step": e2e_ms, "launch": r.get("launch", "eager API calls"),
+                       "staged_value": kv_total / (staged_ms * 1e-3) / 1e9,
+                       "staged_ms_per_step": staged_ms}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -1087,52 +1140,8 @@ def main():
         world, dev)
 
     if rank == 0:
-        peak, peak_src = measured_hbm_peak()
-        achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
-        traffic = None if args.grouped else NCU_TRAFFIC.get(
-            (args.workload + ("+append" if r["fused"] else ""), attention_source_sha()))
-        value = kv_total / (step_ms * 1e-3) / 1e9
-        S = r["num_seqs"]
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
-            "config": config_block(args, r["desc"], S,
-                                   {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                    "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"],
-                                    "pool_blocks": r["num_blocks"]}, flushed=r["l2_flushed"]),
-            "hbm_frac_of_measured": value / peak,
-            "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
-            "physical_kv_GBps": phys_total / (step_ms * 1e-3) / 1e9,
-            "tokens_per_s": S * world / (step_ms * 1e-3),
-            "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
-            "host_slot_assignment_us": r["host_slot_us"],
-            "roofline": {"bound": "hbm",
-                         "kernel": ("paged attention call with the new tokens' K/V append (partition + merge "
-                                    "kernels); bytes include the appended rows read and written"
-                                    if r["fused"] else "paged attention call (partition + merge kernels)")
-                         if r["grouped"] is None
-                         else "shared-prefix attention call (prefix partials on tensor cores + partition + merge); "
-                              "bytes = distinct K/V slots + q + out",
-                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
-                         "launch_ms": attn_ms, "launch_ms_median": attn_med, "timed_launches": args.steps if r["l2_flushed"] else (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
-                         "peak_source": peak_src + ", of measured"},
-            "gpu_launches": r["launches"],
-            "clocks": r["clocks"],
-        }
-        if r["copy"] is not None:
-            line["copy_blocks_setup"] = r["copy"]
-        if r["grouped"] is not None:
-            line["grouped"] = r["grouped"]
-        if "e2e_step_ms" in r:
-            line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
-                           "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                           "ms_per_step": e2e_ms, "launch": r.get("launch", "eager API calls"),
-                           "staged_value": kv_total / (staged_ms * 1e-3) / 1e9,
-                           "staged_ms_per_step": staged_ms}
-        if cpu is not None:
-            line["cpu_baseline"] = cpu
+        line = headline_line(args, r, world, cpu, step_ms, e2e_ms, attn_ms, staged_ms, attn_med, kv_total,
+                             phys_total)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
