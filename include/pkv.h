@@ -423,6 +423,27 @@ int pkv_bm_beam_step(pkv_bm* bm, const int64_t* parents, const int64_t* children
                      const int64_t* retire, int n_retire, int64_t* slots_out, int64_t* cow_pairs_out,
                      int* num_cow);
 
+/* Swapping ([lecture] 调度和抢占, Swapping; [guide] 05): the sequences
+ * seq_ids (host [n], distinct) -- a preempted group, such as a request's
+ * samples or beams -- move whole from src to dst, typically the managers of
+ * an HBM pool and of a page-locked host pool with the same block size.
+ * Every distinct physical block the group maps gets one block taken from
+ * dst's free list, in order of first appearance (sequences in the given
+ * order, each in logical order), and keeps its reference count; the
+ * sequences keep their logical layout and sharing; the old blocks return to
+ * src's free list in the same order.  pairs_out (host [cap_pairs, 2] int64)
+ * receives the moves (src block, dst block), *n_pairs their number: the
+ * block_mapping for pkv_swap_blocks, which the caller runs before the
+ * sequences are used on dst's pool.
+ * The group must hold every reference to its blocks: a block also held by
+ * another sequence or by a registered prefix is PKV_ERR_INVALID_ARG.
+ * PKV_ERR_OOM if dst has too few free blocks, PKV_ERR_NOT_FOUND for an id not
+ * on src, PKV_ERR_INVALID_ARG for an id already on dst, a repeated id,
+ * different block sizes or cap_pairs too small.  All-or-nothing: on any error
+ * neither manager changes. */
+int pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seq_ids, int n, int64_t* pairs_out,
+                int cap_pairs, int* n_pairs);
+
 /* Reference count of a physical block (negative status on a bad id). */
 int pkv_bm_ref_count(const pkv_bm* bm, int32_t block);
 

@@ -42,6 +42,14 @@ Readings where the pages are silent or garbled (each test pins one):
   that writes into a partly filled last prefix block always copies it.
 * Running out of blocks raises ``MemoryError`` and changes nothing.
 * slot = physical id * B + row.
+* Swapping ([lecture] 调度和抢占; [guide] 05): a preempted group of sequences
+  moves, whole, to a second manager that tracks a host pool, and back the same
+  way.  The group must hold every reference to its blocks (its samples or beams
+  share blocks with each other, not with sequences left behind, and not with a
+  registered prefix); each distinct block gets one block on the other side, in
+  order of first appearance (sequences in the given order, each in logical
+  order), and carries its reference count; the old blocks return to their free
+  list in the same order.
 """
 from __future__ import annotations
 
@@ -224,3 +232,46 @@ class BlockManager:
         for r in retire:
             self.free(r)
         return [self.append_slot(c) for c in children]
+
+
+# -- swapping ------------------------------------------------------------------
+def swap(src: BlockManager, dst: BlockManager, seq_ids: Sequence[int]) -> List[Tuple[int, int]]:
+    """Move the sequences ``seq_ids`` (a whole group) from ``src`` to ``dst``.
+
+    Returns the block moves [(src block, dst block)] the caller makes with
+    swap_blocks before the sequences run again on ``dst``'s pool.  All or
+    nothing: a bad id, a block the group does not hold alone, or a short free
+    list on ``dst`` (MemoryError) changes neither manager.
+    """
+    ids = [int(s) for s in seq_ids]
+    if src is dst or src.B != dst.B:
+        raise ValueError("swap needs two managers with the same block size")
+    if len(set(ids)) != len(ids):
+        raise ValueError("a sequence is listed twice")
+    if any(s not in src.seqs for s in ids):
+        raise KeyError("unknown sequence")
+    if any(s in dst.seqs for s in ids):
+        raise ValueError("a sequence already exists on the destination")
+    held: Dict[int, int] = {}                 # block -> references the group holds
+    order: List[int] = []                     # distinct blocks, first appearance first
+    for s in ids:
+        for b in src.seqs[s]:
+            if b.physical not in held:
+                held[b.physical] = 0
+                order.append(b.physical)
+            held[b.physical] += 1
+    for b in order:
+        if held[b] != src.ref[b]:
+            raise ValueError(f"block {b} is also held outside the group")
+    dst._need(len(order))
+    moved = {}
+    for b in order:
+        nb = dst._take()
+        dst.ref[nb] = src.ref[b]
+        moved[b] = nb
+    for s in ids:
+        dst.seqs[s] = [LogicalBlock(moved[b.physical], b.filled) for b in src.seqs.pop(s)]
+    for b in order:
+        src.ref[b] = 0
+        src.free_list.append(b)
+    return [(b, moved[b]) for b in order]

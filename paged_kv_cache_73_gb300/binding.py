@@ -80,6 +80,7 @@ _SIGNATURES = {
     "pkv_bm_block_table": (_I, [_P, _I64, _P, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_bm_block_tables": (_I, [_P, _P, _I, _P, _I, _P]),
     "pkv_bm_beam_step": (_I, [_P, _P, _P, _I, _P, _I, _P, _P, _c.POINTER(_I)]),
+    "pkv_bm_swap": (_I, [_P, _P, _P, _I, _P, _I, _c.POINTER(_I)]),
     "pkv_bm_ref_count": (_I, [_P, _c.c_int32]),
     "pkv_bm_stats": (_I, [_P, _c.POINTER(_I), _c.POINTER(_I64), _c.POINTER(_I64)]),
 }
@@ -554,6 +555,17 @@ class BlockManager:
         _check(self._lib.pkv_bm_beam_step(self._h, _np_ptr(par), _np_ptr(chi), k, _np_ptr(ret), ret.shape[0],
                                           _np_ptr(slots), _np_ptr(pairs), ctypes.byref(nc)))
         return slots[:k], pairs[:nc.value]
+
+    def swap_to(self, dst: "BlockManager", seq_ids: Sequence[int]) -> np.ndarray:
+        """Move the group ``seq_ids`` to ``dst`` (pkv_bm_swap).  Returns the [P, 2] int64 block moves
+        (this manager's block, dst's block): the block_mapping for swap_blocks."""
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        cap = sum(len(self.block_table(int(s))[0]) for s in ids)       # an upper bound on distinct blocks
+        pairs = np.empty((max(cap, 1), 2), dtype=np.int64)
+        n = _c.c_int(0)
+        _check(self._lib.pkv_bm_swap(self._h, dst._h, _np_ptr(ids), ids.shape[0], _np_ptr(pairs), cap,
+                                     ctypes.byref(n)))
+        return pairs[:n.value]
 
     def ref_count(self, block: int) -> int:
         r = self._lib.pkv_bm_ref_count(self._h, block)

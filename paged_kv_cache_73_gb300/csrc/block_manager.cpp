@@ -374,6 +374,68 @@ int pkv_bm_beam_step(pkv_bm* bm, const int64_t* parents, const int64_t* children
   return PKV_OK;
 }
 
+int pkv_bm_swap(pkv_bm* src_bm, pkv_bm* dst_bm, const int64_t* seq_ids, int n, int64_t* pairs_out, int cap_pairs,
+                int* n_pairs) {
+  // [lecture] 调度和抢占 (Swapping), [guide] 05: a preempted group leaves one pool whole and
+  // comes back whole; every check comes before the first change.
+  if (!src_bm || !dst_bm || src_bm == dst_bm)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: two distinct managers needed");
+  Manager* src = M(src_bm);
+  Manager* dst = M(dst_bm);
+  if (src->B != dst->B)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: block sizes differ (%d, %d)", src->B, dst->B);
+  if (n < 0 || (n > 0 && (!seq_ids || !n_pairs)) || cap_pairs < 0 || (cap_pairs > 0 && !pairs_out))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: bad arguments");
+  std::unordered_map<int64_t, int> seen;
+  for (int i = 0; i < n; ++i) {
+    if (!seen.emplace(seq_ids[i], i).second)
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: sequence %lld listed twice", (long long)seq_ids[i]);
+    if (!src->seqs.count(seq_ids[i]))
+      return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_swap: unknown sequence %lld", (long long)seq_ids[i]);
+    if (dst->seqs.count(seq_ids[i]))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: sequence %lld exists on the destination",
+                       (long long)seq_ids[i]);
+  }
+  // distinct blocks in order of first appearance, with the references the group holds
+  std::unordered_map<int32_t, int> held;
+  std::vector<int32_t> order;
+  for (int i = 0; i < n; ++i) {
+    for (const Logical& lb : src->seqs[seq_ids[i]]) {
+      auto ins = held.emplace(lb.phys, 0);
+      if (ins.second) order.push_back(lb.phys);
+      ins.first->second += 1;
+    }
+  }
+  for (int32_t b : order)
+    if (held[b] != src->ref[b])
+      return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: block %d is also held outside the group", b);
+  if ((int)order.size() > (int)dst->free_list.size()) return oom(dst, (int)order.size());
+  if ((int)order.size() > cap_pairs)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_swap: %d block moves, room for %d", (int)order.size(), cap_pairs);
+  std::unordered_map<int32_t, int32_t> moved;
+  for (size_t i = 0; i < order.size(); ++i) {
+    const int32_t b = order[i];
+    const int32_t nb = dst->take();
+    dst->ref[nb] = src->ref[b];
+    moved[b] = nb;
+    pairs_out[2 * i] = b;
+    pairs_out[2 * i + 1] = nb;
+  }
+  for (int i = 0; i < n; ++i) {
+    auto it = src->seqs.find(seq_ids[i]);
+    std::vector<Logical> blocks = std::move(it->second);
+    src->seqs.erase(it);
+    for (Logical& lb : blocks) lb.phys = moved[lb.phys];
+    dst->seqs.emplace(seq_ids[i], std::move(blocks));
+  }
+  for (int32_t b : order) {
+    src->ref[b] = 0;
+    src->free_list.push_back(b);
+  }
+  if (n_pairs) *n_pairs = (int)order.size();
+  return PKV_OK;
+}
+
 int pkv_bm_ref_count(const pkv_bm* bm, int32_t block) {
   if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_ref_count: null manager");
   const Manager* m = M(bm);

@@ -264,3 +264,95 @@ def test_beam_step_errors_leave_state_unchanged():
     assert bm.block_table(0) == ([0, 1], 6) and bm.stats()[0] == 2
     slots, pairs = bm.beam_step([0, 0, 0], [1, 2, 3], [0])
     assert len(pairs) == 2 and bm.stats()[0] == 0
+
+
+@pytest.mark.parametrize("B,N,M,seed", [(4, 48, 32, 0), (16, 40, 24, 1), (1, 60, 60, 2)])
+def test_random_group_swaps_match_oracle(B, N, M, seed):
+    # request groups (a prompt and its forks) grow on a device manager, are swapped out whole to a
+    # host manager and back: the same moves, tables, reference counts and free lists on both sides
+    rng = np.random.default_rng(200 + seed)
+    od, oh = rng.permutation(N), rng.permutation(M)
+    nat_d, nat_h = pkv.BlockManager(N, B, od), pkv.BlockManager(M, B, oh)
+    ora_d, ora_h = obm.BlockManager(N, B, od), obm.BlockManager(M, B, oh)
+    on_dev, on_host = [], []
+    nid = 0
+    swaps = 0
+    for step in range(600):
+        op = int(rng.integers(0, 6))
+        if op == 0 or not (on_dev or on_host):
+            n, plen = int(rng.integers(1, 4)), int(rng.integers(1, 4 * B + 1))
+            try:
+                ora_d.add_seq(nid, plen)
+            except MemoryError:
+                with pytest.raises(pkv.PkvOutOfBlocks):
+                    nat_d.add_seq(nid, plen)
+                continue
+            nat_d.add_seq(nid, plen)
+            for i in range(1, n):
+                ora_d.fork(nid, nid + i)
+                nat_d.fork(nid, nid + i)
+            on_dev.append(list(range(nid, nid + n)))
+            nid += n
+        elif op in (1, 2) and on_dev:
+            g = on_dev[int(rng.integers(0, len(on_dev)))]
+            s = int(rng.choice(g))
+            try:
+                want = ora_d.append_slot(s)
+            except MemoryError:
+                with pytest.raises(pkv.PkvOutOfBlocks):
+                    nat_d.append_slot(s)
+                continue
+            assert nat_d.append_slot(s) == want
+        elif op == 3 and on_dev:
+            i = int(rng.integers(0, len(on_dev)))
+            try:
+                want = obm.swap(ora_d, ora_h, on_dev[i])
+            except MemoryError:
+                with pytest.raises(pkv.PkvOutOfBlocks):
+                    nat_d.swap_to(nat_h, on_dev[i])
+                continue
+            assert nat_d.swap_to(nat_h, on_dev[i]).tolist() == [list(p) for p in want]
+            on_host.append(on_dev.pop(i))
+            swaps += 1
+        elif op == 4 and on_host:
+            i = int(rng.integers(0, len(on_host)))
+            try:
+                want = obm.swap(ora_h, ora_d, on_host[i])
+            except MemoryError:
+                with pytest.raises(pkv.PkvOutOfBlocks):
+                    nat_h.swap_to(nat_d, on_host[i])
+                continue
+            assert nat_h.swap_to(nat_d, on_host[i]).tolist() == [list(p) for p in want]
+            on_dev.append(on_host.pop(i))
+            swaps += 1
+        elif op == 5 and len(on_dev) > 1:
+            for s in on_dev.pop(int(rng.integers(0, len(on_dev)))):
+                ora_d.free(s)
+                nat_d.free(s)
+        if step % 25 == 0:
+            _compare(nat_d, ora_d, [s for g in on_dev for s in g], N)
+            _compare(nat_h, ora_h, [s for g in on_host for s in g], M)
+    _compare(nat_d, ora_d, [s for g in on_dev for s in g], N)
+    _compare(nat_h, ora_h, [s for g in on_host for s in g], M)
+    assert swaps >= 20
+
+
+def test_group_swap_errors_leave_state_unchanged():
+    dev, host = pkv.BlockManager(16, 4), pkv.BlockManager(2, 4)
+    dev.add_seq(0, 6)
+    dev.fork(0, 1)
+    dev.add_seq(2, 9)
+    state = ([dev.block_table(s) for s in (0, 1, 2)], dev.stats(), host.stats())
+    with pytest.raises(pkv.PkvError):
+        dev.swap_to(host, [0])                             # its sibling holds the same blocks
+    with pytest.raises(pkv.PkvOutOfBlocks):
+        dev.swap_to(host, [2])                             # 3 blocks, the host has 2
+    with pytest.raises(pkv.PkvError):
+        dev.swap_to(host, [0, 1, 0])
+    with pytest.raises(pkv.PkvError):
+        dev.swap_to(dev, [2])
+    other = pkv.BlockManager(16, 8)
+    with pytest.raises(pkv.PkvError):
+        dev.swap_to(other, [2])                            # block sizes differ
+    assert state == ([dev.block_table(s) for s in (0, 1, 2)], dev.stats(), host.stats())
+    assert dev.swap_to(host, [0, 1]).shape == (2, 2)       # the whole group fits

@@ -87,3 +87,45 @@ def test_swap_bad_pair_recorded(cuda_device):
     before = hk[0].clone()
     pkv.swap_blocks(dk, dv, hk, hv, torch.tensor([[1, 2]], dtype=torch.int64, device=cuda_device))
     assert pkv.device_error() == 4 and torch.equal(hk[0], before)
+
+
+def test_preempted_group_round_trip_keeps_attention(cuda_device):
+    # a request's four samples are preempted: the block manager moves the group to the host pool's
+    # manager, swap_blocks copies the group's blocks out, the freed device blocks are overwritten,
+    # and the group comes back into other device blocks; attention over the restored tables is the
+    # same, bit for bit (the kernel's result does not depend on physical ids)
+    B, H, D, N, M, maxb = 16, 4, 128, 96, 64, 24
+    dev_bm = pkv.BlockManager(N, B, np.random.default_rng(1).permutation(N))
+    host_bm = pkv.BlockManager(M, B, np.random.default_rng(2).permutation(M))
+    dev_bm.add_seq(0, 300)
+    for c in (1, 2, 3):
+        dev_bm.fork(0, c)
+    for s in range(4):
+        dev_bm.append_slot(s)                               # copies of the shared partly filled block
+    dev_bm.add_seq(10, 200)                                 # another request, left on the device
+    group = [0, 1, 2, 3]
+    k = wl.dense_tensor((N, H, B, D), 700, wl.STREAM_K, cuda_device)
+    v = wl.dense_tensor((N, H, B, D), 700, wl.STREAM_V, cuda_device)
+    q = wl.dense_tensor((len(group), H, D), 701, wl.STREAM_Q, cuda_device)
+    hk = torch.zeros((M, H, B, D), dtype=torch.float16).pin_memory()
+    hv = torch.zeros((M, H, B, D), dtype=torch.float16).pin_memory()
+
+    def attend():
+        tables, lens = dev_bm.block_tables(group, maxb)
+        return pkv.paged_attention_decode(q, k, v, torch.from_numpy(tables).to(cuda_device),
+                                          torch.from_numpy(lens).to(cuda_device), D ** -0.5, B)
+
+    before = attend()
+    out_pairs = dev_bm.swap_to(host_bm, group)
+    pkv.swap_blocks([k], [v], [hk], [hv], torch.from_numpy(out_pairs).to(cuda_device))
+    freed = torch.from_numpy(out_pairs[:, 0]).to(cuda_device)
+    k[freed] = float("nan")                                 # reused by someone else meanwhile
+    v[freed] = float("nan")
+    dev_bm.add_seq(20, B * 3)
+    in_pairs = host_bm.swap_to(dev_bm, group)
+    pkv.swap_blocks([hk], [hv], [k], [v], torch.from_numpy(in_pairs).to(cuda_device))
+    after = attend()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert len(out_pairs) == len(in_pairs) == 19 + 3         # 18 shared full blocks + the partial + 3 copies
+    assert torch.equal(before, after)

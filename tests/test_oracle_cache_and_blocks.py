@@ -367,3 +367,101 @@ def test_swap_out_and_back_restores_blocks():
     for layer in range(L):
         for (s0, _), (_, d1) in zip(out_map, back_map):
             np.testing.assert_array_equal(dev_k[layer][d1], orig_k[layer][s0])
+
+
+# -- swapping a preempted group between two managers ([lecture] 调度和抢占; [guide] 05) ----------
+def _layout(bm, seqs):
+    """Each sequence's fills, and which (sequence, logical block) positions share a physical block:
+    everything of the state that does not depend on physical ids."""
+    fills = {s: bm.filled(s) for s in seqs}
+    where = {}
+    for s in seqs:
+        for j, phys in enumerate(bm.block_table(s)[0]):
+            where.setdefault(phys, []).append((s, j))
+    classes = sorted(sorted(v) for v in where.values())
+    refs = sorted((sorted(v), bm.ref_count(p)) for p, v in where.items())
+    return fills, classes, refs
+
+
+def _request_group(bm, first_id, prompt_len, n):
+    """A request's n samples: one prompt, n-1 forks, one appended token each (copy-on-write)."""
+    bm.add_seq(first_id, prompt_len)
+    for i in range(1, n):
+        bm.fork(first_id, first_id + i)
+    for i in range(n):
+        bm.append_slot(first_id + i)
+    return list(range(first_id, first_id + n))
+
+
+def test_group_swap_round_trip_keeps_layout_and_sharing():
+    dev = obm.BlockManager(40, 4, list(np.random.default_rng(3).permutation(40)))
+    host = obm.BlockManager(30, 4, list(np.random.default_rng(4).permutation(30)))
+    group = _request_group(dev, 0, 10, 4)                  # 3 blocks: 2 shared full, 1 shared partial + copies
+    other = _request_group(dev, 10, 6, 2)                  # stays on the device
+    before = _layout(dev, group)
+    other_before = [dev.block_table(s) for s in other]
+    distinct = {p for s in group for p in dev.block_table(s)[0]}
+    free_dev, free_host = dev.num_free(), host.num_free()
+    pairs = obm.swap(dev, host, group)
+    # one move per distinct block, each side's blocks distinct, the sources exactly the group's blocks
+    assert len(pairs) == len(distinct)
+    assert {s for s, _ in pairs} == distinct and len({d for _, d in pairs}) == len(pairs)
+    assert dev.num_free() == free_dev + len(pairs) and host.num_free() == free_host - len(pairs)
+    assert all(s not in dev.seqs for s in group) and _layout(host, group) == before
+    assert all(dev.ref_count(s) == 0 for s, _ in pairs)
+    assert [dev.block_table(s) for s in other] == other_before
+    # the freed device blocks are reused meanwhile; the group comes back into other blocks
+    dev.add_seq(99, 4 * len(pairs))
+    back = obm.swap(host, dev, group)
+    assert len(back) == len(pairs) and _layout(dev, group) == before
+    assert host.num_free() == free_host and not host.seqs
+    # a moved block is the same block: the pairs compose to a map from old to new device ids
+    old_to_new = {s0: d1 for (s0, h0) in pairs for (h1, d1) in back if h0 == h1}
+    assert len(old_to_new) == len(pairs)
+
+
+def test_group_swap_keeps_copy_on_write_pending():
+    # two samples share a partly filled last block when swapped; after coming back, the first to
+    # write still copies it and the second writes in place
+    dev = obm.BlockManager(16, 4)
+    host = obm.BlockManager(16, 4)
+    dev.add_seq(0, 6)
+    dev.fork(0, 1)
+    obm.swap(dev, host, [0, 1])
+    obm.swap(host, dev, [0, 1])
+    last = dev.block_table(0)[0][-1]
+    assert dev.ref_count(last) == 2
+    _, src, dst = dev.append_slot(0)
+    assert src == last and dst >= 0
+    assert dev.append_slot(1)[1:] == (-1, -1)
+
+
+def test_group_swap_refuses_a_block_held_outside_the_group():
+    dev = obm.BlockManager(16, 4)
+    host = obm.BlockManager(16, 4)
+    dev.add_seq(0, 6)
+    dev.fork(0, 1)
+    pid_slots = dev.register_prefix(7, 8)
+    dev.add_seq_with_prefix(2, 7)
+    state = (list(dev.free_list), {s: dev.block_table(s) for s in dev.seqs}, list(dev.ref))
+    with pytest.raises(ValueError):
+        obm.swap(dev, host, [0])                           # its sibling holds the same blocks
+    with pytest.raises(ValueError):
+        obm.swap(dev, host, [2])                           # the registered prefix holds its blocks
+    with pytest.raises(ValueError):
+        obm.swap(dev, host, [0, 0, 1])
+    with pytest.raises(KeyError):
+        obm.swap(dev, host, [0, 1, 5])
+    assert state == (list(dev.free_list), {s: dev.block_table(s) for s in dev.seqs}, list(dev.ref))
+    assert host.num_free() == 16 and not host.seqs and len(pid_slots) == 8
+
+
+def test_group_swap_out_of_blocks_changes_nothing():
+    dev = obm.BlockManager(16, 4)
+    host = obm.BlockManager(2, 4)
+    dev.add_seq(0, 9)                                      # 3 blocks, the host has 2
+    state = (list(dev.free_list), dev.block_table(0), list(dev.ref))
+    with pytest.raises(MemoryError):
+        obm.swap(dev, host, [0])
+    assert state == (list(dev.free_list), dev.block_table(0), list(dev.ref))
+    assert host.num_free() == 2 and not host.seqs
