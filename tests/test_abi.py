@@ -86,6 +86,73 @@ def test_decode_append_host_validation(lib, kw, status):
         assert lib.pkv_last_error()
 
 
+def _prefill(lib, **kw):
+    a = dict(q=16, k=16, v=16, tables=16, lens=16, qs=16, S=2, T=8, maxq=4, H=2, D=64, N=8, maxb=4, scale=0.125,
+             B=16, out=16)
+    a.update(kw)
+    return lib.pkv_paged_attention_prefill(a["q"], a["k"], a["v"], a["tables"], a["lens"], a["qs"], a["S"], a["T"],
+                                           a["maxq"], a["H"], a["D"], a["N"], a["maxb"], a["scale"], a["B"],
+                                           a["out"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(B=12), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(H=0), pkv.PKV_ERR_INVALID_ARG),
+    (dict(T=-1), pkv.PKV_ERR_INVALID_ARG),
+    (dict(qs=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(out=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(k=40), pkv.PKV_ERR_INVALID_ARG),                 # not 16-byte aligned
+    (dict(scale=0.0), pkv.PKV_ERR_INVALID_ARG),            # the causal max needs scale > 0
+    (dict(scale=float("nan")), pkv.PKV_ERR_INVALID_ARG),
+    (dict(T=0), pkv.PKV_OK),                               # no new tokens: nothing to do
+])
+def test_prefill_host_validation(lib, kw, status):
+    assert _prefill(lib, **kw) == status
+    if status != pkv.PKV_OK:
+        assert lib.pkv_last_error()
+
+
+def _shared_prefix(lib, **kw):
+    a = dict(q=16, k=16, v=16, tables=16, lens=16, gs=16, pl=16, G=1, maxg=2, S=2, H=2, D=64, N=8, maxb=4,
+             scale=0.125, B=16, out=16, ws=16, ws_bytes=1 << 20)
+    a.update(kw)
+    return lib.pkv_paged_attention_decode_shared_prefix(a["q"], a["k"], a["v"], a["tables"], a["lens"], a["gs"],
+                                                        a["pl"], a["G"], a["maxg"], a["S"], a["H"], a["D"], a["N"],
+                                                        a["maxb"], a["scale"], a["B"], a["out"], a["ws"],
+                                                        a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(B=2), pkv.PKV_ERR_UNSUPPORTED),
+    (dict(G=0), pkv.PKV_ERR_INVALID_ARG),
+    (dict(maxg=0), pkv.PKV_ERR_INVALID_ARG),
+    (dict(gs=None), pkv.PKV_ERR_INVALID_ARG),
+    (dict(ws=None), pkv.PKV_ERR_INVALID_ARG),              # the prefix partials always need a workspace
+    (dict(ws=24), pkv.PKV_ERR_INVALID_ARG),
+    (dict(scale=-1.0), pkv.PKV_ERR_INVALID_ARG),
+    (dict(S=0), pkv.PKV_OK),
+])
+def test_shared_prefix_host_validation(lib, kw, status):
+    assert _shared_prefix(lib, **kw) == status
+    if status != pkv.PKV_OK:
+        assert lib.pkv_last_error()
+
+
+def test_multi_layer_reshape_host_validation(lib):
+    ptrs = lambda *xs: ctypes.cast((ctypes.c_void_p * len(xs))(*xs), ctypes.c_void_p)
+    good = ptrs(16, 32)
+    call = lambda k=good, L=2, T=4, D=64: lib.pkv_reshape_and_cache_layers(k, good, good, good, L, 16, T, 2, D, 16, 8,
+                                                                          None)
+    assert call(D=80) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(T=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(T=0) == pkv.PKV_OK and call(L=0) == pkv.PKV_OK
+    assert call(k=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(k=ptrs(16, 40)) == pkv.PKV_ERR_INVALID_ARG              # layer 1's key not 16-byte aligned
+    assert call(k=ptrs(16, 0)) == pkv.PKV_ERR_INVALID_ARG               # layer 1's key null
+
+
 def test_workspace_size(lib):
     # one partition (<= 128 tokens of capacity) needs no workspace
     assert pkv.paged_attention_workspace_size(4, 2, 64, 8, 16) == 0
