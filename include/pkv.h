@@ -444,6 +444,20 @@ int pkv_bm_beam_step(pkv_bm* bm, const int64_t* parents, const int64_t* children
 int pkv_bm_swap(pkv_bm* src, pkv_bm* dst, const int64_t* seq_ids, int n, int64_t* pairs_out,
                 int cap_pairs, int* n_pairs);
 
+/* Observability ([note] 局限与展望, 复杂系统带来新的调度和可观测性问题: a paged
+ * cache should expose block occupancy, tail waste, the distribution of
+ * reference counts, prefix-cache hits and preemptions).
+ * pkv_bm_ref_histogram: hist (host [cap] int64) receives, for r < cap - 1,
+ * the number of physical blocks whose reference count is r (hist[0] = free
+ * blocks); hist[cap - 1] counts every block with a count >= cap - 1.
+ * pkv_bm_counters: out (host [n] int64) receives the first n of, in order,
+ * copy-on-write copies reported, sequences added on a registered prefix,
+ * block references those sequences took from prefixes (prefix hits), groups
+ * swapped away from this manager, blocks swapped away, groups swapped in,
+ * blocks swapped in.  Returns how many were written (at most 7). */
+int pkv_bm_ref_histogram(const pkv_bm* bm, int64_t* hist, int cap);
+int pkv_bm_counters(const pkv_bm* bm, int64_t* out, int n);
+
 /* Reference count of a physical block (negative status on a bad id). */
 int pkv_bm_ref_count(const pkv_bm* bm, int32_t block);
 

@@ -79,6 +79,9 @@ class BlockManager:
         self.seqs: Dict[int, List[LogicalBlock]] = {}
         self.prefixes: Dict[int, List[LogicalBlock]] = {}
         self.cow_copies = 0
+        self.prefix_seqs = 0          # sequences added on a registered prefix
+        self.prefix_blocks = 0        # block references they took from prefixes
+        self.groups_out = self.blocks_out = self.groups_in = self.blocks_in = 0
 
     # -- physical blocks -------------------------------------------------
     def _take(self) -> int:
@@ -177,6 +180,8 @@ class BlockManager:
         for b in src:
             self.ref[b.physical] += 1
         self.seqs[seq_id] = [LogicalBlock(b.physical, b.filled) for b in src]
+        self.prefix_seqs += 1
+        self.prefix_blocks += len(src)
 
     def drop_prefix(self, prefix_id: int) -> None:
         for b in self.prefixes.pop(prefix_id):
@@ -195,6 +200,18 @@ class BlockManager:
 
     def num_free(self) -> int:
         return len(self.free_list)
+
+    def ref_histogram(self, cap: int = 8) -> List[int]:
+        """Blocks per reference count r < cap - 1; the last entry counts every larger count."""
+        hist = [0] * cap
+        for r in self.ref:
+            hist[min(r, cap - 1)] += 1
+        return hist
+
+    def counters(self) -> Dict[str, int]:
+        return {"cow_copies": self.cow_copies, "prefix_seqs": self.prefix_seqs, "prefix_blocks": self.prefix_blocks,
+                "groups_out": self.groups_out, "blocks_out": self.blocks_out, "groups_in": self.groups_in,
+                "blocks_in": self.blocks_in}
 
     def tail_waste_tokens(self) -> int:
         """Sum over sequences of the unfilled slots of their blocks."""
@@ -274,4 +291,9 @@ def swap(src: BlockManager, dst: BlockManager, seq_ids: Sequence[int]) -> List[T
     for b in order:
         src.ref[b] = 0
         src.free_list.append(b)
+    if ids:
+        src.groups_out += 1
+        dst.groups_in += 1
+    src.blocks_out += len(order)
+    dst.blocks_in += len(order)
     return [(b, moved[b]) for b in order]

@@ -81,6 +81,8 @@ _SIGNATURES = {
     "pkv_bm_block_tables": (_I, [_P, _P, _I, _P, _I, _P]),
     "pkv_bm_beam_step": (_I, [_P, _P, _P, _I, _P, _I, _P, _P, _c.POINTER(_I)]),
     "pkv_bm_swap": (_I, [_P, _P, _P, _I, _P, _I, _c.POINTER(_I)]),
+    "pkv_bm_ref_histogram": (_I, [_P, _P, _I]),
+    "pkv_bm_counters": (_I, [_P, _P, _I]),
     "pkv_bm_ref_count": (_I, [_P, _c.c_int32]),
     "pkv_bm_stats": (_I, [_P, _c.POINTER(_I), _c.POINTER(_I64), _c.POINTER(_I64)]),
 }
@@ -566,6 +568,22 @@ class BlockManager:
         _check(self._lib.pkv_bm_swap(self._h, dst._h, _np_ptr(ids), ids.shape[0], _np_ptr(pairs), cap,
                                      ctypes.byref(n)))
         return pairs[:n.value]
+
+    COUNTERS = ("cow_copies", "prefix_seqs", "prefix_blocks", "groups_out", "blocks_out", "groups_in", "blocks_in")
+
+    def ref_histogram(self, cap: int = 8) -> np.ndarray:
+        """[cap] int64: blocks with reference count r (r < cap - 1), the last entry counting the rest."""
+        hist = np.empty(cap, dtype=np.int64)
+        _check(self._lib.pkv_bm_ref_histogram(self._h, _np_ptr(hist), cap))
+        return hist
+
+    def counters(self) -> dict:
+        """Copy-on-write copies, prefix hits (sequences and block references) and swap traffic."""
+        out = np.zeros(len(self.COUNTERS), dtype=np.int64)
+        n = self._lib.pkv_bm_counters(self._h, _np_ptr(out), out.shape[0])
+        if n < 0:
+            _check(n)
+        return {k: int(v) for k, v in zip(self.COUNTERS, out)}
 
     def ref_count(self, block: int) -> int:
         r = self._lib.pkv_bm_ref_count(self._h, block)

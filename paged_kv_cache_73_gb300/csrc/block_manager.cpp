@@ -33,6 +33,10 @@ struct Manager {
   std::unordered_map<int64_t, std::vector<Logical>> seqs;
   std::unordered_map<int64_t, std::vector<Logical>> prefixes;
   int64_t cow_copies = 0;
+  // event counters: sequences added on a registered prefix and the block references they took
+  // from it; groups and blocks that left this manager (swapped away) or arrived (swapped in)
+  int64_t prefix_seqs = 0, prefix_blocks = 0;
+  int64_t groups_out = 0, blocks_out = 0, groups_in = 0, blocks_in = 0;
 
   int32_t take() {
     int32_t b = free_list.front();
@@ -89,6 +93,8 @@ struct Manager {
     return slot;
   }
 };
+
+constexpr int kBmCounters = 7;
 
 Manager* M(pkv_bm* bm) { return reinterpret_cast<Manager*>(bm); }
 const Manager* M(const pkv_bm* bm) { return reinterpret_cast<const Manager*>(bm); }
@@ -244,6 +250,8 @@ int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id) {
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq_with_prefix: sequence %lld exists", (long long)seq_id);
   std::vector<Logical> copy = it->second;
   for (const Logical& lb : copy) m->ref[lb.phys] += 1;
+  m->prefix_seqs += 1;
+  m->prefix_blocks += (int64_t)copy.size();
   m->seqs.emplace(seq_id, std::move(copy));
   return PKV_OK;
 }
@@ -432,8 +440,31 @@ int pkv_bm_swap(pkv_bm* src_bm, pkv_bm* dst_bm, const int64_t* seq_ids, int n, i
     src->ref[b] = 0;
     src->free_list.push_back(b);
   }
+  if (n > 0) {
+    src->groups_out += 1;
+    dst->groups_in += 1;
+  }
+  src->blocks_out += (int64_t)order.size();
+  dst->blocks_in += (int64_t)order.size();
   if (n_pairs) *n_pairs = (int)order.size();
   return PKV_OK;
+}
+
+int pkv_bm_ref_histogram(const pkv_bm* bm, int64_t* hist, int cap) {
+  if (!bm || !hist || cap <= 0) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_ref_histogram: bad arguments");
+  const Manager* m = M(bm);
+  for (int r = 0; r < cap; ++r) hist[r] = 0;
+  for (int32_t c : m->ref) hist[c < cap - 1 ? c : cap - 1] += 1;
+  return PKV_OK;
+}
+
+int pkv_bm_counters(const pkv_bm* bm, int64_t* out, int n) {
+  if (!bm || !out || n < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_counters: bad arguments");
+  const Manager* m = M(bm);
+  const int64_t all[kBmCounters] = {m->cow_copies, m->prefix_seqs, m->prefix_blocks, m->groups_out,
+                                    m->blocks_out, m->groups_in,   m->blocks_in};
+  for (int i = 0; i < n && i < kBmCounters; ++i) out[i] = all[i];
+  return n < kBmCounters ? n : kBmCounters;
 }
 
 int pkv_bm_ref_count(const pkv_bm* bm, int32_t block) {

@@ -66,6 +66,8 @@ def _compare(nat, ora, live, num_blocks):
         assert nat.ref_count(b) == ora.ref_count(b)
     free, waste, copies = nat.stats()
     assert (free, waste, copies) == (ora.num_free(), ora.tail_waste_tokens(), ora.cow_copies)
+    assert nat.ref_histogram(6).tolist() == ora.ref_histogram(6)
+    assert nat.counters() == ora.counters()
 
 
 @pytest.mark.parametrize("B,N,seed", [(4, 64, 0), (16, 300, 1), (8, 40, 2), (1, 50, 3)])

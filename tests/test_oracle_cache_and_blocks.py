@@ -465,3 +465,25 @@ def test_group_swap_out_of_blocks_changes_nothing():
         obm.swap(dev, host, [0])
     assert state == (list(dev.free_list), dev.block_table(0), list(dev.ref))
     assert host.num_free() == 2 and not host.seqs
+
+
+def test_observability_counts():
+    # the reference-count histogram is a partition of the pool, and the counters count events
+    bm = obm.BlockManager(32, 4)
+    host = obm.BlockManager(16, 4)
+    bm.register_prefix(1, 8)                               # 2 blocks held by the prefix
+    for s in range(3):
+        bm.add_seq_with_prefix(s, 1)                       # 3 sequences x 2 prefix blocks
+    bm.add_seq(10, 6)
+    bm.fork(10, 11)
+    bm.append_slot(10)                                     # copies the shared partial block
+    hist = bm.ref_histogram(8)
+    assert sum(hist) == 32 and hist[0] == bm.num_free()
+    assert hist[4] == 2                                    # the prefix blocks: prefix + 3 sequences
+    assert hist[2] == 1 and hist[1] == 2                   # 10/11's full block; 11's partial and 10's copy
+    c = bm.counters()
+    assert (c["prefix_seqs"], c["prefix_blocks"], c["cow_copies"]) == (3, 6, 1)
+    obm.swap(bm, host, [10, 11])
+    assert bm.counters()["groups_out"] == 1 and bm.counters()["blocks_out"] == 3
+    assert host.counters()["groups_in"] == 1 and host.counters()["blocks_in"] == 3
+    assert bm.ref_histogram(3)[2] == 2                     # counts >= 2 fold into the last entry
