@@ -291,6 +291,13 @@ def _grow(bm, seqs, targets):
             have[s] += 1
 
 
+def block_manager_summary(bm) -> dict:
+    """The manager's state after the step's slot assignment: occupancy, sharing and events."""
+    free, waste, _ = bm.stats()
+    return {"free_blocks": free, "tail_waste_tokens": waste, "ref_histogram": bm.ref_histogram(8).tolist(),
+            **bm.counters()}
+
+
 def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 64, capacity_block: int = 16,
                       pool_blocks=None):
     """A decode step's batch built through the host block manager over the recipe's lengths.
@@ -353,7 +360,7 @@ def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 
     else:
         desc = f"{workload}: {recipe.notes}, 40 x 128, block {B}, shuffled blocks"
     return {"w": w, "slots": slots, "pairs": pairs, "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2),
-            "host_us": host_us, "desc": desc, "workload": workload}
+            "host_us": host_us, "desc": desc, "workload": workload, "bm": block_manager_summary(bm)}
 
 
 def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: int = 128, B: int = 16):
@@ -404,7 +411,7 @@ def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: i
     return {"w": w, "slots": np.array(slots, dtype=np.int64),
             "pairs": np.array(pairs, dtype=np.int64).reshape(-1, 2),
             "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2), "host_us": host_us, "desc": desc,
-            "workload": "beam_search"}
+            "workload": "beam_search", "bm": block_manager_summary(bm)}
 
 
 def run_gpu(args, rank, world, dev):
@@ -546,7 +553,7 @@ def run_gpu(args, rank, world, dev):
            "num_seqs": S,
            "launches": K * ((1 if n_pairs else 0) + (0 if fused else 1) + attn_kernels), "part_tokens": part_tokens,
            "host_slot_us": x["host_us"], "clocks": clock_summary, "n_pairs": n_pairs, "copy": copy,
-           "desc": x["desc"], "num_blocks": w.num_blocks}
+           "desc": x["desc"], "num_blocks": w.num_blocks, "bm": x["bm"]}
     if not args.no_e2e:
         res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped, fused))
     return res
@@ -1082,6 +1089,8 @@ def headline_line(args, r, world, cpu, step_ms, e2e_ms, attn_ms, staged_ms, attn
     }
     if r["copy"] is not None:
         line["copy_blocks_setup"] = r["copy"]
+    if r.get("bm") is not None:
+        line["block_manager"] = r["bm"]
     if r["grouped"] is not None:
         line["grouped"] = r["grouped"]
     if "e2e_step_ms" in r:

@@ -33,3 +33,16 @@ def test_prefix_capped_at_the_shortest_members_full_blocks():
     lens = np.array([64, 40], dtype=np.int32)
     starts, prefixes = bench.shared_prefix_groups(tables, lens, B)
     assert starts.tolist() == [0, 2] and prefixes.tolist() == [32]
+
+
+def test_block_manager_summary_of_the_step_batches():
+    # the bench's batches as the block manager built them: parallel sampling with 511-token prompts
+    # makes 3 copies per prompt (96) and keeps each prompt's 31 full blocks shared by its 4 samples;
+    # the shared prefix's 64 blocks are held by the prefix and all 256 requests
+    x = bench.build_step_inputs(1003, "parallel_sampling_cow")["bm"]
+    assert x["cow_copies"] == 96 and x["ref_histogram"][4] == 32 * 31
+    y = bench.build_step_inputs(1004, "shared_prefix")["bm"]
+    assert (y["prefix_seqs"], y["prefix_blocks"]) == (256, 256 * 64) and y["ref_histogram"][7] == 64
+    z = bench.build_step_inputs(1002, "opt13b")["bm"]
+    assert z["cow_copies"] == 0 and sum(z["ref_histogram"][2:]) == 0
+    assert z["ref_histogram"][0] == z["free_blocks"]

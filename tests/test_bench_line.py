@@ -17,7 +17,8 @@ def _run(fused=True, flushed=False):
     return {"attn_bytes": 1_365_910_128, "fused": fused, "grouped": None, "num_seqs": 64, "desc": bench.WORKLOAD,
             "part_tokens": 1024, "n_pairs": 0, "num_blocks": 5235, "l2_flushed": flushed, "host_slot_us": 20.0,
             "launches": 4000, "clocks": {"sm_mhz": 2070.0, "reasons": []}, "copy": None,
-            "e2e_step_ms": 0.2, "h2d": 1_999_616, "d2h": 655_360, "launch": "graph"}
+            "e2e_step_ms": 0.2, "h2d": 1_999_616, "d2h": 655_360, "launch": "graph",
+            "bm": {"free_blocks": 1047, "cow_copies": 0}}
 
 
 def _line(args, r, world=1, cpu=None):
@@ -46,6 +47,7 @@ def test_contract_keys_and_arithmetic(monkeypatch):
     assert e2e["value"] == pytest.approx(1.36e9 / 0.2e-3 / 1e9)
     assert e2e["h2d_bytes_per_step"] == 1_999_616 and e2e["d2h_bytes_per_step"] == 655_360
     assert line["cpu_baseline"] is cpu
+    assert line["block_manager"]["free_blocks"] == 1047
 
 
 def test_whole_job_value_over_ranks(monkeypatch):
