@@ -558,7 +558,7 @@ class BlockManager:
                                           _np_ptr(slots), _np_ptr(pairs), ctypes.byref(nc)))
         return slots[:k], pairs[:nc.value]
 
-    def swap_to(self, dst: "BlockManager", seq_ids: Sequence[int]) -> np.ndarray:
+    def swap(self, dst: "BlockManager", seq_ids: Sequence[int]) -> np.ndarray:
         """Move the group ``seq_ids`` to ``dst`` (pkv_bm_swap).  Returns the [P, 2] int64 block moves
         (this manager's block, dst's block): the block_mapping for swap_blocks."""
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))

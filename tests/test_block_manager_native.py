@@ -311,9 +311,9 @@ def test_random_group_swaps_match_oracle(B, N, M, seed):
                 want = obm.swap(ora_d, ora_h, on_dev[i])
             except MemoryError:
                 with pytest.raises(pkv.PkvOutOfBlocks):
-                    nat_d.swap_to(nat_h, on_dev[i])
+                    nat_d.swap(nat_h, on_dev[i])
                 continue
-            assert nat_d.swap_to(nat_h, on_dev[i]).tolist() == [list(p) for p in want]
+            assert nat_d.swap(nat_h, on_dev[i]).tolist() == [list(p) for p in want]
             on_host.append(on_dev.pop(i))
             swaps += 1
         elif op == 4 and on_host:
@@ -322,9 +322,9 @@ def test_random_group_swaps_match_oracle(B, N, M, seed):
                 want = obm.swap(ora_h, ora_d, on_host[i])
             except MemoryError:
                 with pytest.raises(pkv.PkvOutOfBlocks):
-                    nat_h.swap_to(nat_d, on_host[i])
+                    nat_h.swap(nat_d, on_host[i])
                 continue
-            assert nat_h.swap_to(nat_d, on_host[i]).tolist() == [list(p) for p in want]
+            assert nat_h.swap(nat_d, on_host[i]).tolist() == [list(p) for p in want]
             on_dev.append(on_host.pop(i))
             swaps += 1
         elif op == 5 and len(on_dev) > 1:
@@ -346,15 +346,15 @@ def test_group_swap_errors_leave_state_unchanged():
     dev.add_seq(2, 9)
     state = ([dev.block_table(s) for s in (0, 1, 2)], dev.stats(), host.stats())
     with pytest.raises(pkv.PkvError):
-        dev.swap_to(host, [0])                             # its sibling holds the same blocks
+        dev.swap(host, [0])                             # its sibling holds the same blocks
     with pytest.raises(pkv.PkvOutOfBlocks):
-        dev.swap_to(host, [2])                             # 3 blocks, the host has 2
+        dev.swap(host, [2])                             # 3 blocks, the host has 2
     with pytest.raises(pkv.PkvError):
-        dev.swap_to(host, [0, 1, 0])
+        dev.swap(host, [0, 1, 0])
     with pytest.raises(pkv.PkvError):
-        dev.swap_to(dev, [2])
+        dev.swap(dev, [2])
     other = pkv.BlockManager(16, 8)
     with pytest.raises(pkv.PkvError):
-        dev.swap_to(other, [2])                            # block sizes differ
+        dev.swap(other, [2])                            # block sizes differ
     assert state == ([dev.block_table(s) for s in (0, 1, 2)], dev.stats(), host.stats())
-    assert dev.swap_to(host, [0, 1]).shape == (2, 2)       # the whole group fits
+    assert dev.swap(host, [0, 1]).shape == (2, 2)       # the whole group fits

@@ -116,13 +116,13 @@ def test_preempted_group_round_trip_keeps_attention(cuda_device):
                                           torch.from_numpy(lens).to(cuda_device), D ** -0.5, B)
 
     before = attend()
-    out_pairs = dev_bm.swap_to(host_bm, group)
+    out_pairs = dev_bm.swap(host_bm, group)
     pkv.swap_blocks([k], [v], [hk], [hv], torch.from_numpy(out_pairs).to(cuda_device))
     freed = torch.from_numpy(out_pairs[:, 0]).to(cuda_device)
     k[freed] = float("nan")                                 # reused by someone else meanwhile
     v[freed] = float("nan")
     dev_bm.add_seq(20, B * 3)
-    in_pairs = host_bm.swap_to(dev_bm, group)
+    in_pairs = host_bm.swap(dev_bm, group)
     pkv.swap_blocks([hk], [hv], [k], [v], torch.from_numpy(in_pairs).to(cuda_device))
     after = attend()
     torch.cuda.synchronize()
