@@ -2,33 +2,44 @@
 
 One step = one decode step of the OPT-13B-shaped single-layer batch (64
 sequences, 40 heads x 128, block size 16, context lengths ~ U[128, 2048],
-physical blocks shuffled): copy_blocks of the step's copy-on-write pairs,
-reshape_and_cache of the 64 new tokens, paged decode attention (partition
-kernel + merge kernel).  Slot assignment (the host block manager) runs once
-at set-up; its host time is reported separately.
+physical blocks shuffled): copy_blocks of the step's copy-on-write pairs (none
+in this batch), then the 64 new tokens' K/V write and paged decode attention in
+one launch (pkv_paged_attention_decode_append; --unfused: reshape_and_cache,
+then pkv_paged_attention_decode).  The tables and slots come from the host
+block manager.
 
-Prints ONE JSON line (rank 0).  `value` is effective KV GB/s: the K/V bytes
-attention reads per step (logical, a shared block counted per reader) over
-the device-timed step.  `e2e` is the same metric through the same C-ABI
-calls with every step's inputs in page-locked host memory, read by the kernels
-across NVLink-C2C, and the output written back there (`staged_value`: the
-same step with one host->device and one device->host copy).  `roofline` is
-the paged attention call alone against the measured HBM copy bandwidth.
+Prints ONE JSON line (rank 0):
+* value: effective KV GB/s, the K/V bytes attention reads per step (logical, a
+  shared block counted per reader) over the device time of exactly K steps
+  (CUDA events before and after them, nothing in between);
+* roofline: the attention call alone, max(200, K) launches back to back after
+  the timed region, against the measured HBM copy bandwidth; its median comes
+  from a separate loop with events around every launch;
+* sustained: at least one second of back-to-back steps, with its own clock
+  samples; `clocks` spans the timed region and this segment;
+* e2e: a real decode loop through the C ABI from the host.  Every step the
+  host block manager assigns the new tokens' slots and builds the tables
+  (pkv_bm_append_slots, pkv_bm_block_tables) into page-locked host memory, the
+  kernels read them (and q and the new K/V rows) across NVLink-C2C and write
+  the output there, and the host waits for it; the contexts grow by one token
+  a step.  `graph_replay` is the same step's fixed inputs replayed as a CUDA
+  graph;
+* configs: the tiny batch, parallel sampling with copy-on-write, the shared
+  prefix and the capacity sweep at 1 and 64 sequences: GB/s, the fraction of
+  the measured peak and the max abs error of sampled sequences against the
+  oracle (whose outputs the CPU-baseline leg computes);
+* cpu_baseline: the oracle (numpy fp64) on the whole batch, one host core, and
+  one single-threaded process per core.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                  [--workload opt13b|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity|beam_search
-                              |swap|layers40|prefill]
-                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F] [--grouped]
+                  [--workload opt13b|tiny|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity
+                              |beam_search|swap|layers40|prefill]
+                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F] [--grouped] [--unfused]
 
 `--workload swap`, `--workload layers40` and `--workload prefill` print their
 own lines (swap_blocks between HBM and page-locked host memory; 40-layer
 copy_blocks and reshape_and_cache in one launch; prefill attention over a
 cached prefix on the tensor cores) with their own metric names.
-
-The default workload is the headline one above.  The others build their batch
-through the same block manager (prompt forks with copy-on-write, a shared
-prefix, full 2048-token contexts); their copy-on-write copies are timed as
-one copy_blocks call (`copy_blocks_setup`).
 
 --grouped makes the attention call pkv_paged_attention_decode_shared_prefix:
 consecutive sequences whose leading blocks are the same physical blocks form a
@@ -36,8 +47,9 @@ group whose shared prefix is read once (groups under 8 members still read it
 per sequence); the metric is unchanged and `roofline` then counts distinct K/V
 slots.
 
---impl reference times the CPU oracle on the host cores instead (a bounded
-sample of the same workload per step) and prints the same metric.
+--impl reference times the CPU oracle on the host cores instead: each step the
+new-token writes and fp64 attention over the whole batch, whose tables and
+slots the oracle's own block manager builds (libpkv.so is not loaded).
 """
 from __future__ import annotations
 
@@ -68,31 +80,45 @@ METRIC = "paged decode attention effective KV GB/s (% of HBM peak) and decode to
 UNIT = "GB/s"
 WORKLOAD = ("opt13b_decode_step: 64 seqs, 40 heads x 128, block 16, ctx ~ U[128,2048], shuffled blocks, "
             "+ the K/V write of 64 new tokens (in the attention launch; --unfused: reshape_and_cache first)")
-SEED = 1002
+# seed of each workload's length draws and physical-block permutation: 1000 + its index
+WORKLOAD_SEEDS = {"tiny": 1001, "opt13b": 1002, "parallel_sampling": 1003, "parallel_sampling_cow": 1003,
+                  "shared_prefix": 1004, "capacity": 1005, "beam_search": 1006}
+SEED = WORKLOAD_SEEDS["opt13b"]
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0                                # GB300 HBM3e, nominal
-EVENT_EVERY = 16
+# a step whose distinct K/V is under twice this is preceded by a write of twice the device's L2
+L2_NOMINAL_BYTES = 129 * 10 ** 6
+ROOFLINE_LAUNCHES = 200                                 # attention calls timed for the roofline, at least
+SUSTAINED_S = 1.0                                       # seconds of back-to-back steps, at least
+CONFIG_STEPS = 50                                       # timed steps of each entry of `configs`
+REF_MAX_KV_BYTES = 2.5e9                                # the oracle arm samples batches larger than this
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call (partition + merge
-# kernels) from an ncu capture, keyed by (workload, sha256 of the attention source it was taken
-# on); a changed kernel reports null until it is captured again.
+# dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call from an ncu capture,
+# keyed by (workload, sha256 of the attention source it was taken on); a changed kernel reports
+# null until it is captured again.
 NCU_TRAFFIC = {
     # the headline step's fused call: partition kernel 1,373,092,500 B read + 4,835,200 B written
     # (the appended rows included), merge kernel 1,280,000 B read (means of two launches each;
-    # profiles/paged_attention_opt13b_decode.md; captured on source 671088f0..., which differs from
-    # this key's source in the file's header comment only)
+    # captured on source 671088f0..., which differs from this key's source in the file's header
+    # comment only)
     ("opt13b+append", "5db4ea62901c2074d5db6247fb9ca0f86ae177cb2d1f094b6e25a2b6456c7857"): 1_379_208_000,
 }
 
+WORKLOADS = ("opt13b", "tiny", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity",
+             "beam_search")
+AUX_WORKLOADS = ("swap", "layers40", "prefill")
 
-def parse():
+
+def parse(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
-    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loops (profiling runs)")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' entries (profiling runs)")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the roofline and sustained loops (profiling runs)")
     ap.add_argument("--unfused", action="store_true",
                     help="write the new tokens with a separate reshape_and_cache call before attention "
                          "(default: pkv_paged_attention_decode_append, one launch)")
@@ -105,7 +131,7 @@ def parse():
     ap.add_argument("--capacity-block", type=int, default=16, help="capacity workload: block size")
     ap.add_argument("--pool-frac", type=float, default=0.0,
                     help="capacity workload: size the pool to this fraction of free HBM (0 = just enough)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def attention_source_sha() -> str:
@@ -122,6 +148,16 @@ def measured_hbm_peak():
         return v, "measured (MEASURED_PEAKS.json hbm_gbs: torch copy, read+write bytes)"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured bf16 dense burst (MEASURED_PEAKS.json bf16_tflops; fp16 has the same nominal rate), of measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 burst"
 
 
 class ClockSampler:
@@ -243,7 +279,8 @@ class ClockSampler:
 
 # ---- workloads -------------------------------------------------------------------------------------
 
-WORKLOADS = ("opt13b", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity", "beam_search")
+def workload_seed(workload: str) -> int:
+    return WORKLOAD_SEEDS.get(workload, SEED)
 
 
 def attention_algorithmic_bytes(w) -> int:
@@ -277,45 +314,113 @@ def shared_prefix_groups(tables, lens, B):
     return np.array(starts, dtype=np.int32), np.array(prefixes, dtype=np.int32)
 
 
-def _grow(bm, seqs, targets):
-    """Append tokens to `seqs` until each holds targets[i] - 1 tokens; returns the copies made."""
-    copies = []
-    have = {s: bm.block_table(s)[1] for s in seqs}
-    while True:
-        live = [s for s, t in zip(seqs, targets) if have[s] < t - 1]
-        if not live:
-            return copies
-        _, pairs = bm.append_slots(live)
-        copies += [tuple(int(x) for x in p) for p in pairs]
-        for s in live:
-            have[s] += 1
+class OracleManager:
+    """The oracle's block manager behind the methods of the binding's BlockManager that the bench
+    calls, with the same arguments and return shapes.  The reference arm and the CPU-baseline leg
+    build their batches with it, so neither loads libpkv.so; a CPU test checks that both managers
+    give the bench's batches identical tables, slots and copies."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order):
+        from oracle import block_manager as obm
+        self.m = obm.BlockManager(num_blocks, block_size, [int(b) for b in free_order])
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    @staticmethod
+    def _pairs(copies):
+        return np.array(copies, dtype=np.int64).reshape(-1, 2)
+
+    def add_seq(self, seq_id, prompt_len):
+        return np.array(self.m.add_seq(int(seq_id), int(prompt_len)), dtype=np.int64)
+
+    def fork(self, parent, child):
+        self.m.fork(int(parent), int(child))
+
+    def register_prefix(self, prefix_id, length):
+        return np.array(self.m.register_prefix(int(prefix_id), int(length)), dtype=np.int64)
+
+    def add_seq_with_prefix(self, seq_id, prefix_id, suffix_len=0):
+        slots, copies = self.m.add_seq_with_prefix(int(seq_id), int(prefix_id), int(suffix_len))
+        return np.array(slots, dtype=np.int64), self._pairs(copies)
+
+    def extend(self, seq_id, n):
+        slots, copies = self.m.extend(int(seq_id), int(n))
+        return np.array(slots, dtype=np.int64), self._pairs(copies)
+
+    def append_slots(self, seq_ids):
+        slots, copies = [], []
+        for s in seq_ids:
+            slot, src, dst = self.m.append_slot(int(s))
+            slots.append(slot)
+            if src >= 0:
+                copies.append((src, dst))
+        return np.array(slots, dtype=np.int64), self._pairs(copies)
+
+    def block_table(self, seq_id):
+        return self.m.block_table(int(seq_id))
+
+    def block_tables(self, seq_ids, max_blocks):
+        tables = np.full((len(seq_ids), max_blocks), -1, dtype=np.int32)
+        lens = np.zeros(len(seq_ids), dtype=np.int32)
+        for i, s in enumerate(seq_ids):
+            ids, ctx = self.m.block_table(int(s))
+            if len(ids) > max_blocks:
+                raise ValueError(f"sequence {s} has {len(ids)} blocks > {max_blocks}")
+            tables[i, :len(ids)] = ids
+            lens[i] = ctx
+        return tables, lens
+
+    def beam_step(self, parents, children, retire):
+        res = self.m.beam_step([int(p) for p in parents], [int(c) for c in children], [int(r) for r in retire])
+        return (np.array([r[0] for r in res], dtype=np.int64),
+                self._pairs([(r[1], r[2]) for r in res if r[1] >= 0]))
+
+    def stats(self):
+        return self.m.num_free(), self.m.tail_waste_tokens(), self.m.cow_copies
+
+    def ref_histogram(self, cap=8):
+        return np.array(self.m.ref_histogram(cap), dtype=np.int64)
+
+    def counters(self):
+        return self.m.counters()
+
+
+def make_manager(kind: str, num_blocks: int, block_size: int, free_order):
+    """The C++ block manager (the product) or, for the oracle's legs, the oracle's."""
+    if kind == "oracle":
+        return OracleManager(num_blocks, block_size, free_order)
+    from paged_kv_cache_73_gb300 import binding as pkv
+    return pkv.BlockManager(num_blocks, block_size, free_order)
 
 
 def block_manager_summary(bm) -> dict:
     """The manager's state after the step's slot assignment: occupancy, sharing and events."""
     free, waste, _ = bm.stats()
-    return {"free_blocks": free, "tail_waste_tokens": waste, "ref_histogram": bm.ref_histogram(8).tolist(),
-            **bm.counters()}
+    return {"free_blocks": int(free), "tail_waste_tokens": int(waste),
+            "ref_histogram": [int(x) for x in bm.ref_histogram(8)], **bm.counters()}
 
 
 def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 64, capacity_block: int = 16,
-                      pool_blocks=None):
-    """A decode step's batch built through the host block manager over the recipe's lengths.
+                      pool_blocks=None, manager: str = "native"):
+    """A decode step's batch built through a host block manager over the recipe's lengths.
 
-    Every sequence is grown to ctx - 1 tokens (prefill, forks, copy-on-write and
-    earlier decode tokens as the workload prescribes), then one append per
-    sequence gives this step's new-token slots and copy pairs.
-    Returns a dict: w (DecodeWorkload over the manager's tables), slots, pairs
-    (this step's copies), setup_pairs (copies made while growing), host_us,
-    desc.
+    Every sequence is grown to ctx - 1 tokens (a prompt, forked samples whose own tokens are
+    placed in one call each, or requests on a registered prefix whose own tokens are placed in the
+    same call; copy-on-write where a shared partly filled block is written), then one append per
+    sequence gives this step's new-token slots and copy pairs.  `manager` is "native" (the C++
+    manager of libpkv.so) or "oracle" (oracle/block_manager.py).
+    Returns a dict: w (DecodeWorkload over the manager's tables), slots, pairs (this step's
+    copies), setup_pairs (copies made while growing), host_us, desc, manager (the live manager,
+    for further steps), seqs, bm (a summary).
     """
-    from paged_kv_cache_73_gb300 import binding as pkv
     from paged_kv_cache_73_gb300 import workloads as wl
 
     if workload == "beam_search":
-        return build_beam_step(seed)
+        return build_beam_step(seed, manager=manager)
     if workload == "opt13b":
         recipe = wl.opt13b(seed=seed)
+    elif workload == "tiny":
+        recipe = wl.tiny(seed=seed)
     elif workload in ("parallel_sampling", "parallel_sampling_cow"):
         recipe = wl.parallel_sampling(seed=seed, prompt_len=512 if workload == "parallel_sampling" else 511)
     elif workload == "shared_prefix":
@@ -328,7 +433,7 @@ def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 
     lens = recipe.context_lens
     S = len(lens)
     N = recipe.num_blocks
-    bm = pkv.BlockManager(N, B, wl.free_list_order(N, seed))
+    bm = make_manager(manager, N, B, wl.free_list_order(N, seed))
     seqs = list(range(S))
     setup = []
     if workload.startswith("parallel_sampling"):
@@ -337,12 +442,15 @@ def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 
             bm.add_seq(base, prompt)
             for i in range(1, n):
                 bm.fork(base, base + i)
-        setup = _grow(bm, seqs, lens)
+        for s in seqs:                                   # each sample's own tokens, in one call
+            _, pr = bm.extend(s, int(lens[s]) - 1 - prompt)
+            setup += pr.tolist()
     elif workload == "shared_prefix":
-        bm.register_prefix(0, 1024)
-        for s in seqs:
-            bm.add_seq_with_prefix(s, 0)
-        setup = _grow(bm, seqs, lens)
+        prefix = 1024
+        bm.register_prefix(0, prefix)
+        for s in seqs:                                   # the request and its own tokens, in one call
+            _, pr = bm.add_seq_with_prefix(s, 0, int(lens[s]) - 1 - prefix)
+            setup += pr.tolist()
     else:
         for s in seqs:
             bm.add_seq(s, int(lens[s]) - 1)
@@ -357,25 +465,28 @@ def build_step_inputs(seed: int, workload: str = "opt13b", capacity_seqs: int = 
         desc = f"capacity: {S} seqs x ctx 2048, 40 x 128, block {B}, {N} pool blocks, shuffled"
     elif workload == "opt13b":
         desc = WORKLOAD
+    elif workload == "tiny":
+        desc = f"tiny: 3 seqs, ctx 7/5/12, 2 heads x 64, block 4, {N} pool blocks, shuffled"
     else:
         desc = f"{workload}: {recipe.notes}, 40 x 128, block {B}, shuffled blocks"
     return {"w": w, "slots": slots, "pairs": pairs, "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2),
-            "host_us": host_us, "desc": desc, "workload": workload, "bm": block_manager_summary(bm)}
+            "host_us": host_us, "desc": desc, "workload": workload, "manager": bm, "seqs": seqs,
+            "bm": block_manager_summary(bm)}
 
 
-def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: int = 128, B: int = 16):
+def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: int = 128, B: int = 16,
+                    manager: str = "native"):
     """Beam search through the block manager: each request keeps `width` candidates; every step
     each new candidate picks a parent among the current ones (seeded), the old beam is retired and
     shared partly filled blocks are copied once per extra sibling.  The measured step is one more
     beam step: its copies, its new tokens' writes and attention over all candidates."""
-    from paged_kv_cache_73_gb300 import binding as pkv
     from paged_kv_cache_73_gb300 import workloads as wl
 
     H, D = 40, 128
     rng = np.random.default_rng(seed)
     prompts = rng.integers(256, 1025, size=requests)
     N = int(2 * (sum(-(-int(p) // B) for p in prompts) + requests * width * (beam_steps // B + 3)))
-    bm = pkv.BlockManager(N, B, wl.free_list_order(N, seed))
+    bm = make_manager(manager, N, B, wl.free_list_order(N, seed))
     beams, nid = [], 0
     for r in range(requests):
         bm.add_seq(nid, int(prompts[r]))
@@ -411,156 +522,500 @@ def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: i
     return {"w": w, "slots": np.array(slots, dtype=np.int64),
             "pairs": np.array(pairs, dtype=np.int64).reshape(-1, 2),
             "setup_pairs": np.array(setup, dtype=np.int64).reshape(-1, 2), "host_us": host_us, "desc": desc,
-            "workload": "beam_search", "bm": block_manager_summary(bm)}
+            "workload": "beam_search", "manager": bm, "seqs": seqs, "bm": block_manager_summary(bm)}
 
 
-def run_gpu(args, rank, world, dev):
+def needs_flush(w) -> bool:
+    """A step whose distinct K/V would stay in L2 between steps is preceded by an L2 flush."""
+    return w.physical_kv_bytes() < 2 * L2_NOMINAL_BYTES
+
+
+# ---- the GPU arm -----------------------------------------------------------------------------------
+
+class Step:
+    """One decode step of a batch on the device: pools, inputs and the calls, through the binding."""
+
+    def __init__(self, x, dev, fused=True, grouped=False):
+        import torch
+        from paged_kv_cache_73_gb300 import binding as pkv
+        from paged_kv_cache_73_gb300 import workloads as wl
+        self.pkv = pkv
+        self.x = x
+        w = self.w = x["w"]
+        S, H, D, B, MB = w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq
+        self.k, self.v = w.pools(dev)
+        self.q = w.q(dev)
+        self.key, self.value = wl.new_tokens(S, H, D, w.seed, dev)
+        self.tables = torch.from_numpy(w.block_tables).to(dev)
+        self.lens = torch.from_numpy(w.context_lens).to(dev)
+        self.slots = torch.from_numpy(np.ascontiguousarray(x["slots"])).to(dev)
+        self.pairs = torch.from_numpy(np.ascontiguousarray(x["pairs"])).to(dev)
+        self.n_pairs = int(x["pairs"].shape[0])
+        self.out = torch.empty_like(self.q)
+        self.ws = pkv.workspace_for(S, H, D, MB, B, dev)
+        self.part_tokens, self.attn_kernels = pkv.paged_attention_plan(S, H, D, MB, B)
+        self.stream = torch.cuda.current_stream()
+        self.grouped = None
+        if grouped:
+            gs_h, pl_h = shared_prefix_groups(w.block_tables, w.context_lens, B)
+            n_ws = pkv.paged_attention_shared_prefix_workspace_size(S, H, D, MB, B)
+            self.grouped = {"gs": torch.from_numpy(gs_h).to(dev), "pl": torch.from_numpy(pl_h).to(dev),
+                            "max_group": int(np.max(np.diff(gs_h))), "groups": int(len(pl_h)),
+                            "prefix_tokens": int(pl_h.sum()), "gs_h": gs_h, "pl_h": pl_h}
+            self.ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device=dev)
+            self.attn_kernels = 3                        # prefix partials, partitions, merge
+        self.fused = fused and not grouped
+        self.kernels_per_step = (1 if self.n_pairs else 0) + (0 if self.fused else 1) + self.attn_kernels
+
+    def attention(self):
+        """The step's attention call (with the new rows' write when fused)."""
+        pkv, w, st = self.pkv, self.w, self.stream
+        if self.fused:
+            pkv.paged_attention_decode_append(self.q, self.key, self.value, self.slots, self.k, self.v, self.tables,
+                                              self.lens, w.scale, w.block_size, out=self.out, workspace=self.ws,
+                                              stream=st)
+        elif self.grouped is None:
+            pkv.paged_attention_decode(self.q, self.k, self.v, self.tables, self.lens, w.scale, w.block_size,
+                                       out=self.out, workspace=self.ws, stream=st)
+        else:
+            g = self.grouped
+            pkv.paged_attention_decode_shared_prefix(self.q, self.k, self.v, self.tables, self.lens, g["gs"], g["pl"],
+                                                     w.scale, w.block_size, g["max_group"], out=self.out,
+                                                     workspace=self.ws, stream=st)
+
+    def __call__(self):
+        pkv, st = self.pkv, self.stream
+        if self.n_pairs:
+            pkv.copy_blocks([self.k], [self.v], self.pairs, stream=st)
+        if not self.fused:
+            pkv.reshape_and_cache(self.key, self.value, self.k, self.v, self.slots, stream=st)
+        self.attention()
+
+    def attention_bytes(self) -> int:
+        """Algorithmic bytes of the attention call: K/V rows, q, out, tables and lengths; plus the
+        new rows read and written when fused; the distinct K/V slots when grouped."""
+        w = self.w
+        if self.grouped is not None:
+            return w.physical_kv_bytes() + w.num_seqs * w.num_heads * w.head_dim * 2 * 2
+        extra = 4 * w.num_seqs * w.num_heads * w.head_dim * 2 if self.fused else 0
+        return attention_algorithmic_bytes(w) + extra
+
+
+def _events(n):
     import torch
-    from paged_kv_cache_73_gb300 import binding as pkv
-    from paged_kv_cache_73_gb300 import workloads as wl
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
-    seed = SEED + 7919 * rank                           # weak scaling: each rank its own batch
+
+def time_steps(fn, n, stream, flush_buf=None):
+    """Device time (ms) of n calls of fn: with flush_buf, each call follows a write of the buffer
+    and has its own events (returns the per-call times); else one event pair around all n (returns
+    [mean])."""
+    import torch
+    if flush_buf is None:
+        a, b = _events(2)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) / n]
+    evs = [_events(2) for _ in range(n)]
+    for i in range(n):
+        flush_buf.fill_(i & 255)
+        evs[i][0].record(stream)
+        fn()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def time_each(fn, n, stream, flush_buf=None):
+    """Per-call device times (ms) of n calls, each between its own events (and after a flush)."""
+    import torch
+    evs = [_events(2) for _ in range(n)]
+    for i in range(n):
+        if flush_buf is not None:
+            flush_buf.fill_(i & 255)
+        evs[i][0].record(stream)
+        fn()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_gpu(args, rank, world, dev, cpu_refs=None):
+    import torch
+
+    seed = workload_seed(args.workload) + 7919 * rank  # weak scaling: each rank its own batch
     x = build_step_inputs(seed, args.workload, args.capacity_seqs, args.capacity_block,
                           pool_blocks_for(args, dev))
-    w, slots, pairs = x["w"], x["slots"], x["pairs"]
-    S, H, D, B, MB = w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq
-    k, v = w.pools(dev)
-    q = w.q(dev)
-    key, value = wl.new_tokens(S, H, D, seed, dev)
-    tables = torch.from_numpy(w.block_tables).to(dev)
-    lens = torch.from_numpy(w.context_lens).to(dev)
-    slots_d = torch.from_numpy(slots).to(dev)
-    pairs_d = torch.from_numpy(np.ascontiguousarray(pairs)).to(dev)
-    out = torch.empty_like(q)
-    ws = pkv.workspace_for(S, H, D, MB, B, dev)
-    part_tokens, attn_kernels = pkv.paged_attention_plan(S, H, D, MB, B)
-    stream = torch.cuda.current_stream()
-    n_pairs = int(pairs.shape[0])
-    grouped = None
-    if args.grouped:
-        gs_h, pl_h = shared_prefix_groups(w.block_tables, w.context_lens, B)
-        n_ws = pkv.paged_attention_shared_prefix_workspace_size(S, H, D, MB, B)
-        grouped = {"gs": torch.from_numpy(gs_h).to(dev), "pl": torch.from_numpy(pl_h).to(dev),
-                   "max_group": int(np.max(np.diff(gs_h))), "groups": int(len(pl_h)),
-                   "prefix_tokens": int(pl_h.sum()), "gs_h": gs_h, "pl_h": pl_h}
-        ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device=dev)
-        attn_kernels = 3                                 # prefix partials, partitions, merge
-
-    def attention(qq, tt, ll, st):
-        if grouped is None:
-            pkv.paged_attention_decode(qq, k, v, tt, ll, w.scale, B, out=out, workspace=ws, stream=st)
-        else:
-            pkv.paged_attention_decode_shared_prefix(qq, k, v, tt, ll, grouped["gs"], grouped["pl"], w.scale, B,
-                                                     grouped["max_group"], out=out, workspace=ws, stream=st)
+    st = Step(x, dev, fused=not args.unfused, grouped=args.grouped)
+    pkv, w, stream = st.pkv, st.w, st.stream
+    H, D, B = w.num_heads, w.head_dim, w.block_size
 
     copy = None
     if len(x["setup_pairs"]):
         # the copy-on-write copies made while the batch grew, as one copy_blocks call
         sp = torch.from_numpy(np.ascontiguousarray(x["setup_pairs"])).to(dev)
+        fn = lambda: pkv.copy_blocks([st.k], [st.v], sp, stream=stream)       # noqa: E731
         for _ in range(5):
-            pkv.copy_blocks([k], [v], sp, stream=stream)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(20):
-            pkv.copy_blocks([k], [v], sp, stream=stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / 20
+            fn()
+        ms = time_steps(fn, 20, stream)[0]
         moved = 2 * 2 * len(sp) * H * B * D * 2           # K and V, read and written
         copy = {"pairs": int(len(sp)), "ms": ms, "GB/s": moved / (ms * 1e-3) / 1e9}
-
-    fused = grouped is None and not args.unfused
-
-    def step(ev0=None, ev1=None):
-        if n_pairs:
-            pkv.copy_blocks([k], [v], pairs_d, stream=stream)
-        if fused:
-            # the new tokens' K/V write and the attention in one launch
-            if ev0 is not None:
-                ev0.record(stream)
-            pkv.paged_attention_decode_append(q, key, value, slots_d, k, v, tables, lens, w.scale, B, out=out,
-                                              workspace=ws, stream=stream)
-        else:
-            pkv.reshape_and_cache(key, value, k, v, slots_d, stream=stream)
-            if ev0 is not None:
-                ev0.record(stream)
-            attention(q, tables, lens, stream)
-        if ev1 is not None:
-            ev1.record(stream)
 
     # clocks sampled from before the warm-up on; stopped at exit as well, should the run raise
     clocks = ClockSampler(physical_gpu_index(torch.cuda.current_device())).start()
     atexit.register(clocks.stop)
     for _ in range(max(args.warmup, 3)):
-        step()
+        st()
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 
     K = args.steps
-    l2_bytes = l2_cache_bytes(dev)
-    flush = w.physical_kv_bytes() < 2 * l2_bytes
+    flush = needs_flush(w)
+    scratch = torch.empty(2 * l2_cache_bytes(dev), dtype=torch.uint8, device=dev) if flush else None
     barrier(world)
     torch.cuda.synchronize()
-    if flush:
-        # a step whose K/V would stay in L2: a write of twice the L2 size before every step, outside
-        # the timed region, and each step timed by its own events (start, attention, end)
-        scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
-        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
-        t0 = time.time()
-        for i in range(K):
-            scratch.fill_(i & 255)
-            e0, e1, e2 = evs[i]
-            e0.record(stream)
-            step(e1, e2)
-        torch.cuda.synchronize()
-        t1 = time.time()
-        barrier(world)
-        step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in evs) / K
-        attn_ms = [e1.elapsed_time(e2) for _, e1, e2 in evs]
-    else:
-        # events around the attention call on every EVENT_EVERY-th step only: an event between two
-        # kernels stops the next launch from overlapping the previous kernel's tail (PDL)
-        n_ev = (K + EVENT_EVERY - 1) // EVENT_EVERY
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
-        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.time()
-        start.record(stream)
-        for i in range(K):
-            if i % EVENT_EVERY == 0:
-                step(*ev[i // EVENT_EVERY])
-            else:
-                step()
-        stop.record(stream)
-        torch.cuda.synchronize()
-        t1 = time.time()
-        barrier(world)
-        step_ms = start.elapsed_time(stop) / K
-        attn_ms = [a.elapsed_time(b) for a, b in ev]
-    clock_summary = clocks.summary(t0, t1)
-    clocks.stop()
+    # the timed region: exactly K steps, nothing between them (or, for a batch L2 would hold, each
+    # step after a write of twice the L2 size and between its own events)
+    t0 = time.time()
+    times = time_steps(st, K, stream, scratch)
+    t1 = time.time()
+    barrier(world)
+    step_ms = sum(times) / len(times)
+    region = (t0, t1)
     code = pkv.device_error()
     assert code == 0, f"device check {code}"
 
-    res = {"step_ms": step_ms, "attn_ms": sum(attn_ms) / len(attn_ms), "attn_ms_median": statistics.median(attn_ms),
-           "l2_flushed": flush,
-           "kv_bytes": w.logical_kv_bytes(), "phys_bytes": w.physical_kv_bytes(),
-           # grouped: each shared prefix is read once, so the call's bytes are the distinct slots;
-           # fused: the call also reads the new K/V rows and writes them into the pools
-           "attn_bytes": (attention_algorithmic_bytes(w) + (4 * S * H * D * 2 if fused else 0)) if grouped is None
-           else w.physical_kv_bytes() + S * H * D * 2 * 2,
-           "fused": fused,
-           "grouped": None if grouped is None else {k_: grouped[k_] for k_ in ("groups", "max_group", "prefix_tokens")},
-           "num_seqs": S,
-           "launches": K * ((1 if n_pairs else 0) + (0 if fused else 1) + attn_kernels), "part_tokens": part_tokens,
-           "host_slot_us": x["host_us"], "clocks": clock_summary, "n_pairs": n_pairs, "copy": copy,
+    res = {"step_ms": step_ms, "l2_flushed": flush, "kv_bytes": w.logical_kv_bytes(),
+           "phys_bytes": w.physical_kv_bytes(), "attn_bytes": st.attention_bytes(), "fused": st.fused,
+           "grouped": None if st.grouped is None
+           else {k_: st.grouped[k_] for k_ in ("groups", "max_group", "prefix_tokens")},
+           "num_seqs": w.num_seqs, "launches": K * st.kernels_per_step, "kernels_per_step": st.kernels_per_step,
+           "part_tokens": st.part_tokens, "host_slot_us": x["host_us"], "n_pairs": st.n_pairs, "copy": copy,
            "desc": x["desc"], "num_blocks": w.num_blocks, "bm": x["bm"]}
+
+    if not args.no_sustained:
+        # roofline: the attention call alone, at least ROOFLINE_LAUNCHES launches back to back (each
+        # after a flush and between its own events for a batch L2 would hold); the median of a
+        # separate loop with events around every launch (an event between two launches stops the
+        # next one from overlapping the previous one's tail, so these run a little longer)
+        n_launch = max(ROOFLINE_LAUNCHES, K)
+        lt = time_steps(st.attention, n_launch, stream, scratch)
+        iso = time_each(st.attention, n_launch, stream, scratch)
+        res.update(attn_ms=sum(lt) / len(lt), attn_ms_median=statistics.median(iso), timed_launches=n_launch,
+                   attn_loop="back to back, one event pair around all launches" if scratch is None
+                   else "each launch after an L2 flush, between its own events")
+        # sustained: at least SUSTAINED_S seconds of back-to-back steps, with their own clock samples
+        n_sus = max(K, int(math.ceil(SUSTAINED_S * 1e3 / max(step_ms, 1e-3))))
+        ts0 = time.time()
+        sus = time_steps(st, n_sus, stream, scratch)
+        ts1 = time.time()
+        sus_ms = sum(sus) / len(sus)
+        sus_clocks = clocks.summary(ts0, ts1)
+        res["sustained"] = {"steps": n_sus, "seconds": ts1 - ts0, "ms_per_step": sus_ms,
+                            "kv_bytes": w.logical_kv_bytes() * n_sus, "device_s": sus_ms * n_sus * 1e-3,
+                            "clocks": sus_clocks}
+        res["clocks"] = clocks.summary(t0, ts1)
+        if res["clocks"] is not None:
+            res["clocks"]["window"] = ("from the start of the timed region to the end of the sustained segment "
+                                       "(the roofline loops and the sustained steps follow the timed steps)")
+    else:
+        iso = time_each(st.attention, max(3, min(K, 20)), stream, scratch)
+        res.update(attn_ms=sum(iso) / len(iso), attn_ms_median=statistics.median(iso), timed_launches=len(iso),
+                   attn_loop="events around every launch", clocks=None)
+    res["clocks_timed_region"] = clocks.summary(*region)
+    if res["clocks"] is None:
+        res["clocks"] = res["clocks_timed_region"]
+    clocks.stop()
+    assert pkv.device_error() == 0
+
     if not args.no_e2e:
-        res.update(run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped, fused))
+        res["e2e_loop"] = run_e2e_loop(args, st, dev)
+        res["e2e_replay"] = run_e2e_replay(args, st, dev)
+    del scratch
+    if rank == 0 and not args.no_configs:
+        res["configs"] = run_configs(args, dev, cpu_refs)
     return res
 
 
-AUX_WORKLOADS = ("swap", "layers40", "prefill")
+def run_e2e_loop(args, st, dev):
+    """A decode loop through the C ABI, timed on the host clock: each step the C++ block manager
+    assigns the new tokens' slots (pkv_bm_append_slots) and writes the padded tables
+    (pkv_bm_block_tables) into page-locked host buffers; the kernels read those, q and the new K/V
+    rows across NVLink-C2C and write the output into page-locked host memory (with --grouped: one
+    packed host-to-device copy of the step's inputs and a copy of the output back, since that
+    entry loads q by TMA from device memory); the host waits for the output.  The contexts grow by
+    one token a step, so every step appends where the last one left off."""
+    import torch
+    pkv, w, x = st.pkv, st.w, st.x
+    bm, seqs = x["manager"], x["seqs"]
+    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
+    warm = max(args.warmup, 3)
+    free = int(bm.stats()[0])
+    # steps the free blocks carry: each sequence opens a block at most once every B tokens (and
+    # copies at most one block on its first append)
+    cap = (free // max(S, 1) - 2) * B
+    n = min(args.steps, cap - warm)
+    if n < 1:
+        return {"skipped": f"the pool's {free} free blocks carry no {warm} + 1 steps"}
+    max_blocks = w.max_blocks_per_seq + -(-(warm + n + 1) // B) + 1
+    ws = pkv.workspace_for(S, H, D, max_blocks, B, dev)
+    if st.grouped is not None:
+        n_ws = pkv.paged_attention_shared_prefix_workspace_size(S, H, D, max_blocks, B)
+        ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device=dev)
+    pin = lambda t: t.cpu().contiguous().pin_memory()                        # noqa: E731
+    q_h, key_h, value_h = pin(st.q), pin(st.key), pin(st.value)
+    slots_h = torch.zeros(S, dtype=torch.int64).pin_memory()
+    pairs_h = torch.zeros((max(S, 1), 2), dtype=torch.int64).pin_memory()
+    tables_h = torch.full((S, max_blocks), -1, dtype=torch.int32).pin_memory()
+    lens_h = torch.zeros(S, dtype=torch.int32).pin_memory()
+    out_h = torch.empty(tuple(st.q.shape), dtype=torch.float16).pin_memory()
+    sl_n, pr_n, tb_n, ln_n = slots_h.numpy(), pairs_h.numpy(), tables_h.numpy(), lens_h.numpy()
+    stream = st.stream
+    staged = st.grouped is not None
+    if staged:
+        dev_in = {n_: torch.empty_like(t, device=dev) for n_, t in
+                  (("slots", slots_h), ("pairs", pairs_h), ("tables", tables_h), ("lens", lens_h))}
+        out_d = torch.empty_like(st.q)
+    host_s = [0.0]
 
+    def one_step():
+        h0 = time.perf_counter()
+        sl, pr = bm.append_slots(seqs)
+        tb, ln = bm.block_tables(seqs, max_blocks)
+        sl_n[:] = sl
+        tb_n[:] = tb
+        ln_n[:] = ln
+        npairs = int(pr.shape[0])
+        if npairs:
+            pr_n[:npairs] = pr
+        host_s[0] += time.perf_counter() - h0
+        if not staged:
+            if npairs:
+                pkv.copy_blocks([st.k], [st.v], pairs_h[:npairs], stream=stream)
+            if st.fused:
+                pkv.paged_attention_decode_append(q_h, key_h, value_h, slots_h, st.k, st.v, tables_h, lens_h,
+                                                  w.scale, B, out=out_h, workspace=ws, stream=stream)
+            else:
+                pkv.reshape_and_cache(key_h, value_h, st.k, st.v, slots_h, stream=stream)
+                pkv.paged_attention_decode(q_h, st.k, st.v, tables_h, lens_h, w.scale, B, out=out_h, workspace=ws,
+                                           stream=stream)
+        else:
+            for n_, t in (("slots", slots_h), ("tables", tables_h), ("lens", lens_h)):
+                dev_in[n_].copy_(t, non_blocking=True)
+            if npairs:
+                dev_in["pairs"][:npairs].copy_(pairs_h[:npairs], non_blocking=True)
+                pkv.copy_blocks([st.k], [st.v], dev_in["pairs"][:npairs], stream=stream)
+            pkv.reshape_and_cache(st.key, st.value, st.k, st.v, dev_in["slots"], stream=stream)
+            g = st.grouped
+            pkv.paged_attention_decode_shared_prefix(st.q, st.k, st.v, dev_in["tables"], dev_in["lens"], g["gs"],
+                                                     g["pl"], w.scale, B, g["max_group"], out=out_d, workspace=ws,
+                                                     stream=stream)
+            out_h.copy_(out_d, non_blocking=True)
+        stream.synchronize()
+        return int(ln.astype(np.int64).sum()), npairs
+
+    for _ in range(warm):
+        one_step()
+    assert pkv.device_error() == 0
+    host_s[0] = 0.0
+    kv = 0
+    copies = 0
+    t0 = time.perf_counter()
+    for _ in range(n):
+        tokens, npairs = one_step()
+        kv += tokens * H * D * 2 * 2
+        copies += npairs
+    secs = time.perf_counter() - t0
+    assert pkv.device_error() == 0
+    step_in = q_h.nbytes + key_h.nbytes + value_h.nbytes + slots_h.nbytes + tables_h.nbytes + lens_h.nbytes
+    return {"steps": n, "seconds": secs, "kv_bytes": kv, "ms_per_step": secs / n * 1e3,
+            "host_a1_us_per_step": host_s[0] / n * 1e6, "copies": copies,
+            "h2d_bytes_per_step": step_in + 16 * copies // max(n, 1), "d2h_bytes_per_step": out_h.nbytes,
+            "staged": staged}
+
+
+def run_e2e_replay(args, st, dev):
+    """The step's fixed inputs through the C ABI in page-locked host memory, replayed as a CUDA
+    graph of the API calls (what a serving loop does with a fixed-shape decode step), two ways:
+    direct (the kernels read the inputs and write the output across NVLink-C2C) and staged (one
+    packed host->device copy of the inputs and a device->host copy of the output); the host waits
+    for the output every step.  A grouped step is staged only (q is loaded by TMA)."""
+    import torch
+    pkv, w, x = st.pkv, st.w, st.x
+    parts = {"q": st.q.cpu(), "key": st.key.cpu(), "value": st.value.cpu(),
+             "slots": torch.from_numpy(np.ascontiguousarray(x["slots"])),
+             "pairs": torch.from_numpy(np.ascontiguousarray(x["pairs"])),
+             "tables": torch.from_numpy(w.block_tables), "lens": torch.from_numpy(w.context_lens)}
+    if st.grouped is not None:
+        parts["gs"] = torch.from_numpy(st.grouped["gs_h"])
+        parts["pl"] = torch.from_numpy(st.grouped["pl_h"])
+    # one pinned byte buffer holding every input at a 256-byte-aligned offset, and its device twin
+    offs, total = {}, 0
+    for n_, t in parts.items():
+        offs[n_] = total
+        total += -(-(t.numel() * t.element_size()) // 256) * 256
+    host_buf = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    dbuf, hbuf = {}, {}
+    for n_, t in parts.items():
+        nbytes = t.numel() * t.element_size()
+        host_buf[offs[n_]:offs[n_] + nbytes].copy_(t.contiguous().view(-1).view(torch.uint8))
+        dbuf[n_] = dev_buf[offs[n_]:offs[n_] + nbytes].view(t.dtype).view(t.shape)
+        hbuf[n_] = host_buf[offs[n_]:offs[n_] + nbytes].view(t.dtype).view(t.shape)
+    out_h = torch.empty(tuple(st.q.shape), dtype=torch.float16).pin_memory()
+    out_d = torch.empty_like(st.q)
+    h2d = sum(t.numel() * t.element_size() for t in parts.values())
+    B = w.block_size
+
+    def step_calls(s_, src, out):
+        if st.n_pairs:
+            pkv.copy_blocks([st.k], [st.v], src["pairs"], stream=s_)
+        if st.fused:
+            pkv.paged_attention_decode_append(src["q"], src["key"], src["value"], src["slots"], st.k, st.v,
+                                              src["tables"], src["lens"], w.scale, B, out=out, workspace=st.ws,
+                                              stream=s_)
+            return
+        pkv.reshape_and_cache(src["key"], src["value"], st.k, st.v, src["slots"], stream=s_)
+        if st.grouped is None:
+            pkv.paged_attention_decode(src["q"], st.k, st.v, src["tables"], src["lens"], w.scale, B, out=out,
+                                       workspace=st.ws, stream=s_)
+        else:
+            pkv.paged_attention_decode_shared_prefix(src["q"], st.k, st.v, src["tables"], src["lens"], src["gs"],
+                                                     src["pl"], w.scale, B, st.grouped["max_group"], out=out,
+                                                     workspace=st.ws, stream=s_)
+
+    def staged(s_):
+        dev_buf.copy_(host_buf, non_blocking=True)
+        step_calls(s_, dbuf, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+
+    def direct(s_):
+        step_calls(s_, hbuf, out_h)
+
+    def timed(body):
+        stream = torch.cuda.current_stream()
+        for _ in range(max(args.warmup, 3)):
+            body(stream)
+            stream.synchronize()
+        graph, how = None, "eager API calls"
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            graph, how = g, "CUDA graph of the API calls, replayed"
+        except Exception as e:  # noqa: BLE001 - any capture failure falls back to the eager step
+            how = f"eager API calls (graph capture failed: {type(e).__name__})"
+            torch.cuda.synchronize()
+
+        def one():
+            if graph is not None:
+                graph.replay()
+            else:
+                body(stream)
+            stream.synchronize()
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            one()
+        return (time.perf_counter() - t0) / args.steps * 1e3, how
+
+    staged_ms, how = timed(staged)
+    res = {"staged_ms_per_step": staged_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_h.nbytes}
+    if st.grouped is None:
+        direct_ms, how_d = timed(direct)
+        res.update(ms_per_step=direct_ms, launch=how_d + "; the kernels read the fixed inputs from page-locked "
+                   "host memory over NVLink-C2C and write the output there (no staging copies)")
+    else:
+        res.update(ms_per_step=staged_ms, launch=how + "; one staging copy each way")
+    return res
+
+
+# ---- the other configurations ----------------------------------------------------------------------
+
+# (name, workload, capacity sequences)
+CONFIG_RUNS = (("tiny", "tiny", 0), ("parallel_sampling_cow", "parallel_sampling_cow", 0),
+               ("shared_prefix", "shared_prefix", 0), ("capacity_S1", "capacity", 1),
+               ("capacity_S64", "capacity", 64))
+
+
+def config_sample(w, name):
+    """Sequences of a configuration the oracle checks: all of the tiny batch, else the longest and
+    the shortest (the first and last when all are equally long)."""
+    if name == "tiny":
+        return list(range(w.num_seqs))
+    lens = w.context_lens
+    a, b = int(np.argmax(lens)), int(np.argmin(lens))
+    if a == b:
+        b = w.num_seqs - 1
+    return sorted({a, b})
+
+
+def run_configs(args, dev, cpu_refs):
+    """The other workloads of the path, each as the bench's step on one GPU: effective KV GB/s over
+    CONFIG_STEPS steps (L2 flushed before each step where L2 would hold the batch), the fraction of
+    the measured HBM peak, and the max abs error of sampled sequences against the oracle outputs
+    the CPU-baseline leg computed on the same batch (built there by the oracle's block manager;
+    the sampled table rows are compared too).  The parallel-sampling entry also times its 96
+    copy-on-write copies as one copy_blocks call and checks them byte for byte."""
+    import torch
+    peak, _ = measured_hbm_peak()
+    out = {}
+    for name, workload, cap_seqs in CONFIG_RUNS:
+        x = build_step_inputs(workload_seed(workload), workload, cap_seqs or 64, 16)
+        st = Step(x, dev, fused=True)
+        pkv, w = st.pkv, st.w
+        flush = needs_flush(w)
+        scratch = torch.empty(2 * l2_cache_bytes(dev), dtype=torch.uint8, device=dev) if flush else None
+        st()
+        torch.cuda.synchronize()
+        assert pkv.device_error() == 0
+        entry = {"workload": x["desc"], "num_seqs": w.num_seqs, "logical_kv_bytes": w.logical_kv_bytes(),
+                 "physical_kv_bytes": w.physical_kv_bytes(), "l2_flushed": flush, "steps": CONFIG_STEPS}
+        seqs = config_sample(w, name)
+        ref = None if cpu_refs is None else cpu_refs.get(name)
+        if ref is not None:
+            assert ref["seqs"] == seqs
+            assert np.array_equal(ref["tables"], w.block_tables[seqs]), "oracle-built tables differ"
+            got = st.out[seqs].double().cpu().numpy()
+            entry["max_abs_err"] = float(np.max(np.abs(got - ref["out"])))
+            entry["checked_seqs"] = seqs
+        else:
+            entry["max_abs_err"] = None
+        for _ in range(3):
+            st()
+        times = time_steps(st, CONFIG_STEPS, st.stream, scratch)
+        ms = sum(times) / len(times)
+        entry.update(step_ms=ms, **{"GB/s": w.logical_kv_bytes() / (ms * 1e-3) / 1e9,
+                                    "physical_GB/s": w.physical_kv_bytes() / (ms * 1e-3) / 1e9})
+        entry["frac_of_measured"] = entry["GB/s"] / peak
+        entry["attention_bytes_GB/s"] = st.attention_bytes() / (ms * 1e-3) / 1e9
+        if len(x["setup_pairs"]):
+            sp = torch.from_numpy(np.ascontiguousarray(x["setup_pairs"])).to(dev)
+            fn = lambda: pkv.copy_blocks([st.k], [st.v], sp, stream=st.stream)   # noqa: E731
+            fn()
+            torch.cuda.synchronize()
+            src, dst = sp[:, 0], sp[:, 1]
+            exact = bool(torch.equal(st.k[dst].view(torch.int16), st.k[src].view(torch.int16)) and
+                         torch.equal(st.v[dst].view(torch.int16), st.v[src].view(torch.int16)))
+            cms = time_steps(fn, 20, st.stream)[0]
+            moved = 2 * 2 * len(sp) * w.num_heads * w.block_size * w.head_dim * 2
+            entry["copy_blocks"] = {"pairs": int(len(sp)), "ms": cms, "GB/s": moved / (cms * 1e-3) / 1e9,
+                                    "bit_exact": exact}
+        assert pkv.device_error() == 0
+        out[name] = entry
+        del st, scratch
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---- auxiliary workloads ---------------------------------------------------------------------------
 
 def _timed(fn, reps=10, warm=3):
     import torch
@@ -639,7 +1094,7 @@ def run_swap(args, dev):
 
     m_out = _timed(per_block_out, reps=3, warm=1)
     m_in = _timed(per_block_in, reps=3, warm=1)
-    gbs = lambda ms: payload / (ms * 1e-3) / 1e9
+    gbs = lambda ms: payload / (ms * 1e-3) / 1e9                       # noqa: E731
     value = 2 * payload / ((t_out + t_in) * 1e-3) / 1e9
     return {"metric": "swap_blocks GB/s (HBM <-> page-locked Grace memory, both directions)", "value": value,
             "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f16 (bit copy)",
@@ -677,7 +1132,7 @@ def run_layers40(args, dev):
     assert pkv.device_error() == 0
     r_bytes = 2 * 2 * L * T * H * D * 2                      # K and V, read and written
     c_bytes = 2 * 2 * L * 96 * H * B * D * 2
-    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9                           # noqa: E731
     return {"metric": "multi-layer cache ops GB/s (40 layers, one launch)", "value": gbs(c_bytes, t_c1),
             "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f16 (bit copy)", "data": "synthetic",
             "config": {"workload": "layers40: 40 layers x [1024 blocks, 40, 16, 128]; 64 new tokens; 96 copy pairs"},
@@ -717,7 +1172,7 @@ def run_prefill(args, dev):
     out = torch.empty_like(q)
     maxq = int(news.max())
     flops = sum(4 * D * H * int((np.arange(int(c) - int(n), int(c)) + 1).sum()) for c, n in zip(w.context_lens, news))
-    attn = lambda: pkv.paged_attention_prefill(q, k, v, tables, lens, qsd, w.scale, B, maxq, out=out)
+    attn = lambda: pkv.paged_attention_prefill(q, k, v, tables, lens, qsd, w.scale, B, maxq, out=out)  # noqa: E731
 
     def step():
         pkv.reshape_and_cache(key, value, k, v, slots_d)
@@ -729,9 +1184,9 @@ def run_prefill(args, dev):
     qs2 = np.arange(0, 8 * 4096 + 1, 4096, dtype=np.int32)
     q2 = wl.dense_tensor((8 * 4096, H, D), SEED + 1, wl.STREAM_Q, dev)
     out2 = torch.empty_like(q2)
-    t2, l2, qs2d = (torch.from_numpy(x).to(dev) for x in (wl2.block_tables, wl2.context_lens, qs2))
+    t2, l2, qs2d = (torch.from_numpy(a).to(dev) for a in (wl2.block_tables, wl2.context_lens, qs2))
     flops2 = 8 * 4 * D * H * (4096 * 4097 // 2)
-    attn2 = lambda: pkv.paged_attention_prefill(q2, k2, v2, t2, l2, qs2d, wl2.scale, B, 4096, out=out2)
+    attn2 = lambda: pkv.paged_attention_prefill(q2, k2, v2, t2, l2, qs2d, wl2.scale, B, 4096, out=out2)  # noqa: E731
 
     steps = max(3, min(args.steps, 50))
     with ClockSampler(physical_gpu_index(torch.cuda.current_device())) as clocks:
@@ -764,16 +1219,6 @@ def run_prefill(args, dev):
             "clocks": clock_summary}
 
 
-def measured_tensor_peak():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            v = float(json.load(f)["bf16_tflops"])
-        return v, "measured bf16 dense burst (MEASURED_PEAKS.json bf16_tflops; fp16 has the same nominal rate), of measured"
-    except (OSError, KeyError, ValueError):
-        return 1900.0, "fallback 1.9 PFLOP/s bf16 burst"
-
-
 def pool_blocks_for(args, dev):
     """Pool size for the capacity workload: a fraction of free HBM, or just enough."""
     if args.workload != "capacity" or args.pool_frac <= 0:
@@ -793,153 +1238,52 @@ def physical_gpu_index(local: int) -> int:
     return local
 
 
-def run_e2e(args, w, slots, pairs, q, key, value, k, v, dev, ws, grouped=None, fused=False):
-    """Same step through the C ABI, with the step's inputs in pinned host memory, two ways.
+# ---- the oracle on the host cores -------------------------------------------------------------------
 
-    direct: the kernels read q, the new keys/values, slot mapping, copy pairs,
-    block tables and context lengths from the page-locked host buffer across the
-    host link (NVLink-C2C) and write the attention output into page-locked host
-    memory; the step ends when the stream has finished (wall clock).  Each step's
-    1.4 GB K/V stream evicts the previous step's lines from L2, so every step's
-    inputs cross the link again.
-    staged: one packed host->device copy of the same inputs, the kernels, and a
-    device->host copy of the output, then the wait.
-    The shared-prefix entry loads q by TMA from device memory, so a grouped step
-    is measured staged only.
-    """
-    import torch
-    from paged_kv_cache_73_gb300 import binding as pkv
-
-    parts = {
-        "q": q.cpu(), "key": key.cpu(), "value": value.cpu(),
-        "slots": torch.from_numpy(slots),
-        "pairs": torch.from_numpy(np.ascontiguousarray(pairs)),
-        "tables": torch.from_numpy(w.block_tables),
-        "lens": torch.from_numpy(w.context_lens),
-    }
-    if grouped is not None:
-        parts["gs"] = torch.from_numpy(grouped["gs_h"])
-        parts["pl"] = torch.from_numpy(grouped["pl_h"])
-    # one pinned byte buffer holding every input at a 256-byte-aligned offset, and its device twin
-    offs, total = {}, 0
-    for n, t in parts.items():
-        offs[n] = total
-        total += -(-(t.numel() * t.element_size()) // 256) * 256
-    host_buf = torch.zeros(total, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    dbuf, hbuf = {}, {}
-    for n, t in parts.items():
-        nbytes = t.numel() * t.element_size()
-        host_buf[offs[n]:offs[n] + nbytes].copy_(t.contiguous().view(-1).view(torch.uint8))
-        dbuf[n] = dev_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
-        hbuf[n] = host_buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
-    out_h = torch.empty(tuple(q.shape), dtype=torch.float16).pin_memory()
-    out_d = torch.empty_like(q)
-    n_pairs = int(pairs.shape[0])
-    h2d = sum(t.numel() * t.element_size() for t in parts.values())
-    d2h = out_h.numel() * out_h.element_size()
-
-    def step_calls(st, src, out):
-        if n_pairs:
-            pkv.copy_blocks([k], [v], src["pairs"], stream=st)
-        if fused:
-            pkv.paged_attention_decode_append(src["q"], src["key"], src["value"], src["slots"], k, v, src["tables"],
-                                              src["lens"], w.scale, w.block_size, out=out, workspace=ws, stream=st)
-            return
-        pkv.reshape_and_cache(src["key"], src["value"], k, v, src["slots"], stream=st)
-        if grouped is None:
-            pkv.paged_attention_decode(src["q"], k, v, src["tables"], src["lens"], w.scale, w.block_size,
-                                       out=out, workspace=ws, stream=st)
-        else:
-            pkv.paged_attention_decode_shared_prefix(src["q"], k, v, src["tables"], src["lens"], src["gs"],
-                                                     src["pl"], w.scale, w.block_size, grouped["max_group"],
-                                                     out=out, workspace=ws, stream=st)
-
-    def staged(st):
-        dev_buf.copy_(host_buf, non_blocking=True)
-        step_calls(st, dbuf, out_d)
-        out_h.copy_(out_d, non_blocking=True)
-
-    def direct(st):
-        step_calls(st, hbuf, out_h)
-
-    def timed(body):
-        stream = torch.cuda.current_stream()
-        for _ in range(max(args.warmup, 3)):
-            body(stream)
-            stream.synchronize()
-        # the step as a CUDA graph, recorded once through the same API calls and replayed every
-        # step (what a serving loop does with a fixed-shape decode step); eager calls if capture fails
-        graph, how = None, "eager API calls"
-        try:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                body(torch.cuda.current_stream())
-            torch.cuda.synchronize()
-            graph, how = g, "CUDA graph of the API calls, replayed"
-        except Exception as e:  # noqa: BLE001 - any capture failure falls back to the eager step
-            how = f"eager API calls (graph capture failed: {type(e).__name__})"
-            torch.cuda.synchronize()
-
-        def step():
-            if graph is not None:
-                graph.replay()
-            else:
-                body(stream)
-            stream.synchronize()
-
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            step()
-        return (time.perf_counter() - t0) / args.steps * 1e3, how
-
-    staged_ms, how = timed(staged)
-    res = {"e2e_staged_ms": staged_ms, "h2d": h2d, "d2h": d2h}
-    if grouped is None:
-        direct_ms, how_d = timed(direct)
-        res.update(e2e_step_ms=direct_ms, launch=how_d + "; the kernels read the inputs from page-locked "
-                   "host memory over NVLink-C2C and write the output there (no staging copies)")
-    else:
-        res.update(e2e_step_ms=staged_ms, launch=how + "; one staging copy each way")
-    return res
-
-
-def prepare_cpu_sample(w, seqs, slots, seed):
-    """Host inputs of the oracle for sequences `seqs` of the step (generated once, untimed)."""
+def prepare_cpu_sample(w, seqs, slots, pairs, seed):
+    """Host inputs of the oracle for sequences `seqs` of the step (generated once, untimed): the
+    blocks their tables map (plus the source of every copy into one of them), regenerated on the
+    CPU into a compact pool, and the step's copies and new-token slots renumbered into it."""
     from paged_kv_cache_73_gb300 import workloads as wl
 
     S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
-    kc, vc, tabs, lens = w.compact_pools(seqs)
-    key, value = wl.new_tokens(S, H, D, seed, "cpu")
-    # the new tokens' slots re-expressed in the compact pool's block numbering
-    ids = sorted({int(x) for x in w.block_tables[seqs].ravel() if x >= 0})
+    seqs = list(seqs)
+    mapped = {int(b) for b in w.block_tables[seqs].ravel() if b >= 0}
+    copies = [(int(a), int(b)) for a, b in np.asarray(pairs).reshape(-1, 2) if int(b) in mapped]
+    kc, vc, tabs, lens, ids = w.compact_pools_with(seqs, [a for a, _ in copies])
     remap = {b: i for i, b in enumerate(ids)}
+    key, value = wl.new_tokens(S, H, D, seed, "cpu")
     local = [remap[int(slots[s]) // B] * B + int(slots[s]) % B for s in seqs]
     return {"k": kc.numpy(), "v": vc.numpy(), "tables": tabs, "lens": lens, "slots": local,
+            "pairs": [(remap[a], remap[b]) for a, b in copies],
             "key": key.numpy()[seqs], "value": value.numpy()[seqs], "q": w.q("cpu").numpy()[seqs],
             "scale": w.scale, "kv_bytes": int(lens.astype(np.int64).sum()) * H * D * 2 * 2}
 
 
-def cpu_sample_seconds(x):
-    """Oracle (fp64, host) over a prepared sample: the new-token writes, then attention."""
+def cpu_sample_run(x):
+    """The oracle (fp64, host) over a prepared sample: the step's copies, the new-token writes,
+    then attention.  Returns (seconds, output)."""
     from oracle import attention as oracle_attention
     from oracle import cache_ops as oracle_cache_ops
 
     t0 = time.perf_counter()
+    if x["pairs"]:
+        oracle_cache_ops.copy_blocks([x["k"]], [x["v"]], x["pairs"])
     oracle_cache_ops.reshape_and_cache(x["key"], x["value"], x["k"], x["v"], x["slots"])
-    oracle_attention.paged_decode_attention(x["q"], x["k"], x["v"], x["tables"], x["lens"], x["scale"])
-    return time.perf_counter() - t0
+    out = oracle_attention.paged_decode_attention(x["q"], x["k"], x["v"], x["tables"], x["lens"], x["scale"])
+    return time.perf_counter() - t0, out
+
+
+def cpu_sample_seconds(x):
+    return cpu_sample_run(x)[0]
 
 
 def _cpu_worker(job):
-    """One process of the all-cores CPU baseline: regenerate this worker's share of the sample,
-    wait for the others, time the oracle on it."""
+    """One process of the all-cores CPU baseline: regenerate this worker's share of the sample
+    (the batch built by the oracle's block manager), wait for the others, time the oracle on it."""
     seqs, workload, capacity_seqs, capacity_block, start = job
-    x0 = build_step_inputs(SEED, workload, capacity_seqs, capacity_block)
-    x = prepare_cpu_sample(x0["w"], seqs, x0["slots"], SEED)
+    x0 = build_step_inputs(workload_seed(workload), workload, capacity_seqs, capacity_block, manager="oracle")
+    x = prepare_cpu_sample(x0["w"], seqs, x0["slots"], x0["pairs"], workload_seed(workload))
     start.wait()
     t0 = time.time()
     cpu_sample_seconds(x)
@@ -964,27 +1308,97 @@ def run_cpu_baseline_all_cores(args, seqs):
             "sample": f"the same {len(seqs)} sequences over {n} single-threaded processes, {wall:.2f} s"}
 
 
+def cpu_config_refs():
+    """Oracle outputs of the sampled sequences of every entry of `configs` (the batch built by the
+    oracle's block manager; the step's copies and new-token writes, then attention)."""
+    refs = {}
+    for name, workload, cap_seqs in CONFIG_RUNS:
+        seed = workload_seed(workload)
+        x = build_step_inputs(seed, workload, cap_seqs or 64, 16, manager="oracle")
+        w = x["w"]
+        seqs = config_sample(w, name)
+        _, out = cpu_sample_run(prepare_cpu_sample(w, seqs, x["slots"], x["pairs"], seed))
+        refs[name] = {"seqs": seqs, "out": out, "tables": w.block_tables[seqs].copy()}
+    return refs
+
+
 def run_cpu_baseline(args, budget_s: float = 12.0):
-    x0 = build_step_inputs(SEED, args.workload, args.capacity_seqs, args.capacity_block)
-    w, slots = x0["w"], x0["slots"]
+    """The CPU-baseline leg: the oracle as it stands, on the batch its own block manager builds,
+    timed on one host core over as many sequences as fit the budget (alternately long and short),
+    and on every core; plus the oracle outputs the `configs` entries are checked against."""
+    seed = workload_seed(args.workload)
+    x0 = build_step_inputs(seed, args.workload, args.capacity_seqs, args.capacity_block, manager="oracle")
+    w, slots, pairs = x0["w"], x0["slots"], x0["pairs"]
     S = w.num_seqs
-    order = [int(x) for x in np.argsort(w.context_lens)[::-1]]
+    order = [int(i) for i in np.argsort(w.context_lens)[::-1]]
     seqs = []
     for a, b in zip(order, order[::-1]):               # alternate long and short sequences
         for s in (a, b):
             if s not in seqs:
                 seqs.append(s)
-    probe = cpu_sample_seconds(prepare_cpu_sample(w, seqs[:2], slots, SEED))
+    probe = cpu_sample_seconds(prepare_cpu_sample(w, seqs[:2], slots, pairs, seed))
     n = max(2, min(S, int(budget_s / max(probe / 2, 1e-3))))
-    x = prepare_cpu_sample(w, seqs[:n], slots, SEED)
+    x = prepare_cpu_sample(w, seqs[:n], slots, pairs, seed)
     secs = cpu_sample_seconds(x)
     out = {"value": x["kv_bytes"] / secs / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": f"{n} of the {S} sequences (all {w.num_heads} heads, {int(x['lens'].sum())} tokens), "
-                     f"new-token writes + fp64 attention, numpy single-threaded, {secs:.1f} s"}
+                     f"new-token writes + fp64 attention, numpy single-threaded, {secs:.1f} s; tables and slots "
+                     f"from the oracle's block manager"}
     if (os.cpu_count() or 1) > 1:
         out["all_cores"] = run_cpu_baseline_all_cores(args, seqs[:n])
-    return out
+    refs = None if args.no_configs else cpu_config_refs()
+    return out, refs
 
+
+def reference_sample(w):
+    """The oracle arm's sequences per step: the whole batch, unless its K/V exceeds
+    REF_MAX_KV_BYTES; then the longest sequences up to that many bytes."""
+    if w.logical_kv_bytes() <= REF_MAX_KV_BYTES:
+        return list(range(w.num_seqs)), f"the whole batch ({w.num_seqs} sequences, all {w.num_heads} heads)"
+    per_token = w.num_heads * w.head_dim * 2 * 2
+    seqs, total = [], 0
+    for s in np.argsort(w.context_lens)[::-1]:
+        b = int(w.context_lens[s]) * per_token
+        if seqs and total + b > REF_MAX_KV_BYTES:
+            break
+        seqs.append(int(s))
+        total += b
+    return sorted(seqs), f"{len(seqs)} of the {w.num_seqs} sequences (the longest; the batch exceeds " \
+                         f"{REF_MAX_KV_BYTES / 1e9:.1f} GB of K/V)"
+
+
+def run_reference(args, rank):
+    """The oracle, as it stands, on the host cores: each step the new-token writes and fp64
+    attention over the batch, whose tables and slots the oracle's block manager builds."""
+    if rank != 0:
+        return None
+    if args.workload in AUX_WORKLOADS:
+        return {"impl": "reference", "unavailable": f"the oracle arm times the decode workloads, not {args.workload}"}
+    seed = workload_seed(args.workload)
+    x0 = build_step_inputs(seed, args.workload, args.capacity_seqs, args.capacity_block, manager="oracle")
+    w = x0["w"]
+    seqs, what = reference_sample(w)
+    sample = prepare_cpu_sample(w, seqs, x0["slots"], x0["pairs"], seed)   # generated once, untimed
+    for _ in range(args.warmup):
+        cpu_sample_seconds(sample)
+    secs = 0.0
+    for _ in range(args.steps):
+        secs += cpu_sample_seconds(sample)
+    kv = sample["kv_bytes"] * args.steps
+    value = kv / secs / 1e9
+    desc = f"{what} per step: the step's copies, the new-token writes and fp64 attention (numpy, one thread); " \
+           "tables and slots from the oracle's block manager"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": config_block(args, x0["desc"], w.num_seqs, flushed=needs_flush(w)),
+            "same_config": len(seqs) == w.num_seqs,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---- the line --------------------------------------------------------------------------------------
 
 def reduce_over_ranks(maxed, summed, world, device):
     """Max over ranks of `maxed` (times), sum over ranks of `summed` (bytes)."""
@@ -1010,95 +1424,107 @@ def l2_cache_bytes(dev) -> int:
     return int(getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024)
 
 
-def config_block(args, desc, num_seqs, extra=None, flushed=False):
-    c = {"workload": desc, "num_seqs": num_seqs, "num_heads": 40, "head_dim": 128,
-         "block_size": args.capacity_block if args.workload == "capacity" else 16,
-         "seed": f"{SEED} (+7919*rank)", "kv_storage": "f16",
-         "l2": ("L2 flushed before every step (a write of twice the L2 size, outside the timed region); "
-                "each step timed by its own events") if flushed
-               else "inputs larger than L2: the step reads more than twice the L2 size of distinct K/V"}
-    if extra:
-        c.update(extra)
-    return c
+def config_block(args, desc, num_seqs, flushed=False):
+    """The workload the line is quoted on; the GPU arm and the oracle arm print the same block."""
+    cfg_seed = workload_seed(args.workload)
+    return {"workload": desc, "num_seqs": num_seqs,
+            "num_heads": 2 if args.workload == "tiny" else 40, "head_dim": 64 if args.workload == "tiny" else 128,
+            "block_size": args.capacity_block if args.workload == "capacity" else (4 if args.workload == "tiny" else 16),
+            "seed": f"{cfg_seed} (+7919*rank)", "kv_storage": "f16",
+            "l2": ("L2 flushed before every step (a write of twice the L2 size, outside the timed region); "
+                   "each step timed by its own events") if flushed
+            else "inputs larger than L2: the step reads more than twice the L2 size of distinct K/V"}
 
 
-def run_reference(args, rank):
-    """The oracle, as it stands, on the host cores: each step one sequence of the workload."""
-    if rank != 0:
-        return None
-    x0 = build_step_inputs(SEED, args.workload, args.capacity_seqs, args.capacity_block)
-    w, slots = x0["w"], x0["slots"]
-    order = [int(x) for x in np.random.default_rng(0).permutation(w.num_seqs)][:8]
-    samples = [prepare_cpu_sample(w, [s], slots, SEED) for s in order]   # generated once, untimed
-    for i in range(args.warmup):
-        cpu_sample_seconds(samples[i % len(samples)])
-    secs, kv = 0.0, 0
-    for i in range(args.steps):
-        x = samples[i % len(samples)]
-        secs += cpu_sample_seconds(x)
-        kv += x["kv_bytes"]
-    value = kv / secs / 1e9
-    sample = f"one sequence (all {w.num_heads} heads) per step, cycling over {len(samples)} of the {w.num_seqs}"
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded counter-based generator)",
-            "config": config_block(args, x0["desc"], w.num_seqs, {"reference_sample": sample}),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample + "; new-token write + fp64 attention"},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+def reduce_run(r, world, device):
+    """Whole-job figures of a run: times maxed over ranks, bytes summed over ranks."""
+    loop = r.get("e2e_loop") or {}
+    rep = r.get("e2e_replay") or {}
+    sus = r.get("sustained") or {}
+    names_t = ("step_ms", "attn_ms", "attn_ms_median", "e2e_s", "e2e_replay_ms", "e2e_staged_ms", "sus_s")
+    vals_t = (r["step_ms"], r["attn_ms"], r["attn_ms_median"], loop.get("seconds", 0.0), rep.get("ms_per_step", 0.0),
+              rep.get("staged_ms_per_step", 0.0), sus.get("device_s", 0.0))
+    names_b = ("kv_total", "phys_total", "e2e_kv", "sus_kv")
+    vals_b = (r["kv_bytes"], r["phys_bytes"], loop.get("kv_bytes", 0), sus.get("kv_bytes", 0))
+    t, b = reduce_over_ranks(vals_t, [float(v) for v in vals_b], world, device)
+    return dict(zip(names_t, t)) | dict(zip(names_b, b))
 
 
-def headline_line(args, r, world, cpu, step_ms, e2e_ms, attn_ms, staged_ms, attn_med, kv_total, phys_total):
-    """The JSON line of a decode run: `r` is this rank's run_gpu result, the times (ms) are maxima
-    over ranks and the byte counts sums over ranks."""
+def headline_line(args, r, world, cpu, red):
+    """The JSON line of a decode run: `r` is this rank's run_gpu result, `red` the whole-job
+    figures (reduce_run)."""
     peak, peak_src = measured_hbm_peak()
-    achieved = r["attn_bytes"] / (attn_ms * 1e-3) / 1e9
+    achieved = r["attn_bytes"] / (red["attn_ms"] * 1e-3) / 1e9
     traffic = None if args.grouped else NCU_TRAFFIC.get(
         (args.workload + ("+append" if r["fused"] else ""), attention_source_sha()))
-    value = kv_total / (step_ms * 1e-3) / 1e9
+    value = red["kv_total"] / (red["step_ms"] * 1e-3) / 1e9
     S = r["num_seqs"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": red["step_ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
-        "config": config_block(args, r["desc"], S,
-                               {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                                "partition_tokens": r["part_tokens"], "cow_pairs_per_step": r["n_pairs"],
-                                "pool_blocks": r["num_blocks"]}, flushed=r["l2_flushed"]),
+        "config": config_block(args, r["desc"], S, flushed=r["l2_flushed"]),
+        "parallelism": f"replicas x{world} (each rank its own batch, no exchange)" if world > 1 else "single GPU",
+        "plan": {"partition_tokens": r["part_tokens"], "kernels_per_step": r["kernels_per_step"],
+                 "cow_pairs_per_step": r["n_pairs"], "pool_blocks": r["num_blocks"]},
         "hbm_frac_of_measured": value / peak,
         "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
-        "physical_kv_GBps": phys_total / (step_ms * 1e-3) / 1e9,
-        "tokens_per_s": S * world / (step_ms * 1e-3),
-        "tokens_per_s_40_layer_attention_only": S * world / (40 * step_ms * 1e-3),
+        "physical_kv_GBps": red["phys_total"] / (red["step_ms"] * 1e-3) / 1e9,
+        "tokens_per_s": S * world / (red["step_ms"] * 1e-3),
+        "tokens_per_s_40_layer_attention_only": S * world / (40 * red["step_ms"] * 1e-3),
         "host_slot_assignment_us": r["host_slot_us"],
         "roofline": {"bound": "hbm",
-                     "kernel": ("paged attention call with the new tokens' K/V append (partition + merge "
-                                "kernels); bytes include the appended rows read and written"
-                                if r["fused"] else "paged attention call (partition + merge kernels)")
-                     if r["grouped"] is None
+                     "kernel": ("paged attention call with the new tokens' K/V append; bytes include the "
+                                "appended rows read and written" if r["fused"]
+                                else "paged attention call") if r["grouped"] is None
                      else "shared-prefix attention call (prefix partials on tensor cores + partition + merge); "
                           "bytes = distinct K/V slots + q + out",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": r["attn_bytes"],
-                     "launch_ms": attn_ms, "launch_ms_median": attn_med,
-                     "timed_launches": args.steps if r["l2_flushed"] else (args.steps + EVENT_EVERY - 1) // EVENT_EVERY,
+                     "launch_ms": red["attn_ms"], "launch_ms_median_isolated": red["attn_ms_median"],
+                     "timed_launches": r["timed_launches"], "launch_timing": r["attn_loop"],
                      "peak_source": peak_src + ", of measured"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
+        "clocks_timed_region": r["clocks_timed_region"],
     }
+    if r.get("sustained"):
+        s = r["sustained"]
+        sv = red["sus_kv"] / red["sus_s"] / 1e9 if red["sus_s"] > 0 else None
+        mhz = (s.get("clocks") or {}).get("sm_mhz")
+        line["sustained"] = {"value": sv, "unit": UNIT, "steps": s["steps"], "seconds": s["seconds"],
+                             "ms_per_step": s["ms_per_step"], "clocks": s["clocks"],
+                             "ms_x_median_sm_mhz": None if mhz is None else s["ms_per_step"] * mhz}
     if r["copy"] is not None:
         line["copy_blocks_setup"] = r["copy"]
     if r.get("bm") is not None:
         line["block_manager"] = r["bm"]
     if r["grouped"] is not None:
         line["grouped"] = r["grouped"]
-    if "e2e_step_ms" in r:
-        line["e2e"] = {"value": kv_total / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
-                       "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                       "ms_per_step": e2e_ms, "launch": r.get("launch", "eager API calls"),
-                       "staged_value": kv_total / (staged_ms * 1e-3) / 1e9,
-                       "staged_ms_per_step": staged_ms}
+    loop, rep = r.get("e2e_loop"), r.get("e2e_replay")
+    if loop and "seconds" in loop:
+        e2e = {"value": red["e2e_kv"] / red["e2e_s"] / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": loop["h2d_bytes_per_step"], "d2h_bytes_per_step": loop["d2h_bytes_per_step"],
+               "ms_per_step": loop["ms_per_step"], "steps": loop["steps"],
+               "host_a1_us_per_step": loop["host_a1_us_per_step"], "copies": loop["copies"],
+               "launch": ("eager API calls; every step pkv_bm_append_slots + pkv_bm_block_tables write the step's "
+                          "slots, tables and lengths into page-locked host memory, the kernels read them (and q and "
+                          "the new K/V rows) across NVLink-C2C and write the output there, the host waits; contexts "
+                          "grow by one token a step") if not loop["staged"]
+               else ("eager API calls; every step pkv_bm_append_slots + pkv_bm_block_tables, one copy of the "
+                     "step's inputs to the device and of the output back, the host waits; contexts grow by one "
+                     "token a step")}
+        if rep:
+            e2e["graph_replay"] = {"value": red["kv_total"] / (red["e2e_replay_ms"] * 1e-3) / 1e9,
+                                   "ms_per_step": rep["ms_per_step"], "launch": rep["launch"],
+                                   "staged_value": red["kv_total"] / (red["e2e_staged_ms"] * 1e-3) / 1e9,
+                                   "staged_ms_per_step": rep["staged_ms_per_step"],
+                                   "h2d_bytes_per_step": rep["h2d_bytes_per_step"]}
+        line["e2e"] = e2e
+    elif loop:
+        line["e2e"] = {"value": None, "unit": UNIT, "skipped": loop.get("skipped")}
+    if r.get("configs") is not None:
+        line["configs"] = r["configs"]
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
@@ -1120,38 +1546,28 @@ def main():
     if not torch.cuda.is_available():
         print(json.dumps({"metric": METRIC, "error": "no CUDA device"}), flush=True)
         sys.exit(1)
+
+    cpu, refs = None, None
+    if rank == 0 and not args.no_cpu_baseline and args.workload not in AUX_WORKLOADS:
+        cpu, refs = run_cpu_baseline(args)                # before any GPU work: the oracle runs alone
+
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
+    from paged_kv_cache_73_gb300 import binding as pkv
+    pkv.load()
     if args.workload in AUX_WORKLOADS:
-        from paged_kv_cache_73_gb300 import binding as pkv
-        pkv.load()
         line = {"swap": run_swap, "layers40": run_layers40, "prefill": run_prefill}[args.workload](args, dev)
         if rank == 0:
             print(json.dumps(line), flush=True)
-        return
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = run_cpu_baseline(args)                      # before any timing: the oracle runs alone
-
-    from paged_kv_cache_73_gb300 import binding as pkv
-    pkv.load()
-    r = run_gpu(args, rank, world, dev)
-
-    # whole-job numbers: bytes of all ranks over the slowest rank's time
-    (step_ms, e2e_ms, attn_ms, staged_ms, attn_med), (kv_total, phys_total) = reduce_over_ranks(
-        [r["step_ms"], r.get("e2e_step_ms", 0.0), r["attn_ms"], r.get("e2e_staged_ms", 0.0), r["attn_ms_median"]],
-        [float(r["kv_bytes"]), float(r["phys_bytes"])],
-        world, dev)
-
-    if rank == 0:
-        line = headline_line(args, r, world, cpu, step_ms, e2e_ms, attn_ms, staged_ms, attn_med, kv_total,
-                             phys_total)
-        print(json.dumps(line), flush=True)
+    else:
+        r = run_gpu(args, rank, world, dev, refs)
+        red = reduce_run(r, world, dev)                   # whole job: all ranks' bytes over the slowest rank
+        if rank == 0:
+            print(json.dumps(headline_line(args, r, world, cpu, red)), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -74,9 +74,11 @@ enum {
   PKV_DEV_BAD_SLOT = 3,         /* a slot >= num_blocks*block_size */
   PKV_DEV_BAD_COPY_PAIR = 4,    /* a copy pair with an id outside [0, num_blocks) */
   PKV_DEV_WAIT_TIMEOUT = 5,     /* a shared-memory copy did not complete in time */
-  PKV_DEV_BAD_QUERY_RANGE = 6,  /* prefill: new tokens outside [0, context_len] or outside q */
+  PKV_DEV_BAD_QUERY_RANGE = 6,  /* prefill: new tokens outside [0, context_len] or outside q, or
+                                   more new tokens than max_query_len covers */
   PKV_DEV_PREFIX_MISMATCH = 7   /* shared-prefix decode: a sequence's first prefix blocks differ
-                                   from its group's first sequence's, or a bad group layout */
+                                   from its group's first sequence's, a bad group layout, or a
+                                   group larger than max_group_size */
 };
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
@@ -190,7 +192,9 @@ int pkv_paged_attention_decode_append(const uint16_t* q, const uint16_t* key, co
  *   prefix_lens    device [num_groups] int32: multiples of block_size, each at
  *                  most the group's shortest context (0: no shared prefix)
  *   max_group_size host: the largest group_start[g+1] - group_start[g] (sizes the
- *                  grid; members past it are not processed)
+ *                  grid).  A larger group records PKV_DEV_PREFIX_MISMATCH: its
+ *                  members past the grid get no prefix part and their rows are
+ *                  wrong.
  *   workspace      at least pkv_paged_attention_shared_prefix_workspace_size(...)
  *                  bytes, 16-byte aligned, required.
  *   other arguments as for pkv_paged_attention_decode.
@@ -231,8 +235,9 @@ int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* 
  *   q, out        device [total_q, num_heads, head_dim] fp16, 16-byte aligned;
  *                 out must not overlap the inputs
  *   query_start   device [num_seqs + 1] int32, non-decreasing, last = total_q
- *   max_query_len host: the largest n_s (sizes the grid; larger n_s are not
- *                 fully processed)
+ *   max_query_len host: the largest n_s (sizes the grid).  A larger n_s records
+ *                 PKV_DEV_BAD_QUERY_RANGE, and its rows past the grid are not
+ *                 written.
  *   pools, tables, context_lens as for pkv_paged_attention_decode.
  * scale must be positive.  A sequence with n_s = 0 is skipped; n_s > ctx_s or
  * rows outside q record PKV_DEV_BAD_QUERY_RANGE; a table entry outside
@@ -261,9 +266,12 @@ int pkv_paged_attention_prefill(const uint16_t* q, const uint16_t* k_cache, cons
  *
  *   - A batch whose scratch would exceed the array is rejected with
  *     PKV_ERR_WORKSPACE (and a message) before anything is launched.
- *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress with the device current); make that first
- *     call before any stream capture.
+ *   - The first call on a device looks up the array's device address in the
+ *     caller's current context (cudaGetSymbolAddress with the device current);
+ *     make that first call before any stream capture.  The address is kept
+ *     per context: after cudaDeviceReset, or from a thread whose current
+ *     context is another one (a plugin's own cuCtxCreate), the next call looks
+ *     it up again, and that call too should come before any capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind.  Nothing in it needs clearing: each call writes every partial
  *     result before reading it.  Calls whose kernels overlap on the GPU (on
@@ -396,10 +404,28 @@ int pkv_bm_append_slots(pkv_bm* bm, const int64_t* seq_ids, int n, int64_t* slot
 
 int pkv_bm_free(pkv_bm* bm, int64_t seq_id);
 
+/* n >= 0 appends to one sequence in one all-or-nothing call: the slots of its
+ * next n tokens, in order, to slots_out (host [n]).  Only the first append can
+ * need a copy (of a shared partly filled last block; later appends find the
+ * last block private): it goes to cow_pair_out (host [2] int64 (src, dst), may
+ * be NULL) with *num_cow = 1, else *num_cow = 0 (num_cow may be NULL).  The
+ * prompt phase of a request uses it to place all of its new tokens at once. */
+int pkv_bm_extend(pkv_bm* bm, int64_t seq_id, int n, int64_t* slots_out, int64_t* cow_pair_out, int* num_cow);
+
 /* A provider-stored prefix of len >= 1 tokens ([guide] 04); slots_out as in
  * pkv_bm_add_seq. */
 int pkv_bm_register_prefix(pkv_bm* bm, int64_t prefix_id, int len, int64_t* slots_out);
-int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id);
+
+/* A request on a registered prefix ([guide] 04, steps 2 and 4): its first
+ * logical blocks map onto the prefix's physical blocks (reference counts +1),
+ * then its suffix_len >= 0 own tokens (the task input its prompt phase runs
+ * over) get slots as pkv_bm_extend gives them: slots_out host [suffix_len]
+ * (may be NULL when suffix_len is 0).  A partly filled last prefix block is
+ * shared with the prefix, so the first suffix token copies it (cow_pair_out,
+ * *num_cow = 1; both may be NULL).  All-or-nothing: PKV_ERR_OOM if the suffix
+ * needs more blocks than are free, and nothing changes. */
+int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id, int suffix_len, int64_t* slots_out,
+                               int64_t* cow_pair_out, int* num_cow);
 int pkv_bm_drop_prefix(pkv_bm* bm, int64_t prefix_id);
 
 /* One sequence's physical ids (host out[cap]), block count and token count. */

@@ -157,6 +157,34 @@ class BlockManager:
         last.filled += 1
         return slot, src, dst
 
+    def extend(self, seq_id: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """n appends to one sequence, all or nothing ([guide] 04: the prompt phase places a
+        request's whole task input at once).  Returns (slots in order, copies made).
+
+        The blocks the n appends will take are counted first by walking the same decisions
+        append_slot makes (full last block -> a new block; shared partly filled last block -> a
+        copy, after which the block is private), so a short free list raises MemoryError before
+        anything changes.
+        """
+        if n < 0:
+            raise ValueError("n must be non-negative")
+        last = self.seqs[seq_id][-1]
+        filled, shared, need = last.filled, self.ref[last.physical] > 1, 0
+        for _ in range(n):
+            if filled == self.B:
+                need, filled, shared = need + 1, 0, False
+            elif shared:
+                need, shared = need + 1, False
+            filled += 1
+        self._need(need)
+        slots, copies = [], []
+        for _ in range(n):
+            slot, src, dst = self.append_slot(seq_id)
+            slots.append(slot)
+            if src >= 0:
+                copies.append((src, dst))
+        return slots, copies
+
     def free(self, seq_id: int) -> None:
         for b in self.seqs.pop(seq_id):
             self._release(b.physical)
@@ -172,16 +200,29 @@ class BlockManager:
         self.prefixes[prefix_id] = blocks
         return self._slots(blocks)
 
-    def add_seq_with_prefix(self, seq_id: int, prefix_id: int) -> None:
-        """A request whose first logical blocks are the prefix's physical blocks."""
+    def add_seq_with_prefix(self, seq_id: int, prefix_id: int,
+                            suffix_len: int = 0) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """A request whose first logical blocks are the prefix's physical blocks ([guide] 04 steps
+        2 and 4), followed by ``suffix_len`` tokens of its own (the task input).  Returns the
+        suffix tokens' slots and the copies made (at most one: a partly filled last prefix block
+        is shared with the prefix).  All or nothing: MemoryError leaves the state unchanged."""
         if seq_id in self.seqs:
             raise ValueError(f"sequence {seq_id} exists")
+        if suffix_len < 0:
+            raise ValueError("suffix_len must be non-negative")
         src = self.prefixes[prefix_id]
         for b in src:
             self.ref[b.physical] += 1
         self.seqs[seq_id] = [LogicalBlock(b.physical, b.filled) for b in src]
+        try:
+            out = self.extend(seq_id, suffix_len)
+        except MemoryError:
+            for b in self.seqs.pop(seq_id):
+                self.ref[b.physical] -= 1
+            raise
         self.prefix_seqs += 1
         self.prefix_blocks += len(src)
+        return out
 
     def drop_prefix(self, prefix_id: int) -> None:
         for b in self.prefixes.pop(prefix_id):

@@ -75,7 +75,8 @@ _SIGNATURES = {
     "pkv_bm_append_slots": (_I, [_P, _P, _I, _P, _P, _c.POINTER(_I)]),
     "pkv_bm_free": (_I, [_P, _I64]),
     "pkv_bm_register_prefix": (_I, [_P, _I64, _I, _P]),
-    "pkv_bm_add_seq_with_prefix": (_I, [_P, _I64, _I64]),
+    "pkv_bm_add_seq_with_prefix": (_I, [_P, _I64, _I64, _I, _P, _P, _c.POINTER(_I)]),
+    "pkv_bm_extend": (_I, [_P, _I64, _I, _P, _P, _c.POINTER(_I)]),
     "pkv_bm_drop_prefix": (_I, [_P, _I64]),
     "pkv_bm_block_table": (_I, [_P, _I64, _P, _I, _c.POINTER(_I), _c.POINTER(_I)]),
     "pkv_bm_block_tables": (_I, [_P, _P, _I, _P, _I, _P]),
@@ -142,6 +143,11 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dim: int, cuda: bool =
         raise PkvError(PKV_ERR_INVALID_ARG,
                        f"{name}: want a contiguous {where}{dtype} tensor of rank {dim}, "
                        f"got {t.dtype} {tuple(t.shape)} contiguous={t.is_contiguous()} device={t.device}")
+    if t.is_cuda and t.device.index != torch.cuda.current_device():
+        # the library launches on the current device; another device's memory would be a peer read
+        raise PkvError(PKV_ERR_INVALID_ARG,
+                       f"{name}: on {t.device}, but the current CUDA device is cuda:{torch.cuda.current_device()} "
+                       f"(make it current, e.g. with torch.cuda.device({t.device}))")
 
 
 def _out_like(q: torch.Tensor) -> torch.Tensor:
@@ -521,8 +527,24 @@ class BlockManager:
         _check(self._lib.pkv_bm_register_prefix(self._h, prefix_id, length, _np_ptr(slots)))
         return slots[:length]
 
-    def add_seq_with_prefix(self, seq_id: int, prefix_id: int) -> None:
-        _check(self._lib.pkv_bm_add_seq_with_prefix(self._h, seq_id, prefix_id))
+    def add_seq_with_prefix(self, seq_id: int, prefix_id: int, suffix_len: int = 0) -> Tuple[np.ndarray, np.ndarray]:
+        """Map the prefix's blocks, then place ``suffix_len`` own tokens (all or nothing).
+        Returns the suffix slots [suffix_len] and the copies [0 or 1, 2] (src, dst) to run first."""
+        slots = np.empty(max(suffix_len, 1), dtype=np.int64)
+        pair = np.empty(2, dtype=np.int64)
+        nc = _c.c_int(0)
+        _check(self._lib.pkv_bm_add_seq_with_prefix(self._h, seq_id, prefix_id, suffix_len, _np_ptr(slots),
+                                                    _np_ptr(pair), ctypes.byref(nc)))
+        return slots[:suffix_len], pair.reshape(1, 2)[:nc.value]
+
+    def extend(self, seq_id: int, n: int) -> Tuple[np.ndarray, np.ndarray]:
+        """Slots of the sequence's next n tokens in one all-or-nothing call, and the copy
+        [0 or 1, 2] (src, dst) that must run before they are written."""
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pair = np.empty(2, dtype=np.int64)
+        nc = _c.c_int(0)
+        _check(self._lib.pkv_bm_extend(self._h, seq_id, n, _np_ptr(slots), _np_ptr(pair), ctypes.byref(nc)))
+        return slots[:n], pair.reshape(1, 2)[:nc.value]
 
     def drop_prefix(self, prefix_id: int) -> None:
         _check(self._lib.pkv_bm_drop_prefix(self._h, prefix_id))

@@ -35,6 +35,7 @@
 //  * Every wait is bounded by a global-timer deadline; on expiry the kernel
 //    records PKV_DEV_WAIT_TIMEOUT, waits (bounded) for its own copies in
 //    flight and returns.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -873,6 +874,8 @@ int pkv_paged_attention_plan(int num_seqs, int num_heads, int head_dim, int max_
       (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32))
     return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_plan: head_dim %d / block_size %d", head_dim,
                      block_size);
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > (1LL << 30))
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_plan: context capacity above 2^30 tokens");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
   const int max_ctx = max_blocks_per_seq * block_size;
@@ -1038,24 +1041,59 @@ constexpr size_t kStaticWorkspaceBytes = size_t(16) << 20;  // 16 MiB, held on e
 
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-// Device address of g_static_workspace on `dev` (looked up once per device, with
-// that device current); nullptr with the status in *rc on failure.
+// Driver calls that name the caller's current context, reached through the runtime's entry-point
+// query so that the library does not link libcuda itself.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (never reused within the process, unlike the
+// context handle, which a context created after cudaDeviceReset may share).  0 on failure.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_static_workspace in the caller's current context on `dev`.  The lookup
+// (cudaGetSymbolAddress, with the device current) runs once per context: the first call on a
+// device, and again after cudaDeviceReset or under another context (a plugin's own cuCtxCreate),
+// since the array then lives at another address.  nullptr with the status in *rc on failure.
 void* static_workspace_address(int dev, int* rc) {
   static std::mutex mu;
+  static unsigned long long ctx_of[64] = {0};
   static void* addr[64] = {nullptr};
   std::lock_guard<std::mutex> g(mu);
   if (dev < 0 || dev >= 64) {
     *rc = pkv::fail(PKV_ERR_UNSUPPORTED, "static-workspace attention: device ordinal %d above 63", dev);
     return nullptr;
   }
-  if (!addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void* ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
     if (e != cudaSuccess || ptr == nullptr) {
+      addr[dev] = nullptr;
       *rc = pkv::fail(PKV_ERR_CUDA, "static-workspace attention: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
       return nullptr;
     }
     addr[dev] = ptr;
+    ctx_of[dev] = ctx;
   }
   *rc = PKV_OK;
   return addr[dev];
@@ -1076,6 +1114,8 @@ int pkv_paged_attention_decode_static_workspace(const uint16_t* q, const uint16_
     return pkv_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads,
                                       head_dim, num_blocks, max_blocks_per_seq, scale, block_size, out, nullptr, 0,
                                       stream);
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > (1LL << 30))
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode_static_workspace: context capacity above 2^30 tokens");
   int part_tokens = 0, kernels = 0;
   int rc = pkv_paged_attention_plan(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size, &part_tokens,
                                     &kernels);

@@ -70,6 +70,34 @@ struct Manager {
     if (last.filled == B) return true;
     return ref[last.phys] - extra_dec > 1;
   }
+  // Free blocks that n >= 0 appends to `blocks` take: a copy of a shared partly filled last
+  // block (the first append), then a new block each time the last one is full.
+  int blocks_for_appends(const std::vector<Logical>& blocks, int n) const {
+    if (n <= 0) return 0;
+    const Logical& last = blocks.back();
+    const int room = B - last.filled;                  // rows left in the last block
+    const int copy = (room > 0 && ref[last.phys] > 1) ? 1 : 0;
+    const int past = n - room;                         // tokens that spill into new blocks
+    return copy + (past > 0 ? (past + B - 1) / B : 0);
+  }
+  // n appends in order (the caller checked the free blocks): slots to slots_out[0..n), the one
+  // possible copy to cow_pair_out[0..2) with *num_cow = 0 or 1.
+  void extend(std::vector<Logical>& blocks, int n, int64_t* slots_out, int64_t* cow_pair_out, int* num_cow) {
+    int c = 0;
+    for (int i = 0; i < n; ++i) {
+      int32_t s, d;
+      const int64_t slot = append(blocks, &s, &d);
+      if (slots_out) slots_out[i] = slot;
+      if (s >= 0) {
+        if (cow_pair_out) {
+          cow_pair_out[0] = s;
+          cow_pair_out[1] = d;
+        }
+        ++c;
+      }
+    }
+    if (num_cow) *num_cow = c;
+  }
   // One append; the caller checked that a free block exists if one is needed.
   int64_t append(std::vector<Logical>& blocks, int32_t* src, int32_t* dst) {
     *src = -1;
@@ -240,19 +268,48 @@ int pkv_bm_register_prefix(pkv_bm* bm, int64_t prefix_id, int len, int64_t* slot
   return PKV_OK;
 }
 
-int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id) {
+int pkv_bm_add_seq_with_prefix(pkv_bm* bm, int64_t seq_id, int64_t prefix_id, int suffix_len, int64_t* slots_out,
+                               int64_t* cow_pair_out, int* num_cow) {
   if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq_with_prefix: null manager");
+  if (suffix_len < 0 || (suffix_len > 0 && !slots_out))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq_with_prefix: suffix_len=%d (slots_out %s)", suffix_len,
+                     slots_out ? "given" : "null");
   Manager* m = M(bm);
   auto it = m->prefixes.find(prefix_id);
   if (it == m->prefixes.end())
     return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_add_seq_with_prefix: no prefix %lld", (long long)prefix_id);
   if (m->seqs.count(seq_id))
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_add_seq_with_prefix: sequence %lld exists", (long long)seq_id);
+  // the suffix's blocks, counted as if the sequence already held its reference on every prefix
+  // block: a partly filled last prefix block is then shared, so the first suffix token copies it
   std::vector<Logical> copy = it->second;
+  int need = 0;
+  if (suffix_len > 0) {
+    const Logical& last = copy.back();
+    const int room = m->B - last.filled;
+    const int past = suffix_len - room;
+    need = (room > 0 ? 1 : 0) + (past > 0 ? (past + m->B - 1) / m->B : 0);
+  }
+  if (need > (int)m->free_list.size()) return oom(m, need);
   for (const Logical& lb : copy) m->ref[lb.phys] += 1;
   m->prefix_seqs += 1;
   m->prefix_blocks += (int64_t)copy.size();
-  m->seqs.emplace(seq_id, std::move(copy));
+  auto& blocks = m->seqs.emplace(seq_id, std::move(copy)).first->second;
+  m->extend(blocks, suffix_len, slots_out, cow_pair_out, num_cow);
+  if (suffix_len == 0 && num_cow) *num_cow = 0;
+  return PKV_OK;
+}
+
+int pkv_bm_extend(pkv_bm* bm, int64_t seq_id, int n, int64_t* slots_out, int64_t* cow_pair_out, int* num_cow) {
+  if (!bm || n < 0 || (n > 0 && !slots_out))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_bm_extend: bad argument (n=%d)", n);
+  Manager* m = M(bm);
+  auto it = m->seqs.find(seq_id);
+  if (it == m->seqs.end()) return pkv::fail(PKV_ERR_NOT_FOUND, "pkv_bm_extend: no sequence %lld", (long long)seq_id);
+  const int need = m->blocks_for_appends(it->second, n);
+  if (need > (int)m->free_list.size()) return oom(m, need);
+  m->extend(it->second, n, slots_out, cow_pair_out, num_cow);
+  if (n == 0 && num_cow) *num_cow = 0;
   return PKV_OK;
 }
 

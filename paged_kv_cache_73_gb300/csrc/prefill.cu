@@ -366,6 +366,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       if (tid == 0 && qt == 0 && h == 0) record_error(PKV_DEV_PREFIX_MISMATCH);
       return;
     }
+    // a group larger than the grid covers (the caller's max_group_size understated it): its later
+    // members would get no prefix partial, so the call is flagged
+    if (tid == 0 && qt == 0 && h == 0 && n > static_cast<int>(gridDim.x) * TC_QTILES * TC_BM)
+      record_error(PKV_DEV_PREFIX_MISMATCH);
     if (i0 >= n) return;
     if (ctx == 0 || n < pkv::kMinSharedGroup) {
       // no shared prefix, or a group too small to share it (its members read their whole context
@@ -387,6 +391,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       if (tid == 0 && qt == 0) record_error(ctx > p.max_blocks * B ? PKV_DEV_BAD_CONTEXT_LEN : PKV_DEV_BAD_QUERY_RANGE);
       return;
     }
+    // more new tokens than the grid covers (the caller's max_query_len understated them): the rows
+    // past the grid are not written, so the call is flagged
+    if (tid == 0 && qt == 0 && h == 0 && n > static_cast<int>(gridDim.x) * TC_QTILES * TC_BM)
+      record_error(PKV_DEV_BAD_QUERY_RANGE);
     if (i0 >= n) return;
   }
   const int ntile_q = i0 + TC_BM < n ? 2 : 1;                 // query tiles with real tokens

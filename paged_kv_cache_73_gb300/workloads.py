@@ -188,14 +188,20 @@ class DecodeWorkload:
         block ``ids[i]`` of the full pool, and ``tables`` point into it.  Used
         to check sampled sequences of a batch far too large for the CPU.
         """
+        return self.compact_pools_with(seqs, (), device)[:4]
+
+    def compact_pools_with(self, seqs: Sequence[int], extra_blocks: Sequence[int] = (), device="cpu"):
+        """compact_pools plus the physical blocks ``extra_blocks`` (e.g. the sources of copies into
+        the sequences' blocks); returns (k, v, tables, lens, ids), ``ids`` the sorted physical ids
+        of the compact pool's blocks."""
         seqs = list(seqs)
         tabs = self.block_tables[seqs]
         lens = self.context_lens[seqs]
-        ids = sorted({int(b) for b in tabs.ravel() if b >= 0})
+        ids = sorted({int(b) for b in tabs.ravel() if b >= 0} | {int(b) for b in extra_blocks})
         remap = {b: i for i, b in enumerate(ids)}
         k = torch.empty((len(ids), self.num_heads, self.block_size, self.head_dim), dtype=torch.float16)
         v = torch.empty_like(k)
-        fills = torch.tensor([self.block_fill[b] for b in ids], dtype=torch.int64)
+        fills = torch.tensor([self.block_fill.get(b, 0) for b in ids], dtype=torch.int64)   # unmapped: all NaN
         keep = (torch.arange(self.block_size)[None, :] < fills[:, None])[:, None, :, None]
         nan = torch.tensor(float("nan"), dtype=torch.float16)
         # generated with the full pool's flat indices, stored at the compact position
@@ -208,7 +214,7 @@ class DecodeWorkload:
             for j in range(tabs.shape[1]):
                 if tabs[r, j] >= 0:
                     new_tabs[r, j] = remap[int(tabs[r, j])]
-        return k.to(device), v.to(device), new_tabs, lens.copy()
+        return k.to(device), v.to(device), new_tabs, lens.copy(), ids
 
 
 def _blocks_for(n_tokens: int, block_size: int) -> int:
@@ -372,3 +378,57 @@ def from_tables(name: str, seed: int, num_heads: int, head_dim: int, block_size:
     w = _assemble(name, seed, num_heads, head_dim, block_size, num_blocks, rows, notes)
     w.block_tables = np.ascontiguousarray(block_tables.astype(np.int32))
     return w
+
+
+# ---- inputs for the hard regimes of the softmax ------------------------------------------------------
+#
+# These draw ordinary Gaussian numbers (numpy, seeded) at a chosen spread instead of the counter
+# stream, on the CPU, for batches small enough to build there: spreads far above 1 (logits spanning
+# tens or hundreds of units), far below the fp16 normal range (subnormal keys or values), and keys
+# laid along each query's direction with a coefficient that follows the token's position, so that
+# q.k_t moves steadily from one end of the context to the other.
+
+def _nan_outside(w: DecodeWorkload, pool: np.ndarray) -> np.ndarray:
+    """NaN in every slot of ``pool`` that no table row maps (as fill_pool does)."""
+    keep = np.zeros(pool.shape[0] * w.block_size, dtype=bool)
+    for b, f in w.block_fill.items():
+        keep[b * w.block_size: b * w.block_size + f] = True
+    flat = pool.reshape(pool.shape[0], pool.shape[1], w.block_size, -1).transpose(0, 2, 1, 3)
+    flat = flat.reshape(pool.shape[0] * w.block_size, pool.shape[1], -1)
+    flat[~keep] = np.nan
+    return flat.reshape(pool.shape[0], w.block_size, pool.shape[1], -1).transpose(0, 2, 1, 3).copy()
+
+
+def gaussian_inputs(w: DecodeWorkload, seed: int, q_std: float = 1.0, k_std: float = 1.0, v_std: float = 1.0):
+    """(q [S, H, D], k pool, v pool) as CPU fp16 tensors: independent N(0, std^2) draws rounded to
+    fp16 (tiny spreads give fp16 subnormals), NaN in the slots no table maps."""
+    rng = np.random.default_rng(seed)
+    S, H, D, B, N = w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.num_blocks
+    q = (rng.standard_normal((S, H, D)) * q_std).astype(np.float16)
+    k = _nan_outside(w, (rng.standard_normal((N, H, B, D)) * k_std).astype(np.float16))
+    v = _nan_outside(w, (rng.standard_normal((N, H, B, D)) * v_std).astype(np.float16))
+    return torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v)
+
+
+def ramp_inputs(w: DecodeWorkload, seed: int, first: float, last: float, q_norm: float = 8.0,
+                noise: float = 0.02, rows_per_seq: Optional[Sequence[int]] = None):
+    """q and K/V pools in which q[s, h] . k_t runs linearly from about ``first`` (t = 0) to about
+    ``last`` (t = ctx_s - 1): q[s, h] = q_norm * u with u a random unit vector per (s, h), and
+    k_t = c_t / q_norm * u + N(0, noise^2) per element with c_t the ramp value; v ~ N(0, 1).  All
+    fp16 on the CPU, NaN in unmapped slots.  With ``rows_per_seq``, q has that many rows per
+    sequence (prefill: every new token of a sequence shares its u), stacked in sequence order."""
+    rng = np.random.default_rng(seed)
+    S, H, D, B, N = w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.num_blocks
+    u = rng.standard_normal((S, H, D))
+    u /= np.linalg.norm(u, axis=2, keepdims=True)
+    k = rng.standard_normal((N, H, B, D)) * noise
+    for s in range(S):
+        ctx = int(w.context_lens[s])
+        for t in range(ctx):
+            c = first + (last - first) * (t / max(ctx - 1, 1))
+            k[int(w.block_tables[s, t // B]), :, t % B, :] += (c / q_norm) * u[s]
+    v = rng.standard_normal((N, H, B, D))
+    rows = [1] * S if rows_per_seq is None else [int(r) for r in rows_per_seq]
+    q = np.concatenate([np.repeat((q_norm * u[s])[None], rows[s], axis=0) for s in range(S)], axis=0)
+    return (torch.from_numpy(q.astype(np.float16)), torch.from_numpy(_nan_outside(w, k.astype(np.float16))),
+            torch.from_numpy(_nan_outside(w, v.astype(np.float16))))

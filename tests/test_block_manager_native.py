@@ -79,7 +79,7 @@ def test_random_operations_match_oracle(B, N, seed):
     live, prefixes = [], []
     nid = 0
     for step in range(1500):
-        op = int(rng.integers(0, 14))
+        op = int(rng.integers(0, 15))
         try:
             if op < 2 or not live:
                 n = int(rng.integers(1, 5 * B))
@@ -113,9 +113,17 @@ def test_random_operations_match_oracle(B, N, seed):
                 assert list(got) == want
                 prefixes.append(pid)
             elif op < 7 and prefixes:
+                # a request on a prefix, with its suffix placed in the same call (all or nothing)
                 pid = int(rng.choice(prefixes))
-                ora.add_seq_with_prefix(nid, pid)
-                nat.add_seq_with_prefix(nid, pid)
+                suffix = int(rng.integers(0, 3 * B))
+                try:
+                    want_slots, want_pairs = ora.add_seq_with_prefix(nid, pid, suffix)
+                except MemoryError:
+                    with pytest.raises(pkv.PkvOutOfBlocks):
+                        nat.add_seq_with_prefix(nid, pid, suffix)
+                    continue
+                got_slots, got_pairs = nat.add_seq_with_prefix(nid, pid, suffix)
+                assert list(got_slots) == want_slots and got_pairs.tolist() == [list(p) for p in want_pairs]
                 live.append(nid)
                 nid += 1
             elif op < 8 and prefixes:
@@ -146,6 +154,18 @@ def test_random_operations_match_oracle(B, N, seed):
                     if src >= 0:
                         want_pairs.append([src, dst])
                 assert pairs.tolist() == want_pairs
+            elif op < 11:
+                # several tokens of one sequence at once (all or nothing)
+                s = int(rng.choice(live))
+                n = int(rng.integers(0, 3 * B + 2))
+                try:
+                    want_slots, want_pairs = ora.extend(s, n)
+                except MemoryError:
+                    with pytest.raises(pkv.PkvOutOfBlocks):
+                        nat.extend(s, n)
+                    continue
+                got_slots, got_pairs = nat.extend(s, n)
+                assert list(got_slots) == want_slots and got_pairs.tolist() == [list(p) for p in want_pairs]
             else:
                 s = int(rng.choice(live))
                 try:
@@ -180,6 +200,26 @@ def test_errors_leave_state_unchanged():
     with pytest.raises(pkv.PkvError):
         pkv.BlockManager(4, 4, [0, 1, 1, 2])  # not a permutation
     assert bm.stats()[0] == 0
+
+
+def test_extend_and_prefix_suffix_all_or_nothing():
+    bm = pkv.BlockManager(6, 4, list(range(6)))
+    bm.register_prefix(1, 6)                  # blocks 0 (4 tokens), 1 (2 tokens)
+    with pytest.raises(pkv.PkvOutOfBlocks):
+        bm.add_seq_with_prefix(2, 1, 15)      # copy of block 1 + 3 new blocks > 4 free
+    assert bm.stats()[0] == 4 and bm.ref_count(0) == 1 and bm.ref_count(1) == 1
+    with pytest.raises(pkv.PkvError):
+        bm.block_table(2)                     # the failed request left no sequence behind
+    slots, pairs = bm.add_seq_with_prefix(2, 1, 10)   # copy 1 -> 2, then blocks 3 and 4
+    assert pairs.tolist() == [[1, 2]]
+    assert slots.tolist() == [2 * 4 + 2, 2 * 4 + 3] + [3 * 4 + r for r in range(4)] + [4 * 4 + r for r in range(4)]
+    assert bm.block_table(2) == ([0, 2, 3, 4], 16)
+    with pytest.raises(pkv.PkvOutOfBlocks):
+        bm.extend(2, 5)                       # 2 new blocks, 1 free
+    assert bm.block_table(2) == ([0, 2, 3, 4], 16) and bm.stats()[0] == 1
+    slots, pairs = bm.extend(2, 4)
+    assert slots.tolist() == [5 * 4 + r for r in range(4)] and pairs.shape == (0, 2)
+    assert bm.extend(2, 0)[0].shape == (0,)
 
 
 def test_batch_tables_padded():

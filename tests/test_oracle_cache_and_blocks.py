@@ -255,6 +255,61 @@ def test_shared_prefix_last_block_is_copy_on_write():
     assert bm.num_free() == 256
 
 
+def test_extend_places_the_walkthrough_decode_tokens_at_once():
+    # the single-request walk-through: after the 7-token prompt (blocks 7 and 1, fills 4 and 3),
+    # "fathers" fills logical block 1 and "brought" opens a third block; placing both tokens in
+    # one call gives the same slots and fills
+    g = _golden()["single_request"]
+    B = g["block_size"]
+    bm = obm.BlockManager(8, B, _free_order(8, g["free_order_head"]))
+    bm.add_seq(0, len(g["prompt"]))
+    slots, copies = bm.extend(0, len(g["decode"]))
+    third = g["free_order_head"][2]
+    assert slots == [g["after_prefill"]["table"][1] * B + 3, third * B + 0] and copies == []
+    assert bm.filled(0) == g["decode"][-1]["filled"]
+    assert len(bm.block_table(0)[0]) == g["decode"][-1]["num_logical_blocks"]
+
+
+@pytest.mark.parametrize("prefix_len,suffix", [(1024, 300), (1029, 300), (1029, 3), (40, 0), (7, 9)])
+def test_prefix_request_places_its_suffix(prefix_len, suffix):
+    # [guide] 04, steps 2 and 4: the request maps its first logical blocks onto the cached prefix
+    # and its prompt phase covers only its own tokens; a partly filled last prefix block is
+    # copied once, before the first own token is written into it
+    B, N = 16, 256
+    bm = obm.BlockManager(N, B)
+    pre = bm.register_prefix(0, prefix_len)
+    free0 = bm.num_free()
+    slots, copies = bm.add_seq_with_prefix(1, 0, suffix)
+    table, ctx = bm.block_table(1)
+    assert ctx == prefix_len + suffix and len(slots) == suffix == len(set(slots))
+    assert len(table) == -(-ctx // B)                       # blocks for exactly ctx tokens
+    partial = prefix_len % B != 0
+    assert len(copies) == (1 if partial and suffix > 0 else 0)
+    if copies:
+        assert copies[0] == (pre[-1] // B, table[prefix_len // B])
+    shared = prefix_len // B + (1 if partial and suffix == 0 else 0)
+    assert [b for b in table[:shared]] == [x // B for x in pre[::B]][:shared]
+    assert free0 - bm.num_free() == len(table) - shared        # blocks taken = blocks not shared
+    # each own token sits at its position: row (p mod B) of the table's block p / B
+    for i, sl in enumerate(slots):
+        p_ = prefix_len + i
+        assert sl == table[p_ // B] * B + p_ % B
+    assert bm.filled(1)[:-1] == [B] * (len(table) - 1)          # at most one partly filled block
+
+
+def test_extend_is_all_or_nothing():
+    bm = obm.BlockManager(4, 4, [0, 1, 2, 3])
+    bm.add_seq(0, 3)
+    bm.fork(0, 1)
+    with pytest.raises(MemoryError):
+        bm.extend(1, 14)                                    # copy + 3 new blocks > 3 free
+    assert bm.filled(1) == [3] and bm.ref_count(0) == 2 and bm.num_free() == 3
+    bm.register_prefix(7, 2)                                # block 1
+    with pytest.raises(MemoryError):
+        bm.add_seq_with_prefix(2, 7, 11)                    # copy + 3 new blocks > 2 free
+    assert 2 not in bm.seqs and bm.ref_count(1) == 1 and bm.prefix_seqs == 0
+
+
 def test_full_prefix_blocks_shared_without_copy():
     bm = obm.BlockManager(256, 16)
     bm.register_prefix(0, 1024)
