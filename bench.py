@@ -741,96 +741,133 @@ def run_gpu(args, rank, world, dev, cpu_refs=None):
 
 
 def run_e2e_loop(args, st, dev):
-    """A decode loop through the C ABI, timed on the host clock: each step the C++ block manager
+    """A decode loop through the C ABI, timed on the host clock.  Each step the C++ block manager
     assigns the new tokens' slots (pkv_bm_append_slots) and writes the padded tables
     (pkv_bm_block_tables) into page-locked host buffers; the kernels read those, q and the new K/V
-    rows across NVLink-C2C and write the output into page-locked host memory (with --grouped: one
-    packed host-to-device copy of the step's inputs and a copy of the output back, since that
-    entry loads q by TMA from device memory); the host waits for the output.  The contexts grow by
-    one token a step, so every step appends where the last one left off."""
+    rows across NVLink-C2C and write the output into page-locked host memory; the host waits for
+    the output.  The contexts grow by one token a step.
+
+    A step's slot assignment needs no result of the step before, so the host assigns step i+1's
+    slots and tables into the second of two buffer sets while the kernels of step i run, as a
+    serving loop would.  The direct form calls the C entry points with the buffers' addresses, as
+    a C caller does.  With --grouped the step's inputs are copied to the device in one packed copy
+    and the output back (that entry loads q by TMA from device memory), through the binding."""
+    import ctypes
     import torch
     pkv, w, x = st.pkv, st.w, st.x
     bm, seqs = x["manager"], x["seqs"]
-    S, H, D, B = w.num_seqs, w.num_heads, w.head_dim, w.block_size
+    S, H, D, B, N = w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.num_blocks
     warm = max(args.warmup, 3)
     free = int(bm.stats()[0])
     # steps the free blocks carry: each sequence opens a block at most once every B tokens (and
     # copies at most one block on its first append)
     cap = (free // max(S, 1) - 2) * B
-    n = min(args.steps, cap - warm)
+    n = min(args.steps, cap - warm - 1)
     if n < 1:
         return {"skipped": f"the pool's {free} free blocks carry no {warm} + 1 steps"}
-    max_blocks = w.max_blocks_per_seq + -(-(warm + n + 1) // B) + 1
-    ws = pkv.workspace_for(S, H, D, max_blocks, B, dev)
-    if st.grouped is not None:
-        n_ws = pkv.paged_attention_shared_prefix_workspace_size(S, H, D, max_blocks, B)
-        ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device=dev)
-    pin = lambda t: t.cpu().contiguous().pin_memory()                        # noqa: E731
-    q_h, key_h, value_h = pin(st.q), pin(st.key), pin(st.value)
-    slots_h = torch.zeros(S, dtype=torch.int64).pin_memory()
-    pairs_h = torch.zeros((max(S, 1), 2), dtype=torch.int64).pin_memory()
-    tables_h = torch.full((S, max_blocks), -1, dtype=torch.int32).pin_memory()
-    lens_h = torch.zeros(S, dtype=torch.int32).pin_memory()
-    out_h = torch.empty(tuple(st.q.shape), dtype=torch.float16).pin_memory()
-    sl_n, pr_n, tb_n, ln_n = slots_h.numpy(), pairs_h.numpy(), tables_h.numpy(), lens_h.numpy()
-    stream = st.stream
+    max_blocks = w.max_blocks_per_seq + -(-(warm + n + 2) // B) + 1
     staged = st.grouped is not None
     if staged:
-        dev_in = {n_: torch.empty_like(t, device=dev) for n_, t in
-                  (("slots", slots_h), ("pairs", pairs_h), ("tables", tables_h), ("lens", lens_h))}
-        out_d = torch.empty_like(st.q)
+        n_ws = pkv.paged_attention_shared_prefix_workspace_size(S, H, D, max_blocks, B)
+        ws = torch.empty(max(n_ws, 16), dtype=torch.uint8, device=dev)
+    else:
+        ws = pkv.workspace_for(S, H, D, max_blocks, B, dev)
+    pin = lambda t: t.cpu().contiguous().pin_memory()                        # noqa: E731
+    q_h, key_h, value_h = pin(st.q), pin(st.key), pin(st.value)
+    out_h = torch.empty(tuple(st.q.shape), dtype=torch.float16).pin_memory()
+
+    class Buf:
+        def __init__(self):
+            self.slots = torch.zeros(S, dtype=torch.int64).pin_memory()
+            self.pairs = torch.zeros((max(S, 1), 2), dtype=torch.int64).pin_memory()
+            self.tables = torch.full((S, max_blocks), -1, dtype=torch.int32).pin_memory()
+            self.lens = torch.zeros(S, dtype=torch.int32).pin_memory()
+            self.npairs = 0
+            self.tokens = 0
+
+    bufs = [Buf(), Buf()]
+    lib = pkv.load()
+    ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+    ncow = ctypes.c_int(0)
+    handle = bm._h
+    stream = st.stream
+    sh = stream.cuda_stream
+    kp = (ctypes.c_void_p * 1)(st.k.data_ptr())
+    vp = (ctypes.c_void_p * 1)(st.v.data_ptr())
+    ws_ptr = None if ws is None else ws.data_ptr()
+    ws_bytes = 0 if ws is None else ws.numel()
     host_s = [0.0]
 
-    def one_step():
-        h0 = time.perf_counter()
-        sl, pr = bm.append_slots(seqs)
-        tb, ln = bm.block_tables(seqs, max_blocks)
-        sl_n[:] = sl
-        tb_n[:] = tb
-        ln_n[:] = ln
-        npairs = int(pr.shape[0])
-        if npairs:
-            pr_n[:npairs] = pr
-        host_s[0] += time.perf_counter() - h0
-        if not staged:
-            if npairs:
-                pkv.copy_blocks([st.k], [st.v], pairs_h[:npairs], stream=stream)
-            if st.fused:
-                pkv.paged_attention_decode_append(q_h, key_h, value_h, slots_h, st.k, st.v, tables_h, lens_h,
-                                                  w.scale, B, out=out_h, workspace=ws, stream=stream)
-            else:
-                pkv.reshape_and_cache(key_h, value_h, st.k, st.v, slots_h, stream=stream)
-                pkv.paged_attention_decode(q_h, st.k, st.v, tables_h, lens_h, w.scale, B, out=out_h, workspace=ws,
-                                           stream=stream)
-        else:
-            for n_, t in (("slots", slots_h), ("tables", tables_h), ("lens", lens_h)):
-                dev_in[n_].copy_(t, non_blocking=True)
-            if npairs:
-                dev_in["pairs"][:npairs].copy_(pairs_h[:npairs], non_blocking=True)
-                pkv.copy_blocks([st.k], [st.v], dev_in["pairs"][:npairs], stream=stream)
-            pkv.reshape_and_cache(st.key, st.value, st.k, st.v, dev_in["slots"], stream=stream)
-            g = st.grouped
-            pkv.paged_attention_decode_shared_prefix(st.q, st.k, st.v, dev_in["tables"], dev_in["lens"], g["gs"],
-                                                     g["pl"], w.scale, B, g["max_group"], out=out_d, workspace=ws,
-                                                     stream=stream)
-            out_h.copy_(out_d, non_blocking=True)
-        stream.synchronize()
-        return int(ln.astype(np.int64).sum()), npairs
+    def check(rc):
+        if rc != 0:
+            raise pkv.PkvError(rc, lib.pkv_last_error().decode(errors="replace"))
 
-    for _ in range(warm):
-        one_step()
+    def prep(b):
+        """The host's part of a step: slots, copies, tables and lengths into buffer set b."""
+        h0 = time.perf_counter()
+        check(lib.pkv_bm_append_slots(handle, ids.ctypes.data, S, b.slots.data_ptr(), b.pairs.data_ptr(),
+                                      ctypes.byref(ncow)))
+        b.npairs = ncow.value
+        check(lib.pkv_bm_block_tables(handle, ids.ctypes.data, S, b.tables.data_ptr(), max_blocks, b.lens.data_ptr()))
+        b.tokens = int(b.lens.numpy().sum(dtype=np.int64))
+        host_s[0] += time.perf_counter() - h0
+
+    if staged:
+        dev_in = {n_: torch.empty_like(t, device=dev) for n_, t in
+                  (("slots", bufs[0].slots), ("pairs", bufs[0].pairs), ("tables", bufs[0].tables),
+                   ("lens", bufs[0].lens))}
+        out_d = torch.empty_like(st.q)
+
+    def launch(b):
+        """The device part of a step, enqueued on the stream."""
+        if not staged:
+            if b.npairs:
+                check(lib.pkv_copy_blocks(kp, vp, 1, b.pairs.data_ptr(), b.npairs, H, D, B, N, sh))
+            if st.fused:
+                check(lib.pkv_paged_attention_decode_append(
+                    q_h.data_ptr(), key_h.data_ptr(), value_h.data_ptr(), b.slots.data_ptr(), st.k.data_ptr(),
+                    st.v.data_ptr(), b.tables.data_ptr(), b.lens.data_ptr(), S, H, D, N, max_blocks, w.scale, B,
+                    out_h.data_ptr(), ws_ptr, ws_bytes, sh))
+            else:
+                check(lib.pkv_reshape_and_cache(key_h.data_ptr(), value_h.data_ptr(), st.k.data_ptr(),
+                                                st.v.data_ptr(), b.slots.data_ptr(), S, H, D, B, N, sh))
+                check(lib.pkv_paged_attention_decode(
+                    q_h.data_ptr(), st.k.data_ptr(), st.v.data_ptr(), b.tables.data_ptr(), b.lens.data_ptr(), S, H,
+                    D, N, max_blocks, w.scale, B, out_h.data_ptr(), ws_ptr, ws_bytes, sh))
+            return
+        for n_ in ("slots", "tables", "lens"):
+            dev_in[n_].copy_(getattr(b, n_), non_blocking=True)
+        if b.npairs:
+            dev_in["pairs"][:b.npairs].copy_(b.pairs[:b.npairs], non_blocking=True)
+            pkv.copy_blocks([st.k], [st.v], dev_in["pairs"][:b.npairs], stream=stream)
+        pkv.reshape_and_cache(st.key, st.value, st.k, st.v, dev_in["slots"], stream=stream)
+        g = st.grouped
+        pkv.paged_attention_decode_shared_prefix(st.q, st.k, st.v, dev_in["tables"], dev_in["lens"], g["gs"], g["pl"],
+                                                 w.scale, B, g["max_group"], out=out_d, workspace=ws, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+
+    def loop(steps):
+        kv, copies = 0, 0
+        prep(bufs[0])
+        for i in range(steps):
+            b = bufs[i % 2]
+            launch(b)
+            if i + 1 < steps:
+                prep(bufs[(i + 1) % 2])        # the next step's slots and tables, beside the kernels
+            stream.synchronize()               # this step's output is in page-locked host memory
+            kv += b.tokens * H * D * 2 * 2
+            copies += b.npairs
+        return kv, copies
+
+    loop(warm)
     assert pkv.device_error() == 0
     host_s[0] = 0.0
-    kv = 0
-    copies = 0
     t0 = time.perf_counter()
-    for _ in range(n):
-        tokens, npairs = one_step()
-        kv += tokens * H * D * 2 * 2
-        copies += npairs
+    kv, copies = loop(n)
     secs = time.perf_counter() - t0
     assert pkv.device_error() == 0
-    step_in = q_h.nbytes + key_h.nbytes + value_h.nbytes + slots_h.nbytes + tables_h.nbytes + lens_h.nbytes
+    b = bufs[0]
+    step_in = (q_h.nbytes + key_h.nbytes + value_h.nbytes + b.slots.nbytes + b.tables.nbytes + b.lens.nbytes)
     return {"steps": n, "seconds": secs, "kv_bytes": kv, "ms_per_step": secs / n * 1e3,
             "host_a1_us_per_step": host_s[0] / n * 1e6, "copies": copies,
             "h2d_bytes_per_step": step_in + 16 * copies // max(n, 1), "d2h_bytes_per_step": out_h.nbytes,
@@ -1507,13 +1544,14 @@ def headline_line(args, r, world, cpu, red):
                "h2d_bytes_per_step": loop["h2d_bytes_per_step"], "d2h_bytes_per_step": loop["d2h_bytes_per_step"],
                "ms_per_step": loop["ms_per_step"], "steps": loop["steps"],
                "host_a1_us_per_step": loop["host_a1_us_per_step"], "copies": loop["copies"],
-               "launch": ("eager API calls; every step pkv_bm_append_slots + pkv_bm_block_tables write the step's "
-                          "slots, tables and lengths into page-locked host memory, the kernels read them (and q and "
-                          "the new K/V rows) across NVLink-C2C and write the output there, the host waits; contexts "
-                          "grow by one token a step") if not loop["staged"]
-               else ("eager API calls; every step pkv_bm_append_slots + pkv_bm_block_tables, one copy of the "
-                     "step's inputs to the device and of the output back, the host waits; contexts grow by one "
-                     "token a step")}
+               "launch": ("C-ABI calls every step: pkv_bm_append_slots + pkv_bm_block_tables write the step's slots, "
+                          "tables and lengths into page-locked host memory (the next step's into a second buffer "
+                          "set while this step's kernels run), the kernels read them and q and the new K/V rows "
+                          "across NVLink-C2C and write the output there, the host waits for it; contexts grow by "
+                          "one token a step") if not loop["staged"]
+               else ("every step pkv_bm_append_slots + pkv_bm_block_tables (the next step's beside this step's "
+                     "kernels), one copy of the step's inputs to the device and of the output back, the host "
+                     "waits; contexts grow by one token a step")}
         if rep:
             e2e["graph_replay"] = {"value": red["kv_total"] / (red["e2e_replay_ms"] * 1e-3) / 1e9,
                                    "ms_per_step": rep["ms_per_step"], "launch": rep["launch"],

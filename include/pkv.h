@@ -119,9 +119,18 @@ int pkv_device_error(void* stream, int reset, int* code);
  *   workspace    device scratch for the split over the context (partial
  *                max / sum / output per partition); at least
  *                pkv_paged_attention_workspace_size(...) bytes, 16-byte aligned.
- *                May be NULL when that size is 0.  Contents need no
- *                initialisation and are garbage afterwards.  Calls that share a
- *                workspace must be ordered on one stream.
+ *                May be NULL when pkv_paged_attention_plan reports one kernel
+ *                for these sizes (one partition per sequence, or partitions
+ *                merged on chip).  Contents need no initialisation and are
+ *                garbage afterwards.  Calls that share a workspace must be
+ *                ordered on one stream.
+ *
+ * The context is split into partitions (one CTA each).  When a sequence has at
+ * most 8 and the whole grid fits in one wave of resident CTAs, the partitions
+ * of each (sequence, head) run as one thread-block cluster and the first
+ * merges the others' partial results, which they store into its shared memory;
+ * otherwise the partial results go to the workspace and a second kernel
+ * merges them.
  *
  * Returns PKV_ERR_WORKSPACE if the workspace is needed and missing or small.
  * ------------------------------------------------------------------------- */
@@ -130,9 +139,11 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_heads, int head_
 
 /* The launch plan pkv_paged_attention_decode uses on the current device for
  * these sizes: *part_tokens receives the context partition length (tokens per
- * CTA) and *num_kernels the kernels one call launches (1, or 2 when a
- * sequence may span several partitions and a merge pass follows).  Host only;
- * queries the device's SM count once. */
+ * CTA) and *num_kernels the kernels one call launches: 1 when a sequence spans
+ * one partition or its partitions merge inside a thread-block cluster, 2 when
+ * a merge kernel follows (only then is the workspace used).
+ * Host only; queries the device's SM count once.  Context capacities above
+ * 2^30 tokens are PKV_ERR_UNSUPPORTED. */
 int pkv_paged_attention_plan(int num_seqs, int num_heads, int head_dim, int max_blocks_per_seq,
                              int block_size, int* part_tokens, int* num_kernels);
 

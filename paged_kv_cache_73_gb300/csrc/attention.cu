@@ -94,6 +94,49 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   }
   return false;
 }
+// ---- thread-block cluster helpers (the partitions of one (sequence, head) as one cluster) -------
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// The shared::cluster address of this CTA's shared-memory location `addr` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// One arrival on an mbarrier in another CTA of the cluster, releasing this thread's earlier
+// shared::cluster stores to whoever acquires the barrier's phase.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (deadline `ns`) for a phase completed by other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, unsigned long long ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 255u) == 255u && global_ns() - t0 > ns) return false;
+  }
+  return false;
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completion counted on `bar`.
 // K/V tiles are streamed once per (sequence, head), so they are marked first to
 // leave L2 (evict_first); a block shared by many sequences still hits in L2
@@ -126,6 +169,11 @@ struct Cfg {
   static constexpr int NST = RING_BYTES / (NW * STAGE_BYTES) < 8 ? RING_BYTES / (NW * STAGE_BYTES) : 8;
   static constexpr int MAX_PART_TOKENS = 1024;       // longest partition the host plans
   static constexpr int SPEC = (MAX_PART_TOKENS / R + NW * 32 - 1) / (NW * 32);  // table reads per thread
+  static constexpr int CLUSTER_MAX = 8;              // partitions merged inside one cluster, at most
+  // mbarriers: one per ring stage, plus (cluster merge) the receiving barrier and one slot of
+  // padding, so that the 16-byte row stage after them stays 16-byte aligned
+  static constexpr int BARS = NW * NST;
+  static constexpr int BARS_CLUSTER = NW * NST + 2;
   static_assert(NJ >= 1 && NJ <= CPR, "row split");
   static_assert(NST >= 1, "stages");
 };
@@ -258,18 +306,26 @@ __device__ __forceinline__ void chunk_update(const unsigned char* ks, const unsi
 
 // APPEND: the fused new-token write of pkv_paged_attention_decode_append.  A compile-time switch:
 // the plain decode kernel carries none of its registers or branches.
-template <int D, int R, bool APPEND>
+// CLUSTER: the partitions of one (sequence, head) form one thread-block cluster (the grid's x
+// extent, max_parts <= CLUSTER_MAX, is the cluster's), and partition 0 merges the others' partial
+// results, which they store into its shared memory: no workspace and no merge kernel.
+constexpr unsigned long long RECV_WAIT_NS = 10000000000ull;  // 10 s: longer than any partition's bounded waits
+
+template <int D, int R, bool APPEND, bool CLUSTER>
 __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partition_kernel(const AttnParams p) {
   using C = Cfg<D, R>;
   constexpr int NW = C::NW, NST = C::NST;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;                                                   // [NW][NST][K|V]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NST * C::STAGE_BYTES);  // [NW][NST]
-  float* comb = reinterpret_cast<float*>(bars + NW * NST);                      // [NW][D + 2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NW * NST * C::STAGE_BYTES);  // [NW][NST] (+ receive)
+  float* comb = reinterpret_cast<float*>(bars + (CLUSTER ? C::BARS_CLUSTER : C::BARS));  // [NW][D + 2]
   // append only: the new K/V row of head h, handed from the warp that loads it to the one that
   // patches the staged chunk ([2 * D / 8] 16-byte vectors)
   uint4* row_stage = reinterpret_cast<uint4*>(comb + NW * (D + 2));
-  int64_t* chunk_off = reinterpret_cast<int64_t*>(row_stage + (APPEND ? 2 * C::CPR : 0));  // [chunks per part]
+  // cluster only: partition 0 receives partition q's (o[D], m, l) in recv[q]
+  float* recv = reinterpret_cast<float*>(row_stage + (APPEND ? 2 * C::CPR : 0));
+  int64_t* chunk_off = reinterpret_cast<int64_t*>(recv + (CLUSTER ? C::CLUSTER_MAX * (D + 2) : 0));  // [chunks per part]
+  const uint32_t recv_bar = smem_u32(&bars[NW * NST]);
 
   const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -315,7 +371,22 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const bool bad_range = start < 0 || start % B != 0 || ctx_full <= start || ctx_full > max_ctx;
   const int ctx = ctx_full - start;                    // tokens of the range
   const int nparts = bad_range ? 1 : (ctx + p.part_tokens - 1) / p.part_tokens;
-  if (part >= nparts) return;
+  if constexpr (CLUSTER) {
+    // Partition 0 counts one arrival per thread of every other partition with tokens; the cluster
+    // barrier makes that initialisation visible before any of them arrives.  Every thread of every
+    // CTA arrives here and waits once before it exits or reaches another CTA's shared memory.
+    if (part == 0 && tid == 0 && nparts > 1) {
+      mbar_init(recv_bar, NW * 32 * (nparts - 1));
+      fence_mbar_init();
+    }
+    cluster_arrive_release();
+    if (part >= nparts) {
+      cluster_wait_acquire();
+      return;
+    }
+  } else {
+    if (part >= nparts) return;
+  }
   const bool appends = APPEND && part == nparts - 1;
   const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * B;
   const bool slot_ok = appends && slot >= 0 && slot < num_slots;
@@ -345,6 +416,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
         p.ws_ml[2 * w + 1] = 0.f;
       }
     }
+    if constexpr (CLUSTER) cluster_wait_acquire();
     return;
   }
 
@@ -405,17 +477,20 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   }
   if (bad) {
     if (tid == 0) record_error(PKV_DEV_BAD_BLOCK_ID);
-    if (nparts == 1 && p.part_base == 0) {
-      for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
-    } else {
-      const size_t w = (static_cast<size_t>(s) * H + h) * p.max_parts + p.part_base + part;
-      for (int d = tid; d < D; d += NW * 32) p.ws_o[w * D + d] = 0.f;
-      if (tid == 0) {
-        p.ws_ml[2 * w] = -INFINITY;
-        p.ws_ml[2 * w + 1] = 0.f;
+    if constexpr (!CLUSTER) {
+      if (nparts == 1 && p.part_base == 0) {
+        for (int d = tid; d < D; d += NW * 32) p.out[out_off + d] = __float2half_rn(0.f);
+      } else {
+        const size_t w = (static_cast<size_t>(s) * H + h) * p.max_parts + p.part_base + part;
+        for (int d = tid; d < D; d += NW * 32) p.ws_o[w * D + d] = 0.f;
+        if (tid == 0) {
+          p.ws_ml[2 * w] = -INFINITY;
+          p.ws_ml[2 * w + 1] = 0.f;
+        }
       }
+      return;
     }
-    return;
+    // in a cluster the partition still takes part in the merge, with an empty partial result
   }
 
   // q slice of this lane, scaled into the base-2 log domain.
@@ -432,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   }
 
   // Warp `warp` takes local chunks warp, warp + NW, ...
-  const int my_n = n_chunks > warp ? (n_chunks - warp + NW - 1) / NW : 0;
+  const int my_n = (!bad && n_chunks > warp) ? (n_chunks - warp + NW - 1) / NW : 0;
   unsigned char* wring = ring + warp * NST * C::STAGE_BYTES;
   const uint32_t wbar = smem_u32(&bars[warp * NST]);
   const unsigned char* kbase = reinterpret_cast<const unsigned char*>(p.k);
@@ -519,6 +594,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   }
   __syncthreads();
 
+  // this CTA's (M, L); a warp without tokens (m = -inf) weighs nothing
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < NW; ++w) M = fmaxf(M, comb[w * (D + 2) + D]);
@@ -526,7 +602,8 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   float wgt[NW];
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
-    wgt[w] = exp2f(comb[w * (D + 2) + D] - M);
+    const float mw = comb[w * (D + 2) + D];
+    wgt[w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
     L = fmaf(comb[w * (D + 2) + D + 1], wgt[w], L);
   }
   if (nparts == 1 && p.part_base == 0) {
@@ -537,7 +614,8 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
       for (int w = 0; w < NW; ++w) o = fmaf(comb[w * (D + 2) + d], wgt[w], o);
       p.out[out_off + d] = __float2half_rn(o * inv);
     }
-  } else {
+    if constexpr (CLUSTER) cluster_wait_acquire();
+  } else if constexpr (!CLUSTER) {
     const size_t w0 = (static_cast<size_t>(s) * H + h) * p.max_parts + p.part_base + part;
     for (int d = tid; d < D; d += NW * 32) {
       float o = 0.f;
@@ -548,6 +626,47 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     if (tid == 0) {
       p.ws_ml[2 * w0] = M;
       p.ws_ml[2 * w0 + 1] = L;
+    }
+  } else {
+    // the merge inside the cluster: m = max m_q, l = sum l_q 2^(m_q - m), o = sum o_q 2^(m_q - m) / l
+    cluster_wait_acquire();                            // partition 0's receiving barrier is set up
+    if (part != 0) {
+      const uint32_t dst = map_to_rank(smem_u32(recv + part * (D + 2)), 0);
+      for (int d = tid; d < D; d += NW * 32) {
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) o = fmaf(comb[w * (D + 2) + d], wgt[w], o);
+        st_cluster_f32(dst + 4u * d, o);
+      }
+      if (tid == 0) {
+        st_cluster_f32(dst + 4u * D, M);
+        st_cluster_f32(dst + 4u * (D + 1), L);
+      }
+      mbar_arrive_remote(map_to_rank(recv_bar, 0));    // every thread, after its own stores
+      return;
+    }
+    // partition 0 stays until every other partition's threads have arrived: none of them may
+    // store into its shared memory after it has exited
+    if (!mbar_wait_cluster_bounded(recv_bar, 0, RECV_WAIT_NS) && tid == 0) record_error(PKV_DEV_WAIT_TIMEOUT);
+    float Mx = M;
+    for (int q = 1; q < nparts; ++q) Mx = fmaxf(Mx, recv[q * (D + 2) + D]);
+    const float w_own = M == -INFINITY ? 0.f : exp2f(M - Mx);
+    float Lx = L * w_own;
+    for (int q = 1; q < nparts; ++q) {
+      const float mq = recv[q * (D + 2) + D];
+      Lx = fmaf(recv[q * (D + 2) + D + 1], mq == -INFINITY ? 0.f : exp2f(mq - Mx), Lx);
+    }
+    const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+    for (int d = tid; d < D; d += NW * 32) {
+      float o = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) o = fmaf(comb[w * (D + 2) + d], wgt[w], o);
+      o *= w_own;
+      for (int q = 1; q < nparts; ++q) {
+        const float mq = recv[q * (D + 2) + D];
+        o = fmaf(recv[q * (D + 2) + d], mq == -INFINITY ? 0.f : exp2f(mq - Mx), o);
+      }
+      p.out[out_off + d] = __float2half_rn(o * inv);
     }
   }
 }
@@ -646,10 +765,12 @@ constexpr int kMaxPartTokens = 1024;
 static_assert(kMaxPartTokens == Cfg<128, 16>::MAX_PART_TOKENS, "the kernel's table pass covers the longest partition");
 
 template <int D, int R>
-constexpr size_t smem_bytes(int part_tokens, bool append) {
+constexpr size_t smem_bytes(int part_tokens, bool append, bool cluster) {
   using C = Cfg<D, R>;
-  return static_cast<size_t>(C::NW) * C::NST * C::STAGE_BYTES + C::NW * C::NST * 8 +
+  return static_cast<size_t>(C::NW) * C::NST * C::STAGE_BYTES +
+         (cluster ? C::BARS_CLUSTER : C::BARS) * 8 +
          C::NW * (D + 2) * sizeof(float) + (append ? 2 * C::CPR * 16 : 0) +
+         (cluster ? C::CLUSTER_MAX * (D + 2) * sizeof(float) : 0) +
          static_cast<size_t>(part_tokens / R) * sizeof(int64_t);
 }
 
@@ -666,19 +787,23 @@ int device_sms(int dev) {
   return cache[dev];
 }
 
+template <int D, int R, bool APPEND, bool CLUSTER>
+cudaError_t set_smem(int part_tokens) {
+  return cudaFuncSetAttribute(paged_attention_partition_kernel<D, R, APPEND, CLUSTER>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem_bytes<D, R>(part_tokens, APPEND, CLUSTER)));
+}
+
 template <int D, int R>
 cudaError_t prepare_kernel(int dev) {
   static std::mutex mu;
   static bool done[64] = {false};
   std::lock_guard<std::mutex> g(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_bytes<D, R>(kMaxPartTokens, false)));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(paged_attention_partition_kernel<D, R, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<D, R>(kMaxPartTokens, true)));
+  cudaError_t e = set_smem<D, R, false, false>(kMaxPartTokens);
+  if (e == cudaSuccess) e = set_smem<D, R, true, false>(kMaxPartTokens);
+  if (e == cudaSuccess) e = set_smem<D, R, false, true>(kMaxPartTokens);
+  if (e == cudaSuccess) e = set_smem<D, R, true, true>(kMaxPartTokens);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -696,6 +821,19 @@ int choose_part_tokens(int num_seqs, int num_heads, int max_ctx, int sms) {
   return kMinPartTokens;
 }
 
+// Whether a plain decode call merges its partitions inside thread-block clusters (one cluster per
+// (sequence, head), partition 0 merging) rather than through the workspace and a merge kernel:
+// when every (sequence, head) has at most CLUSTER_MAX partitions and the grid fits in one wave of
+// resident CTAs (kResidentPerSm per SM).  There the merge kernel's launch and its dependency on the
+// whole grid are a visible share of the call (one 2048-token sequence: 18.5 against 19.8 us);
+// on grids of many waves the clusters' co-scheduling costs more than the merge kernel (the
+// 64-sequence batch took 213 us against 194, 256 shared-prefix requests 818 against 535).
+constexpr int kResidentPerSm = 3;                 // CTAs of the partition kernel per SM (launch bounds)
+bool cluster_merge(int num_seqs, int num_heads, int max_parts, int sms) {
+  const long long ctas = static_cast<long long>(num_seqs) * num_heads * max_parts;
+  return max_parts > 1 && max_parts <= Cfg<128, 16>::CLUSTER_MAX && ctas <= static_cast<long long>(kResidentPerSm) * sms;
+}
+
 // join: if not null, the merge waits for this event (the shared-prefix product on a side stream).
 template <int D, int R>
 int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* ws, cudaStream_t st,
@@ -709,7 +847,8 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
   const int max_ctx = p.max_blocks * p.block_size;
   p.part_tokens = part_tokens;
   p.max_parts = (max_ctx + part_tokens - 1) / part_tokens + p.part_base;
-  if (p.max_parts > 1) {
+  const bool cluster = p.part_base == 0 && cluster_merge(num_seqs, p.num_heads, p.max_parts, device_sms(dev));
+  if (p.max_parts > 1 && !cluster) {
     const size_t pairs = static_cast<size_t>(num_seqs) * p.num_heads * p.max_parts;
     const size_t need = (ws_ml_floats(pairs) + pairs * D) * sizeof(float);
     if (ws == nullptr || ws_bytes < need)
@@ -719,15 +858,20 @@ int launch(AttnParams p, int num_seqs, int part_tokens, size_t ws_bytes, void* w
     p.ws_o = p.ws_ml + ws_ml_floats(pairs);
   }
   dim3 grid(p.max_parts, p.num_heads, num_seqs);
-  if (p.new_slot != nullptr)
-    e = pkv::launch_pdl(paged_attention_partition_kernel<D, R, true>, grid, dim3(Cfg<D, R>::NW * 32),
-                        smem_bytes<D, R>(part_tokens, true), st, p);
+  const dim3 block(Cfg<D, R>::NW * 32);
+  const bool append = p.new_slot != nullptr;
+  const size_t smem = smem_bytes<D, R>(part_tokens, append, cluster);
+  if (cluster)
+    e = append ? pkv::launch_pdl_cluster(paged_attention_partition_kernel<D, R, true, true>, grid, block, smem, st,
+                                         p.max_parts, p)
+               : pkv::launch_pdl_cluster(paged_attention_partition_kernel<D, R, false, true>, grid, block, smem, st,
+                                         p.max_parts, p);
   else
-    e = pkv::launch_pdl(paged_attention_partition_kernel<D, R, false>, grid, dim3(Cfg<D, R>::NW * 32),
-                        smem_bytes<D, R>(part_tokens, false), st, p);
+    e = append ? pkv::launch_pdl(paged_attention_partition_kernel<D, R, true, false>, grid, block, smem, st, p)
+               : pkv::launch_pdl(paged_attention_partition_kernel<D, R, false, false>, grid, block, smem, st, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention launch: %s", cudaGetErrorString(e));
-  if (p.max_parts > 1) {
+  if (p.max_parts > 1 && !cluster) {
     if (join != nullptr) {
       e = cudaStreamWaitEvent(st, join, 0);
       if (e != cudaSuccess) return pkv::fail(PKV_ERR_CUDA, "paged attention join: %s", cudaGetErrorString(e));
@@ -880,8 +1024,9 @@ int pkv_paged_attention_plan(int num_seqs, int num_heads, int head_dim, int max_
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
   const int max_ctx = max_blocks_per_seq * block_size;
   const int pt = choose_part_tokens(num_seqs, num_heads, max_ctx, device_sms(dev));
+  const int max_parts = (max_ctx + pt - 1) / pt;
   *part_tokens = pt;
-  *num_kernels = num_seqs == 0 ? 0 : ((max_ctx + pt - 1) / pt > 1 ? 2 : 1);
+  *num_kernels = num_seqs == 0 ? 0 : (max_parts > 1 && !cluster_merge(num_seqs, num_heads, max_parts, device_sms(dev)) ? 2 : 1);
   pkv::clear_error();
   return PKV_OK;
 }
@@ -1123,7 +1268,8 @@ int pkv_paged_attention_decode_static_workspace(const uint16_t* q, const uint16_
   const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
   const long long parts = (max_ctx + part_tokens - 1) / part_tokens;
   const size_t pairs = static_cast<size_t>(num_seqs) * num_heads * parts;
-  const unsigned long long need = parts > 1 ? (ws_ml_floats(pairs) + pairs * head_dim) * sizeof(float) : 0;
+  // the plan's scratch: none for one partition, or when the partitions merge inside clusters
+  const unsigned long long need = kernels == 2 ? (ws_ml_floats(pairs) + pairs * head_dim) * sizeof(float) : 0;
   if (need > kStaticWorkspaceBytes)
     return pkv::fail(PKV_ERR_WORKSPACE,
                      "pkv_paged_attention_decode_static_workspace: this batch needs %llu bytes of scratch, above "

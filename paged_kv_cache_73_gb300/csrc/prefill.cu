@@ -275,11 +275,13 @@ __device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, f
       : "f"(x0), "f"(x1), "f"(s), "f"(c));
 }
 // (a0, a1) += (x0, x1)
-__device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+// a0 += the low fp16 of `packed`, a1 += the high one (mixed-precision adds: the sum is taken over
+// exactly the rounded values that go to the tensor cores)
+__device__ __forceinline__ void add_half2(float& a0, float& a1, uint32_t packed) {
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
       : "+f"(a0), "+f"(a1)
-      : "f"(x0), "f"(x1));
+      : "r"(packed));
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
@@ -661,17 +663,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
           tmem_st32(to + lane_off + c * 32, ob);
         }
       }
-      // P = 2^(scale*S - m) as fp16: one paired FMA per two scores, one ex2 per score, the row
-      // sum in four paired accumulators
+      // P = 2^(scale*S - m) as fp16: one paired FMA per two scores, one ex2 per score; the row
+      // sum, in eight accumulators, adds the fp16-rounded weights that multiply V, so the
+      // normalised weights sum to one (summing the unrounded values instead leaves the output off
+      // by up to 2^-11 of |v| where one key dominates)
       float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[TC_BN / 2];
 #pragma unroll
       for (int e = 0; e < TC_BN / 2; ++e) {
         float x0, x1;
         fma2(x0, x1, sv[2 * e], sv[2 * e + 1], p.scale_log2, nref);
-        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
-        add2(sum8[2 * (e & 3)], sum8[2 * (e & 3) + 1], e0, e1);
-        pk[e] = pack_half2(e0, e1);
+        pk[e] = pack_half2(fast_exp2(x0), fast_exp2(x1));
+        add_half2(sum8[2 * (e & 3)], sum8[2 * (e & 3) + 1], pk[e]);
       }
       float sum4[4];
 #pragma unroll

@@ -116,12 +116,28 @@ def test_context_beyond_table_capacity_is_recorded(cuda_device):
 
 
 def test_workspace_too_small_is_refused(cuda_device):
-    w = wl.custom(16, [600], num_heads=2, head_dim=64, block_size=16)
+    # 2000 tokens on a 2-head grid: 16 partitions of 128 tokens, more than one cluster merges, so
+    # the partial results need the workspace
+    w = wl.custom(16, [2000], num_heads=2, head_dim=64, block_size=16)
+    assert pkv.paged_attention_plan(1, 2, 64, w.max_blocks_per_seq, 16)[1] == 2
     q, k, v, tables, lens = device_inputs(w, cuda_device)
     tiny_ws = torch.empty(16, dtype=torch.uint8, device=cuda_device)
     with pytest.raises(pkv.PkvError) as e:
         pkv.paged_attention_decode(q, k, v, tables, lens, w.scale, 16, workspace=tiny_ws)
     assert e.value.status == pkv.PKV_ERR_WORKSPACE
+
+
+def test_on_chip_merge_needs_no_workspace(cuda_device):
+    # 600 tokens on a 2-head grid: 5 partitions merged inside one cluster per head; no workspace
+    w = wl.custom(17, [600, 150], num_heads=2, head_dim=64, block_size=16)
+    assert pkv.paged_attention_plan(2, 2, 64, w.max_blocks_per_seq, 16)[1] == 1
+    q, k, v, tables, lens = device_inputs(w, cuda_device)
+    out = torch.empty_like(q)
+    assert pkv.load().pkv_paged_attention_decode(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), tables.data_ptr(), lens.data_ptr(), 2, 2, 64, k.shape[0],
+        w.max_blocks_per_seq, w.scale, 16, out.data_ptr(), None, 0, None) == pkv.PKV_OK
+    assert pkv.device_error() == 0
+    assert max_err(out, oracle_on(w, [0, 1])) <= ATOL
 
 
 def test_opt13b_batch_full_size(cuda_device):

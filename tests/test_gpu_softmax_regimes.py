@@ -27,9 +27,19 @@ from tests.helpers import ATOL
 
 pytestmark = pytest.mark.gpu
 
-# contexts around partition and block edges; 4 sequences x 4 heads leave the grid small, so the
-# decode kernel splits each context into partitions of 128-256 tokens (several per sequence)
-LENS = [3001, 1, 257, 2048]
+# Two batches with contexts around partition and block edges.  Both leave the grid small, so the
+# decode kernel splits each context into short partitions: 4 x 4 heads up to 3001 tokens gives 12
+# partitions of 256 tokens (merged by the second kernel through the workspace); 4 x 8 heads up to
+# 2048 tokens gives 8 (merged inside one thread-block cluster per sequence and head).
+LAYOUTS = {"merge_kernel": ([3001, 1, 257, 2048], 4, 2), "cluster_merge": ([2048, 1, 257, 1999], 8, 1)}
+
+
+def _batch(name, seed, D, B):
+    lens, H, kernels = LAYOUTS[name]
+    w = wl.custom(seed, lens, num_heads=H, head_dim=D, block_size=B)
+    part, got = pkv.paged_attention_plan(w.num_seqs, H, D, w.max_blocks_per_seq, B)
+    assert got == kernels and -(-max(lens) // part) >= 8       # several partitions per sequence
+    return w
 
 
 def _decode(w, q, k, v, scale, dev, fused=False):
@@ -62,42 +72,44 @@ def _err(got, ref, spread=1.0):
     return float(np.max(np.abs(got - ref))) / spread
 
 
+@pytest.mark.parametrize("layout", sorted(LAYOUTS))
 @pytest.mark.parametrize("D,B", [(128, 16), (64, 8), (128, 32)])
 @pytest.mark.parametrize("scale", [1.0, 4.0])
-def test_decode_large_scale(cuda_device, D, B, scale):
-    w = wl.custom(900 + D + B, LENS, num_heads=4, head_dim=D, block_size=B)
+def test_decode_large_scale(cuda_device, layout, D, B, scale):
+    w = _batch(layout, 900 + D + B, D, B)
     q, k, v = wl.gaussian_inputs(w, 17 + B)
     assert _err(_decode(w, q, k, v, scale, cuda_device), _oracle(w, q, k, v, scale)) <= ATOL
 
 
+@pytest.mark.parametrize("layout", sorted(LAYOUTS))
 @pytest.mark.parametrize("first,last", [(-40.0, 40.0), (40.0, -40.0), (0.0, 300.0)],
                          ids=["rising", "falling", "steep_rise"])
 @pytest.mark.parametrize("fused", [False, True], ids=["decode", "fused_append"])
-def test_decode_logit_ramp_across_partitions(cuda_device, first, last, fused):
+def test_decode_logit_ramp_across_partitions(cuda_device, layout, first, last, fused):
     # q.k_t moves steadily along the context, so consecutive partitions' maxima differ by tens of
     # units (hundreds for the steep rise); the merge must rescale every partition by its own max
-    w = wl.custom(77, LENS, num_heads=4, head_dim=128, block_size=16)
+    w = _batch(layout, 77, 128, 16)
     q, k, v = wl.ramp_inputs(w, 5, first, last)
-    part, kernels = pkv.paged_attention_plan(w.num_seqs, 4, 128, w.max_blocks_per_seq, 16)
-    assert -(-3001 // part) >= 8                                     # several partitions per sequence
     got = _decode(w, q, k, v, 1.0, cuda_device, fused=fused)
     assert _err(got, _oracle(w, q, k, v, 1.0)) <= ATOL
 
 
-def test_decode_wide_values(cuda_device):
+@pytest.mark.parametrize("layout", sorted(LAYOUTS))
+def test_decode_wide_values(cuda_device, layout):
     # q and k drawn with spread 4 (logits of hundreds of units at scale 1/sqrt(D)) and v with
     # spread 30; the error is compared after dividing by v's spread
-    w = wl.custom(31, LENS, num_heads=4, head_dim=128, block_size=16)
+    w = _batch(layout, 31, 128, 16)
     q, k, v = wl.gaussian_inputs(w, 8, q_std=4.0, k_std=4.0, v_std=30.0)
     assert float(v[~torch.isnan(v)].abs().max()) > 100.0
     assert _err(_decode(w, q, k, v, w.scale, cuda_device), _oracle(w, q, k, v, w.scale), spread=30.0) <= ATOL
 
 
-def test_decode_subnormal_values(cuda_device):
+@pytest.mark.parametrize("layout", sorted(LAYOUTS))
+def test_decode_subnormal_values(cuda_device, layout):
     # keys and values in the fp16 subnormal range (below 2^-14): fp32 accumulation keeps them,
     # and the output rounds to fp16 subnormals, whose spacing is 2^-24; the bound is half that
     # spacing plus 2e-3 of the value spread
-    w = wl.custom(32, LENS, num_heads=4, head_dim=64, block_size=16)
+    w = _batch(layout, 32, 64, 16)
     q, k, v = wl.gaussian_inputs(w, 9, q_std=1.0, k_std=2.0 ** -16, v_std=2.0 ** -18)
     vv = v[~torch.isnan(v)]
     assert float(vv.abs().max()) < 2.0 ** -14 and float((vv != 0).float().mean()) > 0.9

@@ -27,7 +27,8 @@ ATOL = 2e-3
 BATCHES = {
     "opt13b_full": wl.opt13b,
     "ragged_small": lambda: wl.custom(31, [1, 7, 300, 1000, 2049, 16], 4, 64, 8),
-    # long contexts: many partitions per sequence, so the scratch holds many partial results
+    # long contexts: more partitions per sequence than one cluster merges, so the partial results
+    # go through the scratch
     "long_contexts": lambda: wl.custom(33, [12000, 9000, 300, 16000], 8, 128, 16),
 }
 
@@ -87,8 +88,9 @@ def test_static_workspace_after_another_batch(lib, cuda_device):
 
 
 def test_static_workspace_refuses_oversized_batch(lib, cuda_device):
-    S, H, D, B, max_blocks = 256, 40, 128, 16, 256            # 4096-token capacity: > 16 MiB of partials
-    part_tokens, _ = pkv.paged_attention_plan(S, H, D, max_blocks, B)
+    S, H, D, B, max_blocks = 256, 40, 128, 16, 1024           # 16384-token capacity: > 16 MiB of partials
+    part_tokens, kernels = pkv.paged_attention_plan(S, H, D, max_blocks, B)
+    assert kernels == 2                                       # too many partitions to merge on chip
     need = S * H * (-(-max_blocks * B // part_tokens)) * (D + 2) * 4
     assert need > pkv.paged_attention_static_workspace_bytes() == 16 << 20
     q = torch.zeros((S, H, D), dtype=torch.float16, device=cuda_device)
