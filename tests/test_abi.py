@@ -160,18 +160,23 @@ def test_workspace_size(lib):
     assert pkv.paged_attention_workspace_size(64, 40, 128, 128, 16) == 64 * 40 * 16 * 130 * 4
 
 
-@pytest.mark.parametrize("S,H,D,max_blocks,want", [
-    (1, 40, 128, 128, 512),      # ctx 2048: 1024-token partitions would leave SMs idle (80 CTAs)
-    (4, 40, 128, 128, 1024),     # 320 CTAs of 1024 tokens already cover every SM
-    (64, 40, 128, 128, 1024),    # the OPT-13B-shaped batch
-    (1, 2, 64, 256, 128),        # too few (sequence, head) pairs for any partition to fill the GPU
+@pytest.mark.parametrize("S,H,D,max_blocks,want,kernels", [
+    (1, 40, 128, 128, 512, 1),      # ctx 2048: 1024-token partitions would leave SMs idle (80 CTAs);
+                                    # 160 CTAs, one wave: the 4 partitions merge in a cluster
+    (4, 40, 128, 128, 1024, 1),     # 320 CTAs of 1024 tokens already cover every SM; one wave
+    (64, 40, 128, 128, 1024, 2),    # the OPT-13B-shaped batch: 5120 CTAs, a merge kernel follows
+    (1, 2, 64, 256, 128, 2),        # too few (sequence, head) pairs to fill the GPU: 32 partitions of
+                                    # 128 tokens, more than one cluster merges
+    (2, 2, 64, 40, 128, 1),         # 5 partitions, 20 CTAs: merged in clusters
+    (8, 8, 64, 8, 128, 1),          # one partition: no merge
 ])
-def test_partition_plan(lib, S, H, D, max_blocks, want):
+def test_partition_plan(lib, S, H, D, max_blocks, want, kernels):
     # the longest partition that still gives every SM a CTA (the rule holds for 148-160 SMs, and
-    # without a device the library assumes 148)
-    part, kernels = pkv.paged_attention_plan(S, H, D, max_blocks, 16)
+    # without a device the library assumes 148); the partitions merge inside thread-block clusters
+    # when a sequence has at most 8 and the grid is at most one wave of 3 CTAs per SM
+    part, got = pkv.paged_attention_plan(S, H, D, max_blocks, 16)
     assert part == want
-    assert kernels == (2 if max_blocks * 16 > part else 1)
+    assert got == kernels
 
 
 def test_cache_ops_host_validation(lib):
