@@ -4,8 +4,9 @@ One step = one decode step of the OPT-13B-shaped single-layer batch (64
 sequences, 40 heads x 128, block size 16, context lengths ~ U[128, 2048],
 physical blocks shuffled): copy_blocks of the step's copy-on-write pairs (none
 in this batch), then the 64 new tokens' K/V write and paged decode attention in
-one launch (pkv_paged_attention_decode_append; --unfused: reshape_and_cache,
-then pkv_paged_attention_decode).  The tables and slots come from the host
+one launch (pkv_paged_attention_decode_append).  Batches whose K/V is mostly
+shared blocks (served from L2) take reshape_and_cache, then
+pkv_paged_attention_decode instead (--step picks either form).  The tables and slots come from the host
 block manager.
 
 Prints ONE JSON line (rank 0):
@@ -34,7 +35,8 @@ Prints ONE JSON line (rank 0):
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                   [--workload opt13b|tiny|parallel_sampling|parallel_sampling_cow|shared_prefix|capacity
                               |beam_search|swap|layers40|prefill]
-                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F] [--grouped] [--unfused]
+                  [--capacity-seqs S] [--capacity-block B] [--pool-frac F] [--grouped]
+                  [--step auto|fused|unfused]
 
 `--workload swap`, `--workload layers40` and `--workload prefill` print their
 own lines (swap_blocks between HBM and page-locked host memory; 40-layer
@@ -79,7 +81,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention effective KV GB/s (% of HBM peak) and decode tokens/s"
 UNIT = "GB/s"
 WORKLOAD = ("opt13b_decode_step: 64 seqs, 40 heads x 128, block 16, ctx ~ U[128,2048], shuffled blocks, "
-            "+ the K/V write of 64 new tokens (in the attention launch; --unfused: reshape_and_cache first)")
+            "+ the K/V write of 64 new tokens (in the attention launch)")
 # seed of each workload's length draws and physical-block permutation: 1000 + its index
 WORKLOAD_SEEDS = {"tiny": 1001, "opt13b": 1002, "parallel_sampling": 1003, "parallel_sampling_cow": 1003,
                   "shared_prefix": 1004, "capacity": 1005, "beam_search": 1006}
@@ -119,9 +121,11 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loops (profiling runs)")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' entries (profiling runs)")
     ap.add_argument("--no-sustained", action="store_true", help="skip the roofline and sustained loops (profiling runs)")
-    ap.add_argument("--unfused", action="store_true",
-                    help="write the new tokens with a separate reshape_and_cache call before attention "
-                         "(default: pkv_paged_attention_decode_append, one launch)")
+    ap.add_argument("--step", choices=["auto", "fused", "unfused"], default="auto",
+                    help="fused: the new tokens' K/V write inside the attention launch "
+                         "(pkv_paged_attention_decode_append); unfused: reshape_and_cache, then attention; "
+                         "auto (default): fused unless shared blocks make up most of the batch's K/V")
+    ap.add_argument("--unfused", action="store_true", help="the same as --step unfused")
     ap.add_argument("--grouped", action="store_true",
                     help="read each shared prefix once per group of sequences (shared-prefix decode entry); "
                          "groups come from the block manager's shared leading blocks")
@@ -525,6 +529,22 @@ def build_beam_step(seed: int, requests: int = 16, width: int = 4, beam_steps: i
             "workload": "beam_search", "manager": bm, "seqs": seqs, "bm": block_manager_summary(bm)}
 
 
+# The fused step (the new rows' write inside the attention launch) is 1 % faster on the OPT-13B-shaped
+# batch, whose K/V streams from HBM, but 2-3.5 % slower where L2 serves shared blocks (parallel
+# sampling 140.0 against 137.7 us, 256 shared-prefix requests 531 against 513): there the
+# partitions are short and the appending CTA's extra work shows.  The host knows which case it has
+# from the block manager's sharing: distinct K/V well below the logical K/V.
+FUSED_MIN_DISTINCT = 0.75
+
+
+def use_fused(args, w) -> bool:
+    """The step form for batch w: --step fused / unfused, or by the batch's sharing (auto)."""
+    step = "unfused" if args.unfused else args.step
+    if step != "auto":
+        return step == "fused"
+    return w.physical_kv_bytes() >= FUSED_MIN_DISTINCT * w.logical_kv_bytes()
+
+
 def needs_flush(w) -> bool:
     """A step whose distinct K/V would stay in L2 between steps is preceded by an L2 flush."""
     return w.physical_kv_bytes() < 2 * L2_NOMINAL_BYTES
@@ -649,7 +669,7 @@ def run_gpu(args, rank, world, dev, cpu_refs=None):
     seed = workload_seed(args.workload) + 7919 * rank  # weak scaling: each rank its own batch
     x = build_step_inputs(seed, args.workload, args.capacity_seqs, args.capacity_block,
                           pool_blocks_for(args, dev))
-    st = Step(x, dev, fused=not args.unfused, grouped=args.grouped)
+    st = Step(x, dev, fused=use_fused(args, x["w"]), grouped=args.grouped)
     pkv, w, stream = st.pkv, st.w, st.stream
     H, D, B = w.num_heads, w.head_dim, w.block_size
 
@@ -1006,14 +1026,15 @@ def run_configs(args, dev, cpu_refs):
     out = {}
     for name, workload, cap_seqs in CONFIG_RUNS:
         x = build_step_inputs(workload_seed(workload), workload, cap_seqs or 64, 16)
-        st = Step(x, dev, fused=True)
+        st = Step(x, dev, fused=use_fused(args, x["w"]))
         pkv, w = st.pkv, st.w
         flush = needs_flush(w)
         scratch = torch.empty(2 * l2_cache_bytes(dev), dtype=torch.uint8, device=dev) if flush else None
         st()
         torch.cuda.synchronize()
         assert pkv.device_error() == 0
-        entry = {"workload": x["desc"], "num_seqs": w.num_seqs, "logical_kv_bytes": w.logical_kv_bytes(),
+        entry = {"workload": x["desc"], "num_seqs": w.num_seqs, "step": "fused" if st.fused else "unfused",
+                 "logical_kv_bytes": w.logical_kv_bytes(),
                  "physical_kv_bytes": w.physical_kv_bytes(), "l2_flushed": flush, "steps": CONFIG_STEPS}
         seqs = config_sample(w, name)
         ref = None if cpu_refs is None else cpu_refs.get(name)
@@ -1503,7 +1524,8 @@ def headline_line(args, r, world, cpu, red):
         "config": config_block(args, r["desc"], S, flushed=r["l2_flushed"]),
         "parallelism": f"replicas x{world} (each rank its own batch, no exchange)" if world > 1 else "single GPU",
         "plan": {"partition_tokens": r["part_tokens"], "kernels_per_step": r["kernels_per_step"],
-                 "cow_pairs_per_step": r["n_pairs"], "pool_blocks": r["num_blocks"]},
+                 "step": "fused" if r["fused"] else "unfused", "cow_pairs_per_step": r["n_pairs"],
+                 "pool_blocks": r["num_blocks"]},
         "hbm_frac_of_measured": value / peak,
         "hbm_frac_of_nominal": value / NOMINAL_HBM_GBS,
         "physical_kv_GBps": red["phys_total"] / (red["step_ms"] * 1e-3) / 1e9,

@@ -349,6 +349,9 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   uint4 new_row = make_uint4(0, 0, 0, 0);
   if (row_loader)
     new_row = *reinterpret_cast<const uint4*>((row_is_v ? p.new_v : p.new_k) + out_off + row_col * 8);
+  // this lane's q slice, read now beside the length and the table; it is converted only after the
+  // first bulk copies are issued, so its round trip overlaps theirs instead of delaying them
+  const uint4 q_raw = *reinterpret_cast<const uint4*>(p.q + out_off + (lane % C::CPR) * 8);
   const int max_ctx = p.max_blocks * B;
   // Without groups every range starts at 0, so this partition's table entries are known before the
   // context length: they are read now, beside it, one per chunk (an index past the table row is not
@@ -493,19 +496,6 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     // in a cluster the partition still takes part in the merge, with an empty partial result
   }
 
-  // q slice of this lane, scaled into the base-2 log domain.
-  float qf[8];
-  {
-    const uint4 raw = *reinterpret_cast<const uint4*>(p.q + out_off + (lane % C::CPR) * 8);
-    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __half22float2(h2[e]);
-      qf[2 * e] = f.x * p.scale_log2;
-      qf[2 * e + 1] = f.y * p.scale_log2;
-    }
-  }
-
   // Warp `warp` takes local chunks warp, warp + NW, ...
   const int my_n = (!bad && n_chunks > warp) ? (n_chunks - warp + NW - 1) / NW : 0;
   unsigned char* wring = ring + warp * NST * C::STAGE_BYTES;
@@ -530,6 +520,18 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     for (; issued < NST && issued < my_n; ++issued) issue(issued);
   }
   issued = __shfl_sync(FULL, issued, 0);
+
+  // q slice of this lane, scaled into the base-2 log domain.
+  float qf[8];
+  {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&q_raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h2[e]);
+      qf[2 * e] = f.x * p.scale_log2;
+      qf[2 * e + 1] = f.y * p.scale_log2;
+    }
+  }
 
   float m = -INFINITY, l_lane = 0.f;
   float acc[8];
