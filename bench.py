@@ -99,11 +99,9 @@ REF_MAX_KV_BYTES = 2.5e9                                # the oracle arm samples
 # keyed by (workload, sha256 of the attention source it was taken on); a changed kernel reports
 # null until it is captured again.
 NCU_TRAFFIC = {
-    # the headline step's fused call: partition kernel 1,373,092,500 B read + 4,835,200 B written
-    # (the appended rows included), merge kernel 1,280,000 B read (means of two launches each;
-    # captured on source 671088f0..., which differs from this key's source in the file's header
-    # comment only)
-    ("opt13b+append", "5db4ea62901c2074d5db6247fb9ca0f86ae177cb2d1f094b6e25a2b6456c7857"): 1_379_208_000,
+    # the headline step's fused call: partition kernel 1,373,098,500 B read + 4,771,328 B written
+    # (the appended rows included), merge kernel 1,281,000 B read (means of two launches each)
+    ("opt13b+append", "cf159d0c7e380c7f61ccd7dc6914a165e3792d26230437f93a341fb7063383cf"): 1_379_150_828,
 }
 
 WORKLOADS = ("opt13b", "tiny", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity",
