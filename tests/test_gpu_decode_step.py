@@ -129,6 +129,46 @@ def test_shared_prefix_decode(cuda_device):
     assert x.attend(seqs) <= ATOL
 
 
+@pytest.mark.parametrize("prefix_len", [1024, 1029])
+def test_prefix_requests_prompt_phase(cuda_device, prefix_len):
+    # [guide] 04: requests map their first blocks onto a cached prefix and run the prompt phase
+    # over their own tokens only.  Each request and all its own tokens are placed in one manager
+    # call (the copy of a partly filled last prefix block, then the tokens' slots); the tokens'
+    # K/V is written, then prefill attention gives each own token attention over the prefix and,
+    # causally, the tokens before it; then one decode step.  Pools bit-exact, attention <= 2e-3.
+    H, D, B = 4, 128, 16
+    x = TwoSides(cuda_device, 1000, H, D, B, seed=1004)
+    x.write(x.nat.register_prefix(0, prefix_len), x.ora.register_prefix(0, prefix_len))
+    rng = np.random.default_rng(prefix_len)
+    seqs = list(range(10))
+    suffix = [int(n) for n in rng.integers(1, 300, size=len(seqs))]
+    all_nat, all_ora = [], []
+    for s, n in zip(seqs, suffix):
+        slots, pairs = x.nat.add_seq_with_prefix(s, 0, n)
+        ora_slots, ora_pairs = x.ora.add_seq_with_prefix(s, 0, n)
+        assert len(ora_pairs) == (1 if prefix_len % B else 0)
+        x.copy(pairs, ora_pairs)                      # the copy runs before the request's writes
+        all_nat += list(slots)
+        all_ora += ora_slots
+    x.write(all_nat, all_ora)                         # every request's own tokens in one call
+    assert x.pools_equal()
+    # prefill: the own tokens of every request over prefix + causal own tokens
+    max_blocks = max(len(x.ora.block_table(s)[0]) for s in seqs)
+    tables, lens = x.nat.block_tables(seqs, max_blocks)
+    qs = np.concatenate([[0], np.cumsum(suffix)]).astype(np.int32)
+    q = wl.dense_tensor((int(qs[-1]), H, D), 55, wl.STREAM_Q, cuda_device)
+    out = pkv.paged_attention_prefill(q, x.k, x.v, torch.from_numpy(tables).to(cuda_device),
+                                      torch.from_numpy(lens).to(cuda_device), torch.from_numpy(qs).to(cuda_device),
+                                      D ** -0.5, B, max(suffix))
+    assert pkv.device_error() == 0
+    ref = oracle_attention.paged_prefill_attention(q.cpu().numpy().astype(np.float64), x.k_ref, x.v_ref, tables,
+                                                   lens, qs, D ** -0.5)
+    assert float(np.max(np.abs(out.cpu().numpy().astype(np.float64) - ref))) <= ATOL
+    x.append(seqs)                                    # then a decode step on top
+    assert x.pools_equal()
+    assert x.attend(seqs) <= ATOL
+
+
 @pytest.mark.parametrize("width,B", [(4, 16), (6, 8)])
 def test_beam_search_decode(cuda_device, width, B):
     # a beam step forks the survivors, retires the old beam and appends one token per candidate;
