@@ -11,9 +11,13 @@
 // bandwidth is the roofline and no tensor cores are used):
 //  * The context is split into partitions of `part_tokens` (128..1024) tokens, the longest
 //    that still gives every SM a CTA; one CTA
-//    handles one (partition, head, sequence).  A second tiny kernel merges the
-//    partitions of a (sequence, head) with the log-sum-exp identity
-//    m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p 2^(m_p - m) / l.
+//    handles one (partition, head, sequence).  The partitions of a (sequence, head)
+//    merge with the log-sum-exp identity
+//    m = max m_p, l = sum l_p 2^(m_p - m), o = sum o_p 2^(m_p - m) / l:
+//    on a grid of at most one wave with at most 8 partitions, inside one
+//    thread-block cluster (partition 0 gathers the others' partials from their
+//    stores into its shared memory); otherwise in a second, tiny kernel over a
+//    workspace.
 //  * The unit of work is a chunk of R = min(B, 16) rows of one (block, head)
 //    tile: R*D*2 contiguous bytes of K and as many of V.  Each warp owns a ring
 //    of NST shared-memory stages; lane 0 fills a stage with two 1-D bulk async
@@ -34,7 +38,9 @@
 //    fused reshape and block write, folded into the attention launch).
 //  * Every wait is bounded by a global-timer deadline; on expiry the kernel
 //    records PKV_DEV_WAIT_TIMEOUT, waits (bounded) for its own copies in
-//    flight and returns.
+//    flight and returns.  In a cluster, partition 0 waits for the others with
+//    a longer deadline than any of their own waits, and never exits before
+//    their stores into its shared memory have landed.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
