@@ -137,3 +137,14 @@ def test_reference_arm_stands_alone():
     assert "whole batch" in line["cpu_baseline"]["sample"] and "oracle's block manager" in line["cpu_baseline"]["sample"]
     assert line["config"] == bench.config_block(bench.parse(["--workload", "tiny"]), line["config"]["workload"], 3,
                                                 flushed=True)
+
+
+def test_step_form_follows_the_batch_sharing():
+    # the fused step unless shared blocks make up most of the batch's K/V (L2 then serves the
+    # partitions and the separate write launch is faster); --step overrides
+    auto = _args()
+    opt = bench.build_step_inputs(bench.workload_seed("opt13b"), "opt13b")["w"]
+    shared = bench.build_step_inputs(bench.workload_seed("shared_prefix"), "shared_prefix")["w"]
+    assert bench.use_fused(auto, opt) and not bench.use_fused(auto, shared)
+    assert bench.use_fused(_args("--step", "fused"), shared)
+    assert not bench.use_fused(_args("--step", "unfused"), opt) and not bench.use_fused(_args("--unfused"), opt)

@@ -30,6 +30,8 @@ BATCHES = {
     # long contexts: more partitions per sequence than one cluster merges, so the partial results
     # go through the scratch
     "long_contexts": lambda: wl.custom(33, [12000, 9000, 300, 16000], 8, 128, 16),
+    # one 2048-token sequence: its partitions merge inside clusters, so no scratch is needed
+    "one_sequence": lambda: wl.capacity(seed=34, num_seqs=1),
 }
 
 
