@@ -1049,7 +1049,7 @@ def run_configs(args, dev, cpu_refs):
     CONFIG_STEPS steps (L2 flushed before each step where L2 would hold the batch), the fraction of
     the measured HBM peak, and the max abs error of sampled sequences against the oracle outputs
     the CPU-baseline leg computed on the same batch (built there by the oracle's block manager;
-    the sampled table rows are compared too).  The parallel-sampling entry also times its 96
+    the sampled table rows are compared too), with that leg's oracle time on them (one core).  The parallel-sampling entry also times its 96
     copy-on-write copies as one copy_blocks call and checks them byte for byte."""
     import torch
     peak, _ = measured_hbm_peak()
@@ -1074,6 +1074,9 @@ def run_configs(args, dev, cpu_refs):
             got = st.out[seqs].double().cpu().numpy()
             entry["max_abs_err"] = float(np.max(np.abs(got - ref["out"])))
             entry["checked_seqs"] = seqs
+            entry["cpu_oracle"] = {"GB/s": ref["cpu_kv_bytes"] / max(ref["cpu_s"], 1e-9) / 1e9, "cores": 1,
+                                   "kind": "oracle",
+                                   "sample": f"the {len(seqs)} checked sequences, {ref['cpu_s'] * 1e3:.1f} ms"}
         else:
             entry["max_abs_err"] = None
         for _ in range(3):
@@ -1405,8 +1408,10 @@ def cpu_config_refs():
         x = build_step_inputs(seed, workload, cap_seqs or 64, 16, manager="oracle")
         w = x["w"]
         seqs = config_sample(w, name)
-        _, out = cpu_sample_run(prepare_cpu_sample(w, seqs, x["slots"], x["pairs"], seed))
-        refs[name] = {"seqs": seqs, "out": out, "tables": w.block_tables[seqs].copy()}
+        sample = prepare_cpu_sample(w, seqs, x["slots"], x["pairs"], seed)
+        secs, out = cpu_sample_run(sample)
+        refs[name] = {"seqs": seqs, "out": out, "tables": w.block_tables[seqs].copy(), "cpu_s": secs,
+                      "cpu_kv_bytes": sample["kv_bytes"]}
     return refs
 
 
