@@ -298,6 +298,23 @@ int pkv_paged_attention_decode_static_workspace(const uint16_t* q, const uint16_
                                                 float scale, int block_size, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * For failure-detection tests only (not a computation of the paper): runs
+ * pkv_paged_attention_decode on sizes whose partitions merge inside
+ * thread-block clusters, but with every partition other than the first
+ * skipping its stores into partition 0's shared memory and its arrivals on
+ * partition 0's barrier, and partition 0's wait for them limited to wait_ms
+ * (1..2000).  Nothing then completes that wait: partition 0 gives up after
+ * wait_ms, records PKV_DEV_WAIT_TIMEOUT (read with pkv_device_error) and writes
+ * an undefined output; no CTA touches another's memory and the context stays
+ * usable.  PKV_ERR_UNSUPPORTED for sizes that would not merge on chip.  No
+ * workspace.
+ * ------------------------------------------------------------------------- */
+int pkv_test_cluster_merge_timeout(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                   int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq, float scale,
+                                   int block_size, uint16_t* out, int wait_ms, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Reshape and cache ([note] 关键设计 5, "fused reshape and block write").
  *
  * For every token t < num_tokens with slot = slot_mapping[t] >= 0:

@@ -63,6 +63,7 @@ _SIGNATURES = {
                                                          _P, _P]),
     "pkv_paged_attention_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _c.c_float, _I, _P,
                                          _P]),
+    "pkv_test_cluster_merge_timeout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _c.c_float, _I, _P, _I, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_reshape_and_cache_layers": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),

@@ -212,6 +212,11 @@ struct AttnParams {
   const __half* new_k;
   const __half* new_v;
   const int64_t* new_slot;
+  // cluster merge: how long partition 0 waits for the others (RECV_WAIT_NS), and, for the
+  // failure-detection test entry only, whether the other partitions skip their stores and arrivals
+  // (so that the wait runs out on a phase nothing completes)
+  unsigned long long recv_wait_ns;
+  int test_skip_merge;
 };
 
 // First token of sequence s's own range: 0 for plain decode, else its group's shared-prefix
@@ -638,6 +643,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   } else {
     // the merge inside the cluster: m = max m_q, l = sum l_q 2^(m_q - m), o = sum o_q 2^(m_q - m) / l
     cluster_wait_acquire();                            // partition 0's receiving barrier is set up
+    if (part != 0 && p.test_skip_merge) return;        // failure-detection test: nothing arrives
     if (part != 0) {
       const uint32_t dst = map_to_rank(smem_u32(recv + part * (D + 2)), 0);
       for (int d = tid; d < D; d += NW * 32) {
@@ -655,7 +661,7 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
     }
     // partition 0 stays until every other partition's threads have arrived: none of them may
     // store into its shared memory after it has exited
-    if (!mbar_wait_cluster_bounded(recv_bar, 0, RECV_WAIT_NS) && tid == 0) record_error(PKV_DEV_WAIT_TIMEOUT);
+    if (!mbar_wait_cluster_bounded(recv_bar, 0, p.recv_wait_ns) && tid == 0) record_error(PKV_DEV_WAIT_TIMEOUT);
     float Mx = M;
     for (int q = 1; q < nparts; ++q) Mx = fmaxf(Mx, recv[q * (D + 2) + D]);
     const float w_own = M == -INFINITY ? 0.f : exp2f(M - Mx);
@@ -930,7 +936,8 @@ int decode_entry(const char* fn, const uint16_t* q, const uint16_t* k_cache, con
                  const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
                  int head_dim, int num_blocks, int max_blocks_per_seq, float scale, int block_size, uint16_t* out,
                  void* workspace, size_t workspace_bytes, void* stream, const uint16_t* new_k,
-                 const uint16_t* new_v, const int64_t* new_slot) {
+                 const uint16_t* new_v, const int64_t* new_slot, unsigned long long recv_wait_ns = RECV_WAIT_NS,
+                 int test_skip_merge = 0) {
   if (num_seqs < 0 || num_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
     return pkv::fail(PKV_ERR_INVALID_ARG,
                      "%s: num_seqs=%d num_heads=%d num_blocks=%d max_blocks_per_seq=%d", fn,
@@ -956,6 +963,8 @@ int decode_entry(const char* fn, const uint16_t* q, const uint16_t* k_cache, con
   if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID_ARG, "%s: scale not finite", fn);
 
   AttnParams p{};
+  p.recv_wait_ns = recv_wait_ns;
+  p.test_skip_merge = test_skip_merge;
   p.new_k = reinterpret_cast<const __half*>(new_k);
   p.new_v = reinterpret_cast<const __half*>(new_v);
   p.new_slot = new_slot;
@@ -1064,6 +1073,24 @@ int pkv_paged_attention_decode_append(const uint16_t* q, const uint16_t* key, co
                       workspace_bytes, stream, key, value, slot_mapping);
 }
 
+int pkv_test_cluster_merge_timeout(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                   int num_heads, int head_dim, int num_blocks, int max_blocks_per_seq, float scale,
+                                   int block_size, uint16_t* out, int wait_ms, void* stream) {
+  int part_tokens = 0, kernels = 0;
+  int rc = pkv_paged_attention_plan(num_seqs, num_heads, head_dim, max_blocks_per_seq, block_size, &part_tokens,
+                                    &kernels);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs <= 0 || kernels != 1 || static_cast<long long>(max_blocks_per_seq) * block_size <= part_tokens)
+    return pkv::fail(PKV_ERR_UNSUPPORTED,
+                     "pkv_test_cluster_merge_timeout: these sizes do not merge partitions inside clusters");
+  if (wait_ms < 1 || wait_ms > 2000)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_test_cluster_merge_timeout: wait_ms %d outside [1, 2000]", wait_ms);
+  return decode_entry("pkv_test_cluster_merge_timeout", q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                      num_heads, head_dim, num_blocks, max_blocks_per_seq, scale, block_size, out, nullptr, 0,
+                      stream, nullptr, nullptr, nullptr, 1000000ull * static_cast<unsigned long long>(wait_ms), 1);
+}
+
 size_t pkv_paged_attention_shared_prefix_workspace_size(int num_seqs, int num_heads, int head_dim,
                                                         int max_blocks_per_seq, int block_size) {
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 || block_size <= 0) return 0;
@@ -1111,6 +1138,7 @@ int pkv_paged_attention_decode_shared_prefix(const uint16_t* q, const uint16_t* 
     return pkv::fail(PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode_shared_prefix: scale must be finite and positive");
 
   AttnParams p{};
+  p.recv_wait_ns = RECV_WAIT_NS;
   p.q = reinterpret_cast<const __half*>(q);
   p.k = reinterpret_cast<const __half*>(k_cache);
   p.v = reinterpret_cast<const __half*>(v_cache);

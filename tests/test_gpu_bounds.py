@@ -7,11 +7,15 @@
 * The binding refuses a CUDA tensor that is not on the current device, on the host, before any
   kernel runs (the library launches on the current device; another device's memory would be
   read as a peer's).
+* Failure detection without a fault: the one wait of one CTA on others (partition 0 of a cluster
+  waiting for the other partitions' partial results) is bounded; a test entry makes it run out on
+  a phase nothing completes, and the host reads the recorded code with the context still usable.
 """
 import numpy as np
 import pytest
 import torch
 
+from oracle import attention as oracle_attention
 from paged_kv_cache_73_gb300 import binding as pkv
 from paged_kv_cache_73_gb300 import workloads as wl
 
@@ -73,3 +77,29 @@ def test_binding_refuses_a_tensor_on_another_device(cuda_device, monkeypatch):
     assert torch.isnan(out).all()                                   # nothing ran
     pkv.paged_attention_decode(q, k, v, tables, lens, w.scale, w.block_size, out=out)
     assert pkv.device_error() == 0 and torch.isfinite(out).all()
+
+
+def test_cluster_merge_wait_runs_out_and_is_reported(cuda_device):
+    # failure detection without a fault: partition 0's bounded wait for the other partitions of its
+    # cluster runs out on a phase nothing completes (they skip their stores and arrivals in this
+    # test entry); the host reads PKV_DEV_WAIT_TIMEOUT and the context stays usable
+    w = wl.custom(84, [2000, 700, 1500, 64], num_heads=8, head_dim=128, block_size=16)
+    q, k, v = w.q(cuda_device), *w.pools(cuda_device)
+    tables = torch.from_numpy(w.block_tables).to(cuda_device)
+    lens = torch.from_numpy(w.context_lens).to(cuda_device)
+    assert pkv.paged_attention_plan(4, 8, 128, w.max_blocks_per_seq, 16) == (256, 1)   # 8 partitions, on chip
+    out = torch.empty_like(q)
+    lib = pkv.load()
+    assert lib.pkv_test_cluster_merge_timeout(q.data_ptr(), k.data_ptr(), v.data_ptr(), tables.data_ptr(),
+                                              lens.data_ptr(), 4, 8, 128, k.shape[0], w.max_blocks_per_seq,
+                                              w.scale, 16, out.data_ptr(), 100, None) == pkv.PKV_OK
+    assert pkv.device_error() == 5                                   # PKV_DEV_WAIT_TIMEOUT
+    good = pkv.paged_attention_decode(q, k, v, tables, lens, w.scale, 16)
+    assert pkv.device_error() == 0
+    kc, vc, tabs, lens_h = w.compact_pools([0, 1, 2, 3])
+    ref = oracle_attention.paged_decode_attention(w.q("cpu").numpy(), kc.numpy(), vc.numpy(), tabs, lens_h, w.scale)
+    assert float(np.max(np.abs(good.cpu().numpy().astype(np.float64) - ref))) <= 2e-3
+    # sizes that do not merge on chip are refused
+    assert lib.pkv_test_cluster_merge_timeout(q.data_ptr(), k.data_ptr(), v.data_ptr(), tables.data_ptr(),
+                                              lens.data_ptr(), 4, 8, 128, k.shape[0], 1, w.scale, 16,
+                                              out.data_ptr(), 100, None) == pkv.PKV_ERR_UNSUPPORTED
