@@ -99,11 +99,9 @@ REF_MAX_KV_BYTES = 2.5e9                                # the oracle arm samples
 # keyed by (workload, sha256 of the attention source it was taken on); a changed kernel reports
 # null until it is captured again.
 NCU_TRAFFIC = {
-    # the headline step's fused call: partition kernel 1,373,098,500 B read + 4,771,328 B written
-    # (the appended rows included), merge kernel 1,281,000 B read (means of two launches each;
-    # captured on source cf159d0c..., which differs from this key's source in the file's header
-    # comment only)
-    ("opt13b+append", "f2a3376216bf30f8b9d5583c6cbba20976d24425f111c3e83ae78c6095e61cb6"): 1_379_150_828,
+    # the headline step's fused call: partition kernel 1,373,184,500 B read + 4,619,648 B written
+    # (the appended rows included), merge kernel 1,280,500 B read (means of two launches each)
+    ("opt13b+append", "48a69f077e356c1d7cd6f140b28e9c9ab3ed98cf570ad35716423b448022a14e"): 1_379_084_648,
 }
 
 WORKLOADS = ("opt13b", "tiny", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity",
