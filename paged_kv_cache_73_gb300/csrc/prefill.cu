@@ -202,6 +202,10 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+// Brings a tensor map (a kernel parameter) into the TMA unit's descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait_parity(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -454,17 +458,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
 
   if (warp == 9 || warp == 10) {
     // ---------------- loads: warp 9 gathers K tiles, warp 10 V tiles ----------------
+    // Lane b handles the tile's b-th block: it issues that block's TMA boxes itself (the lanes'
+    // copies go out together), and its table entry for the next tile is read while this tile's
+    // copies are issued.
     const bool is_k = warp == 9;
     const __half* pool = is_k ? p.k : p.v;
     const CUtensorMap* map = is_k ? &p.tmap_k : &p.tmap_v;
+    if (lane == 0 && p.use_tma) prefetch_tensormap(map);
     const int32_t* table = p.tables + static_cast<size_t>(trow) * p.max_blocks;
     constexpr int ROWS = 32 / CPR;                            // rows per warp-wide cp.async
     const int c = lane % CPR, rsub = lane / CPR;              // this lane's chunk and row offset
     const int nb = TC_BN >> lb;                               // blocks per tile (2..16)
     const uint32_t all_blocks = (nb == 32 ? 0xffffffffu : (1u << nb) - 1u);
+    auto entry = [&](int j) {                                 // this lane's table entry for tile j
+      const int t0 = j * TC_BN + (lane << lb);
+      return lane < nb && t0 < ctx ? __ldg(table + (t0 >> lb)) : -1;
+    };
+    int next_entry = entry(0);
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % NS;
+      // lane b < nb maps the tile's b-th block: phys = -1 past the context or for a bad entry
+      const int t0 = j * TC_BN + (lane << lb);
+      const bool in_ctx = lane < nb && t0 < ctx;
+      int phys = next_entry;
+      if (j + 1 < n_tiles) next_entry = entry(j + 1);
+      if (in_ctx && (phys < 0 || phys >= p.num_blocks)) bad = 1;
+      if (!in_ctx || phys < 0 || phys >= p.num_blocks) phys = -1;
       // slot j%4 is free once the MMAs of tile j-4 that read it are done
       if (j >= NS && !wait(is_k ? k_free(st) : v_free(st), (j / NS - 1) & 1)) {
         failed = true;
@@ -472,28 +492,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) paged_prefill_tc_kernel(const _
       }
       const uint32_t full = is_k ? k_full(st) : v_full(st);
       const uint32_t dst = (is_k ? sk : sv) + st * C::KV_BYTES;
-      // lane b < nb maps the tile's b-th block: phys = -1 past the context or for a bad entry
-      const int t0 = j * TC_BN + (lane << lb);
-      int phys = -1;
-      if (lane < nb && t0 < ctx) {
-        phys = table[t0 >> lb];
-        if (phys < 0 || phys >= p.num_blocks) {
-          bad = 1;
-          phys = -1;
-        }
-      }
       // whole blocks inside the context arrive by TMA (B >= 8, so each lands on a 1024-byte
       // boundary of the swizzled tile); the block holding the context's end, blocks past it and
       // bad entries are copied (or zero-filled) by cp.async
-      const uint32_t tma_mask = __ballot_sync(0xffffffffu, p.use_tma && lane < nb && phys >= 0 && t0 + B <= ctx);
+      const bool by_tma = p.use_tma && phys >= 0 && t0 + B <= ctx;
+      const uint32_t tma_mask = __ballot_sync(0xffffffffu, by_tma);
       if (lane == 0 && tma_mask) mbar_expect_tx(full, static_cast<uint32_t>(__popc(tma_mask)) * B * D * 2);
-      for (int b = 0; b < nb; ++b) {
-        const int pb = __shfl_sync(0xffffffffu, phys, b);
-        if (lane == 0 && ((tma_mask >> b) & 1u)) {
+      __syncwarp();
+      if (by_tma) {
 #pragma unroll
-          for (int half = 0; half < D / 64; ++half)
-            tma_load_3d(dst + half * (TC_BN * 128) + b * B * 128, map, half * 64, h * B, pb, full);
-        }
+        for (int half = 0; half < D / 64; ++half)
+          tma_load_3d(dst + half * (TC_BN * 128) + lane * B * 128, map, half * 64, h * B, phys, full);
       }
       if (tma_mask != all_blocks) {
         for (int r0 = 0; r0 < TC_BN; r0 += ROWS) {
