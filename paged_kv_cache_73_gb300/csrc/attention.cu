@@ -101,8 +101,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   return false;
 }
 // ---- thread-block cluster helpers (the partitions of one (sequence, head) as one cluster) -------
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+// Relaxed arrival: what the other CTAs need before they reach this one's shared memory is the
+// receiving barrier's initialisation, which its own fence (fence.mbarrier_init.release.cluster)
+// publishes.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
@@ -386,14 +389,15 @@ __global__ void __launch_bounds__(Cfg<D, R>::NW * 32, 3) paged_attention_partiti
   const int ctx = ctx_full - start;                    // tokens of the range
   const int nparts = bad_range ? 1 : (ctx + p.part_tokens - 1) / p.part_tokens;
   if constexpr (CLUSTER) {
-    // Partition 0 counts one arrival per thread of every other partition with tokens; the cluster
-    // barrier makes that initialisation visible before any of them arrives.  Every thread of every
-    // CTA arrives here and waits once before it exits or reaches another CTA's shared memory.
+    // Partition 0 counts one arrival per thread of every other partition with tokens; its fence
+    // publishes that initialisation and the cluster barrier orders it before any of them arrives.
+    // Every thread of every CTA arrives here and waits once before it exits or reaches another
+    // CTA's shared memory.
     if (part == 0 && tid == 0 && nparts > 1) {
       mbar_init(recv_bar, NW * 32 * (nparts - 1));
       fence_mbar_init();
     }
-    cluster_arrive_release();
+    cluster_arrive_relaxed();
     if (part >= nparts) {
       cluster_wait_acquire();
       return;
