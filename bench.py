@@ -94,14 +94,15 @@ ROOFLINE_LAUNCHES = 200                                 # attention calls timed 
 SUSTAINED_S = 1.0                                       # seconds of back-to-back steps, at least
 CONFIG_STEPS = 50                                       # timed steps of each entry of `configs`
 REF_MAX_KV_BYTES = 2.5e9                                # the oracle arm samples batches larger than this
+REF_WALL_S = 150.0                                      # the oracle arm's whole run (warm-up included), about
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one paged-attention call from an ncu capture,
 # keyed by (workload, sha256 of the attention source it was taken on); a changed kernel reports
 # null until it is captured again.
 NCU_TRAFFIC = {
-    # the headline step's fused call: partition kernel 1,373,184,500 B read + 4,619,648 B written
-    # (the appended rows included), merge kernel 1,280,500 B read (means of two launches each)
-    ("opt13b+append", "48a69f077e356c1d7cd6f140b28e9c9ab3ed98cf570ad35716423b448022a14e"): 1_379_084_648,
+    # the headline step's fused call: partition kernel 1,373,096,704 B read + 4,926,208 B written
+    # (the appended rows included), merge kernel 1,280,384 B read (means of two launches each)
+    ("opt13b+append", "39ce661f5a57a33b74881bb7a29140e0350bb767558bf3a41d17c172630552dc"): 1_379_303_296,
 }
 
 WORKLOADS = ("opt13b", "tiny", "parallel_sampling", "parallel_sampling_cow", "shared_prefix", "capacity",
@@ -1458,6 +1459,23 @@ def reference_sample(w):
                          f"{REF_MAX_KV_BYTES / 1e9:.1f} GB of K/V)"
 
 
+def fit_reference_sample(w, seqs, step_s, runs, budget_s=REF_WALL_S):
+    """The sequences of `seqs` (in order) the oracle arm keeps so that `runs` steps take about
+    `budget_s` seconds, given that one step over all of `seqs` took `step_s`: a share of the K/V
+    bytes in proportion, at least one sequence.  All of `seqs` when they fit."""
+    if runs * step_s <= budget_s or len(seqs) <= 1:
+        return list(seqs)
+    keep = budget_s / (runs * step_s)
+    lens = [int(w.context_lens[s]) for s in seqs]
+    cap, out, acc = keep * sum(lens), [], 0
+    for s, n in zip(seqs, lens):
+        if out and acc + n > cap:
+            break
+        out.append(s)
+        acc += n
+    return out
+
+
 def run_reference(args, rank):
     """The oracle, as it stands, on the host cores: each step the new-token writes and fp64
     attention over the batch, whose tables and slots the oracle's block manager builds."""
@@ -1470,7 +1488,16 @@ def run_reference(args, rank):
     w = x0["w"]
     seqs, what = reference_sample(w)
     sample = prepare_cpu_sample(w, seqs, x0["slots"], x0["pairs"], seed)   # generated once, untimed
-    for _ in range(args.warmup):
+    # the first warm-up step also sizes the sample: the whole run stays within about REF_WALL_S
+    runs = max(args.warmup, 1) + args.steps
+    kept = fit_reference_sample(w, seqs, cpu_sample_seconds(sample), runs)
+    if len(kept) < len(seqs):
+        seqs = kept
+        what = f"{len(seqs)} of the {w.num_seqs} sequences (all {w.num_heads} heads), so that {runs} steps " \
+               f"fit in about {REF_WALL_S:.0f} s"
+        sample = prepare_cpu_sample(w, seqs, x0["slots"], x0["pairs"], seed)
+        cpu_sample_seconds(sample)
+    for _ in range(max(args.warmup, 1) - 1):
         cpu_sample_seconds(sample)
     secs = 0.0
     for _ in range(args.steps):

@@ -148,3 +148,16 @@ def test_step_form_follows_the_batch_sharing():
     assert bench.use_fused(auto, opt) and not bench.use_fused(auto, shared)
     assert bench.use_fused(_args("--step", "fused"), shared)
     assert not bench.use_fused(_args("--step", "unfused"), opt) and not bench.use_fused(_args("--unfused"), opt)
+
+
+def test_reference_sample_fits_the_wall_budget():
+    # the oracle arm keeps the whole batch while the run fits its budget, else a share of the
+    # batch's K/V in proportion (at least one sequence), so that a run with the default step count
+    # still ends within minutes
+    w = type("W", (), {"context_lens": np.array([100, 200, 300, 400])})()
+    seqs = [0, 1, 2, 3]
+    assert bench.fit_reference_sample(w, seqs, step_s=0.5, runs=25, budget_s=150) == seqs
+    kept = bench.fit_reference_sample(w, seqs, step_s=0.5, runs=1000, budget_s=150)   # 30 % of the bytes
+    assert kept == [0, 1]
+    assert sum(w.context_lens[kept]) <= 0.3 * 1000 + 1e-9
+    assert bench.fit_reference_sample(w, seqs, step_s=10.0, runs=1000, budget_s=150) == [0]
