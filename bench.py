@@ -1493,8 +1493,8 @@ def run_reference(args, rank):
     kept = fit_reference_sample(w, seqs, cpu_sample_seconds(sample), runs)
     if len(kept) < len(seqs):
         seqs = kept
-        what = f"{len(seqs)} of the {w.num_seqs} sequences (all {w.num_heads} heads), so that {runs} steps " \
-               f"fit in about {REF_WALL_S:.0f} s"
+        what = f"{len(seqs)} of the {w.num_seqs} sequences (all {w.num_heads} heads; sized so that {runs} " \
+               f"steps take about {REF_WALL_S:.0f} s)"
         sample = prepare_cpu_sample(w, seqs, x0["slots"], x0["pairs"], seed)
         cpu_sample_seconds(sample)
     for _ in range(max(args.warmup, 1) - 1):
